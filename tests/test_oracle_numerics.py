@@ -1,0 +1,123 @@
+"""Pins for the oracle's numeric building blocks, against library routines,
+closed forms, invariants and brute force (never against a retyped formula)."""
+import math
+
+import numpy as np
+import pytest
+
+from oracle import model as M
+
+torch = pytest.importorskip("torch")
+rng = np.random.default_rng(1234)
+
+
+def test_bf16_matches_torch_cast_on_float32_values():
+    x = rng.standard_normal(5000).astype(np.float32) * np.float32(5.0)
+    # exact ties between neighbouring bfloat16 values, both parities
+    ties = np.array([1 + 2 ** -8, 1 + 3 * 2 ** -8, -(1 + 2 ** -8), 3 * 2 ** -9 * (1 + 2 ** -8)])
+    x = np.concatenate([x.astype(np.float64), ties])
+    ref = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(M.bf16(x), ref)
+    assert M.bf16(1 + 2 ** -8) == 1.0                   # tie -> even (1.0)
+    assert M.bf16(1 + 3 * 2 ** -8) == 1 + 2 ** -6       # tie -> even (1 + 2^-6)
+    assert M.bf16(0.0) == 0.0
+
+
+def test_bf16_direct_from_float64_no_double_rounding():
+    # 1 + 2^-8 + 2^-30 is just above the tie: nearest bf16 is 1 + 2^-7.
+    # Through float32 it would first round to the tie 1 + 2^-8, then to even 1.0.
+    x = 1 + 2 ** -8 + 2 ** -30
+    assert M.bf16(x) == 1 + 2 ** -7
+
+
+def test_rms_norm_matches_torch():
+    x = rng.standard_normal((7, 96))
+    g = rng.standard_normal(96)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (96,), torch.from_numpy(g), eps=1e-5)
+    np.testing.assert_allclose(M.rms_norm(x, g, 1e-5), ref.numpy(), rtol=1e-13, atol=1e-14)
+
+
+def test_linear_matches_brute_force():
+    x = rng.standard_normal((3, 5))
+    w = rng.standard_normal((4, 5)).astype(np.float32)
+    b = rng.standard_normal(4)
+    ref = np.array([[sum(float(x[i, k]) * float(w[o, k]) for k in range(5)) + b[o] for o in range(4)]
+                    for i in range(3)])
+    np.testing.assert_allclose(M.linear(x, w, b, block=3), ref, rtol=1e-14)
+
+
+def test_rope_closed_form_small():
+    # d_h = 4: pair (0, 2) rotates at theta^0 = 1 rad per position, pair (1, 3) at theta^(-1/2).
+    theta = 100.0
+    x = np.array([[[1.0, 2.0, 3.0, 4.0]]])
+    out = M.rope(x, np.array([3]), theta)[0, 0]
+    a0, a1 = 3.0, 3.0 / 10.0
+    exp = [1 * math.cos(a0) - 3 * math.sin(a0), 2 * math.cos(a1) - 4 * math.sin(a1),
+           3 * math.cos(a0) + 1 * math.sin(a0), 4 * math.cos(a1) + 2 * math.sin(a1)]
+    np.testing.assert_allclose(out, exp, rtol=1e-14)
+
+
+def test_rope_complex_form_and_invariants():
+    n, h, d_h, theta = 9, 3, 16, 10000.0
+    x = rng.standard_normal((n, h, d_h))
+    pos = rng.integers(0, 5000, n)
+    out = M.rope(x, pos, theta)
+    # same rotation written as complex multiplication of (x_i + i x_{i+d/2})
+    z = x[..., : d_h // 2] + 1j * x[..., d_h // 2:]
+    freq = theta ** (-np.arange(d_h // 2) * 2.0 / d_h)
+    zr = z * np.exp(1j * pos[:, None, None] * freq[None, None, :])
+    np.testing.assert_allclose(out, np.concatenate([zr.real, zr.imag], axis=-1), rtol=1e-9, atol=1e-12)
+    # position 0 is the identity; rotation preserves norms
+    np.testing.assert_array_equal(M.rope(x, np.zeros(n, int), theta), x)
+    np.testing.assert_allclose(np.linalg.norm(out, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)
+    # relative-position property: <R(p) q, R(p') k> depends only on p - p'
+    q = rng.standard_normal((1, 1, d_h))
+    k = rng.standard_normal((1, 1, d_h))
+    dots = [float((M.rope(q, np.array([p + 7]), theta) * M.rope(k, np.array([p]), theta)).sum())
+            for p in (0, 13, 400, 3001)]
+    np.testing.assert_allclose(dots, dots[0], rtol=1e-9)
+
+
+def test_attention_matches_torch_sdpa_gqa():
+    n, n_q, n_kv, d_h = 37, 8, 2, 16
+    q = rng.standard_normal((n, n_q, d_h))
+    k = rng.standard_normal((n, n_kv, d_h))
+    v = rng.standard_normal((n, n_kv, d_h))
+    pos = np.arange(n)
+    got = M.causal_gqa_attention(q, k, v, pos, pos)
+    tq, tk, tv = (torch.from_numpy(a).permute(1, 0, 2)[None] for a in (q, k, v))
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, is_causal=True, enable_gqa=True)
+    np.testing.assert_allclose(got, ref[0].permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_attention_brute_force_decode_rows():
+    # one query at position 5 over keys 0..7 (keys 6, 7 must be masked)
+    n_q, n_kv, d_h = 4, 2, 3
+    q = rng.standard_normal((1, n_q, d_h))
+    k = rng.standard_normal((8, n_kv, d_h))
+    v = rng.standard_normal((8, n_kv, d_h))
+    got = M.causal_gqa_attention(q, k, v, np.array([5]), np.arange(8))
+    for h in range(n_q):
+        kv = h // 2
+        s = [sum(q[0, h, c] * k[t, kv, c] for c in range(d_h)) / math.sqrt(d_h) for t in range(6)]
+        e = [math.exp(a - max(s)) for a in s]
+        ref = [sum(e[t] * v[t, kv, c] for t in range(6)) / sum(e) for c in range(d_h)]
+        np.testing.assert_allclose(got[0, h], ref, rtol=1e-12)
+
+
+def test_attention_zero_query_is_causal_running_mean():
+    n, d_h = 6, 4
+    v = rng.standard_normal((n, 1, d_h))
+    out = M.causal_gqa_attention(np.zeros((n, 2, d_h)), rng.standard_normal((n, 1, d_h)), v,
+                                 np.arange(n), np.arange(n))
+    run_mean = np.cumsum(v[:, 0], axis=0) / np.arange(1, n + 1)[:, None]
+    np.testing.assert_allclose(out[:, 0], run_mean, rtol=1e-13)
+    np.testing.assert_allclose(out[:, 1], run_mean, rtol=1e-13)
+
+
+def test_silu_special_values():
+    assert M.silu(np.float64(0.0)) == 0.0
+    np.testing.assert_allclose(M.silu(np.float64(40.0)), 40.0, rtol=1e-15)
+    np.testing.assert_allclose(M.silu(np.float64(1.0)), 1.0 / (1.0 + math.exp(-1.0)), rtol=1e-15)
+    x = torch.linspace(-8, 8, 101, dtype=torch.float64)
+    np.testing.assert_allclose(M.silu(x.numpy()), torch.nn.functional.silu(x).numpy(), rtol=1e-14)
