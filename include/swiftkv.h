@@ -1,0 +1,217 @@
+/*
+ * swiftkv.h — C ABI of the SwiftKV prefill-skipping library for one NVIDIA GB300 (sm_103a).
+ *
+ * The method ("SwiftKV: Fast Prefill-Optimized Inference with Knowledge-Preserving
+ * Model Transformation", section 3.2 and section 3.4 "The SwiftKV Rewiring Mechanism",
+ * Eq. 2; the paper's section 3.5 "Optimized Implementation for Inference"):
+ * prompt tokens run the decoder only through layer l; the K/V caches of every
+ * later layer j > l are projected from x_{l+1}, the output of layer l, as
+ * KV_j = W_KV^j x_{l+1}; with AcrossKV each group of g consecutive skipped
+ * layers shares one cache projected with the group's first layer's W_KV; the
+ * skipped layers' Q/attention/O/MLP never run on prompt tokens, except for the
+ * last token of each prompt, which runs every layer to produce the logits of
+ * the first output token.
+ *
+ * Conventions
+ *  - l counts full layers (layers 1..l run in full); 1 <= l <= L. l == L is the
+ *    ordinary model. acrosskv_group g >= 1 must divide L - l.
+ *  - Matrices are bfloat16 bit patterns (uint16_t) in nn.Linear layout [out][in],
+ *    row-major. Gains and biases are float.
+ *  - "device" pointers are CUDA device memory of the current device; "host"
+ *    pointers are ordinary (pageable or pinned) host memory.
+ *  - All GPU work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) without synchronising, unless a function says otherwise. Host
+ *    arrays are fully read before the call returns.
+ *  - Return value: SWIFTKV_OK (0) or a negative swiftkv_error. Errors never abort
+ *    the process and never trap on the device; swiftkv_last_error() describes the
+ *    last failure of the calling thread.
+ *  - Data-dependent checks that need device data (token ids < vocab, page ids <
+ *    num_pages) are done by the kernels: a violation sets a bit in the model's
+ *    device status word (swiftkv_status) and the offending read/write is skipped
+ *    or clamped in bounds.
+ */
+#ifndef SWIFTKV_H
+#define SWIFTKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* swiftkv_stream; /* == cudaStream_t */
+
+enum swiftkv_error {
+  SWIFTKV_OK = 0,
+  SWIFTKV_EINVAL = -1,         /* null pointer, bad size or config field */
+  SWIFTKV_EINVAL_L = -2,       /* l outside [1, L], or different from the loaded model's */
+  SWIFTKV_EINVAL_GROUP = -3,   /* g < 1, (L - l) % g != 0, or different from the model's */
+  SWIFTKV_EINVAL_SEQLENS = -4, /* cu_seqlens not starting at 0 / a prompt shorter than 1 token */
+  SWIFTKV_ENO_PAGES = -5,      /* a sequence needs more pages than its block-table row holds */
+  SWIFTKV_EOOM = -6,           /* device allocation failed */
+  SWIFTKV_ECUDA = -7,          /* a CUDA runtime call or launch failed */
+  SWIFTKV_EDEVICE = -8,        /* reserved: device status word reported a violation */
+  SWIFTKV_EUNSUPPORTED = -9,   /* shape outside what the kernels implement */
+  SWIFTKV_ESTATE = -10         /* weights not (fully) loaded */
+};
+
+/* Bits of the device status word. */
+enum swiftkv_status_bits {
+  SWIFTKV_STATUS_BAD_TOKEN = 1, /* a token id outside [0, vocab): row 0 was used */
+  SWIFTKV_STATUS_BAD_PAGE = 2   /* a block-table entry outside [0, num_pages): access skipped */
+};
+
+/* Shape of the decoder (Llama / Qwen family: RMSNorm, GQA attention with RoPE,
+ * SwiGLU MLP, untied LM head). Supported: d_head in {64, 128}; n_q % n_kv == 0;
+ * d, n_q*d_head multiples of 128; vocab a multiple of 128. */
+typedef struct {
+  int L;            /* decoder layers */
+  int d;            /* model width */
+  int n_q;          /* query heads */
+  int n_kv;         /* key/value heads */
+  int d_head;       /* head dim */
+  int ffn;          /* SwiGLU intermediate width */
+  int vocab;        /* vocabulary size */
+  int qkv_bias;     /* 1: Q/K/V projections carry a bias (added before RoPE) */
+  float rope_theta; /* RoPE base; rotate-half pairs (i, i + d_head/2), no scaling */
+  float rms_eps;    /* RMSNorm epsilon */
+} swiftkv_model_config;
+
+/* One decoder layer's weights in host memory. */
+typedef struct {
+  const float* gamma_attn; /* [d] input RMSNorm gain */
+  const uint16_t* wq;      /* [n_q*d_head][d] */
+  const uint16_t* wk;      /* [n_kv*d_head][d] */
+  const uint16_t* wv;      /* [n_kv*d_head][d] */
+  const float* bq;         /* [n_q*d_head]  (NULL unless qkv_bias) */
+  const float* bk;         /* [n_kv*d_head] (NULL unless qkv_bias) */
+  const float* bv;         /* [n_kv*d_head] (NULL unless qkv_bias) */
+  const uint16_t* wo;      /* [d][n_q*d_head] */
+  const float* gamma_mlp;  /* [d] */
+  const uint16_t* w_gate;  /* [ffn][d] */
+  const uint16_t* w_up;    /* [ffn][d] */
+  const uint16_t* w_down;  /* [d][ffn] */
+} swiftkv_layer_weights;
+
+/* All weights in host memory. */
+typedef struct {
+  const uint16_t* embed;              /* [vocab][d] */
+  const float* gamma_final;           /* [d] */
+  const uint16_t* lm_head;            /* [vocab][d] */
+  const swiftkv_layer_weights* layers; /* [L] */
+} swiftkv_host_weights;
+
+/* Paged KV cache, owned by the caller (device memory).
+ * There are num_caches = swiftkv_cache_count(L, l, g) caches: caches 0..l-1
+ * belong to the full layers, cache l + i to the i-th group of skipped layers.
+ * Each cache has a K pool and a V pool, bf16 [num_pages][n_kv][page_size][d_head]:
+ * one (page, head) block of page_size * d_head elements is contiguous.
+ * Token at position p of sequence s lives in page block_table[s][p / page_size],
+ * row p % page_size. */
+typedef struct {
+  void* const* k_pool;        /* host array [num_caches] of device pointers */
+  void* const* v_pool;        /* host array [num_caches] of device pointers */
+  int num_caches;
+  int num_pages;
+  int page_size;              /* must be 16 */
+  const int32_t* block_table; /* device int32 [num_seqs][max_pages_per_seq] */
+  int max_pages_per_seq;
+} swiftkv_kv_pages;
+
+typedef struct swiftkv_model swiftkv_model; /* opaque; owns device weights + workspace */
+
+/* Number of KV caches for (L, l, g): l + (L - l)/g ("SwiftKV" summary, section 3.4
+ * AcrossKV, "Memory reduction"). Negative swiftkv_error for invalid arguments. */
+int swiftkv_cache_count(int L, int l, int acrosskv_group);
+
+/* Creates an empty model for (cfg, l, g) on the current device. Device memory for
+ * all weights is allocated here. The W_KV packing of the skipped layers depends on
+ * (l, g), so both are fixed for the model's lifetime. */
+int swiftkv_model_create(const swiftkv_model_config* cfg, int l, int acrosskv_group,
+                         swiftkv_model** out);
+
+/* Copies layer j's (0-based) weights from host memory, packing them for the kernels:
+ * Q/K/V concatenated (full layers), gate/up interleaved in 64-row blocks, and for a
+ * skipped layer that represents an AcrossKV group, its W_K/W_V (rows scaled by its
+ * gamma_attn, rounded to bf16) into the wide W_KV of all groups. Synchronises `stream`. */
+int swiftkv_load_layer(swiftkv_model* m, int j, const swiftkv_layer_weights* w,
+                       swiftkv_stream stream);
+
+/* Copies embedding, final gain and LM head from host memory. Synchronises `stream`. */
+int swiftkv_load_globals(swiftkv_model* m, const uint16_t* embed, const float* gamma_final,
+                         const uint16_t* lm_head, swiftkv_stream stream);
+
+/* swiftkv_model_create + swiftkv_load_layer for every layer + swiftkv_load_globals.
+ * On failure *out is NULL and nothing is leaked. */
+int swiftkv_load_weights(const swiftkv_model_config* cfg, const swiftkv_host_weights* w, int l,
+                         int acrosskv_group, swiftkv_stream stream, swiftkv_model** out);
+
+/* SwiftKV prefill of num_seqs packed prompts.
+ *   tokens      device int32 [T], T = cu_seqlens[num_seqs]; prompt s is
+ *               tokens[cu_seqlens[s] .. cu_seqlens[s+1]), positions 0.. within it
+ *   cu_seqlens  HOST int32 [num_seqs + 1], cu_seqlens[0] == 0, every prompt >= 1 token
+ *   l, acrosskv_group  must equal the model's
+ *   kv          caches to fill (all num_caches of them, positions 0..n_s-1 of each sequence)
+ *   logits      device float [num_seqs][vocab]: logits of each prompt's last token
+ * Workspace grows on demand (cudaMalloc) and is kept by the model. num_seqs == 0 is a no-op. */
+int swiftkv_prefill(swiftkv_model* m, const int32_t* tokens, const int32_t* cu_seqlens,
+                    int num_seqs, int l, int acrosskv_group, const swiftkv_kv_pages* kv,
+                    float* logits, swiftkv_stream stream);
+
+/* swiftkv_prefill with HOST tokens [T] and HOST logits [num_seqs][vocab]: copies in,
+ * runs, copies out and synchronises `stream` before returning. */
+int swiftkv_prefill_host(swiftkv_model* m, const int32_t* tokens_host, const int32_t* cu_seqlens,
+                         int num_seqs, int l, int acrosskv_group, const swiftkv_kv_pages* kv,
+                         float* logits_host, swiftkv_stream stream);
+
+/* One decode token for each of `batch` sequences ("SwiftKV" summary, section 3.2:
+ * decode tokens run every layer). Sequence b holds seq_lens[b] cached tokens; its
+ * new token (position seq_lens[b]) writes its K/V at that position into every cache
+ * (for skipped layers projected from its own x_{l+1}, like a prompt token), attends
+ * to positions 0..seq_lens[b], and produces logits and the greedy next token.
+ *   tokens      device int32 [batch]
+ *   seq_lens    HOST int32 [batch]
+ *   logits      device float [batch][vocab]
+ *   next_tokens device int32 [batch]: argmax of the logits, lowest id on ties (may be NULL) */
+int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* seq_lens,
+                        int batch, const swiftkv_kv_pages* kv, float* logits,
+                        int32_t* next_tokens, swiftkv_stream stream);
+
+/* Reads (synchronously) the device status word; clears it when clear != 0.
+ * Returns the swiftkv_status_bits that are set, or a negative swiftkv_error. */
+int swiftkv_status(swiftkv_model* m, int clear);
+
+/* Bytes of device memory the model holds for weights and for workspace. */
+int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspace_bytes);
+
+/* Per-kernel-class timing of the model's own launches, for roofline reporting.
+ * swiftkv_profile_begin clears the records and, until swiftkv_profile_end, brackets
+ * every launch the model enqueues with a pair of CUDA events recorded on the launch's
+ * stream. swiftkv_profile_end synchronises on those events, aggregates them by class
+ * and writes up to max_entries entries; it returns the number of classes (or an error).
+ *   name     kernel class ("gemm_layers", "gemm_wide_kv", "attn_prefill", "rmsnorm", ...)
+ *   calls    launch sites recorded; kernels: CUDA kernels they launched
+ *   ms       summed event time; flops / bytes: summed algorithmic work of those calls */
+typedef struct {
+  char name[32];
+  int calls;
+  int kernels;
+  double ms;
+  double flops;
+  double bytes;
+} swiftkv_profile_entry;
+
+int swiftkv_profile_begin(swiftkv_model* m);
+int swiftkv_profile_end(swiftkv_model* m, swiftkv_profile_entry* out, int max_entries);
+
+/* Message for the last failed call on this thread ("" if none). */
+const char* swiftkv_last_error(void);
+
+/* Frees the model and everything it allocated. NULL is ignored. */
+void swiftkv_free(swiftkv_model* m);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SWIFTKV_H */

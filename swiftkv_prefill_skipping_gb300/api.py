@@ -1,0 +1,172 @@
+"""Torch-facing layer over the C ABI: weights in, paged caches, prefill, decode.
+
+PyTorch provides device memory and streams only; all computation happens in
+libswiftkv.so. Every call checks the library's return code and raises
+``SwiftKVError`` on failure.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(a) -> Optional[int]:
+    if a is None:
+        return None
+    if isinstance(a, np.ndarray):
+        assert a.flags["C_CONTIGUOUS"]
+        return a.ctypes.data
+    assert a.is_contiguous()
+    return a.data_ptr()
+
+
+@dataclass
+class Shape:
+    L: int
+    d: int
+    n_q: int
+    n_kv: int
+    d_h: int
+    ffn: int
+    vocab: int
+    rope_theta: float
+    rms_eps: float = 1e-5
+    qkv_bias: bool = False
+
+    @classmethod
+    def of(cls, s):
+        return cls(L=s.L, d=s.d, n_q=s.n_q, n_kv=s.n_kv, d_h=s.d_h, ffn=s.ffn, vocab=s.vocab,
+                   rope_theta=s.rope_theta, rms_eps=s.rms_eps, qkv_bias=s.qkv_bias)
+
+    def config(self) -> B.ModelConfig:
+        return B.ModelConfig(self.L, self.d, self.n_q, self.n_kv, self.d_h, self.ffn, self.vocab,
+                             int(self.qkv_bias), self.rope_theta, self.rms_eps)
+
+
+class Model:
+    """A SwiftKV model on the current CUDA device, packed for (l, g)."""
+
+    def __init__(self, shape, l: int, g: int = 1):
+        self.shape = Shape.of(shape)
+        self.l, self.g = l, g
+        self.num_caches = B.cache_count(self.shape.L, l, g)
+        self._cfg = self.shape.config()
+        h = C.c_void_p()
+        B.check(B.lib().swiftkv_model_create(C.byref(self._cfg), l, g, C.byref(h)))
+        self.handle = h
+
+    def load_layer(self, j: int, w: dict, stream=None) -> None:
+        lw = B.LayerWeights(*[_ptr(w.get(k)) for k in (
+            "gamma_attn", "wq", "wk", "wv", "bq", "bk", "bv", "wo", "gamma_mlp", "wg", "wu", "wd")])
+        B.check(B.lib().swiftkv_load_layer(self.handle, j, C.byref(lw), _stream(stream)))
+
+    def load_globals(self, w: dict, stream=None) -> None:
+        B.check(B.lib().swiftkv_load_globals(self.handle, _ptr(w["embed"]), _ptr(w["gamma_final"]),
+                                             _ptr(w["lm_head"]), _stream(stream)))
+
+    def free(self) -> None:
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            B.lib().swiftkv_free(self.handle)
+            self.handle = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+    def status(self, clear: bool = True) -> int:
+        return B.check(B.lib().swiftkv_status(self.handle, int(clear)))
+
+    def memory(self):
+        wb, sb = C.c_size_t(), C.c_size_t()
+        B.check(B.lib().swiftkv_memory(self.handle, C.byref(wb), C.byref(sb)))
+        return wb.value, sb.value
+
+
+def load_synthetic(shape, l: int, g: int = 1, seed: int = 0, gain_std: float = 0.0) -> Model:
+    """Model with the seeded synthetic weights of the shared generator (inputs only)."""
+    import synth
+    m = Model(shape, l, g)
+    for j in range(shape.L):
+        rep = j < l or (j - l) % g == 0
+        kinds = None if rep else ("wq", "wo", "wg", "wu", "wd", "gamma_attn", "gamma_mlp", "bq")
+        m.load_layer(j, synth.layer_weights(shape, j, seed=seed, gain_std=gain_std, kinds=kinds))
+    m.load_globals(synth.global_weights(shape, seed=seed, gain_std=gain_std))
+    return m
+
+
+class KVCache:
+    """Caller-owned paged KV cache: num_caches x (K, V) pools of
+    bf16 [num_pages][n_kv][16][d_h], plus a device block table."""
+
+    def __init__(self, model: Model, num_pages: int, block_table: np.ndarray, device=None):
+        s = model.shape
+        dev = device or torch.device("cuda", torch.cuda.current_device())
+        self.num_pages = num_pages
+        shape = (model.num_caches, num_pages, s.n_kv, 16, s.d_h)
+        self.k = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        self.v = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        self.block_table = torch.as_tensor(np.ascontiguousarray(block_table, dtype=np.int32), device=dev)
+        self._kp = (C.c_void_p * model.num_caches)(*[self.k[c].data_ptr() for c in range(model.num_caches)])
+        self._vp = (C.c_void_p * model.num_caches)(*[self.v[c].data_ptr() for c in range(model.num_caches)])
+        self.pages = B.KVPages(C.cast(self._kp, C.POINTER(C.c_void_p)), C.cast(self._vp, C.POINTER(C.c_void_p)),
+                               model.num_caches, num_pages, 16, self.block_table.data_ptr(),
+                               self.block_table.shape[1])
+
+    def gather(self, c: int, s: int, n: int, which: str = "k") -> torch.Tensor:
+        """Cache c's first n rows of sequence s, [n, n_kv, d_h] (test/inspection helper)."""
+        pool = self.k[c] if which == "k" else self.v[c]
+        bt = self.block_table[s]
+        pos = torch.arange(n, device=pool.device)
+        pages = bt[pos // 16].long()
+        return pool[pages, :, pos % 16, :]
+
+
+def prefill(model: Model, tokens: torch.Tensor, cu_seqlens: Sequence[int], kv: KVCache,
+            logits: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """SwiftKV prefill: fills every cache of kv, returns [P, V] last-token logits."""
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    P = len(cu) - 1
+    if logits is None:
+        logits = torch.empty((P, model.shape.vocab), dtype=torch.float32, device=kv.k.device)
+    tokens = tokens.to(torch.int32).contiguous()
+    B.check(B.lib().swiftkv_prefill(model.handle, tokens.data_ptr(), cu.ctypes.data, P, model.l, model.g,
+                                    C.byref(kv.pages), logits.data_ptr(), _stream(stream)))
+    return logits
+
+
+def prefill_host(model: Model, tokens: np.ndarray, cu_seqlens: Sequence[int], kv: KVCache,
+                 logits: Optional[np.ndarray] = None, stream=None) -> np.ndarray:
+    """prefill with host token ids and host logits (copies inside the call; synchronous)."""
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    P = len(cu) - 1
+    if logits is None:
+        logits = np.empty((P, model.shape.vocab), dtype=np.float32)
+    B.check(B.lib().swiftkv_prefill_host(model.handle, _ptr(tokens), cu.ctypes.data, P, model.l, model.g,
+                                         C.byref(kv.pages), _ptr(logits), _stream(stream)))
+    return logits
+
+
+def decode_step(model: Model, tokens: torch.Tensor, seq_lens: Sequence[int], kv: KVCache, stream=None):
+    """One decode token per sequence; returns (logits [B, V], next token ids [B])."""
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    Bsz = len(sl)
+    dev = kv.k.device
+    logits = torch.empty((Bsz, model.shape.vocab), dtype=torch.float32, device=dev)
+    nxt = torch.empty((Bsz,), dtype=torch.int32, device=dev)
+    tokens = tokens.to(torch.int32).contiguous()
+    B.check(B.lib().swiftkv_decode_step(model.handle, tokens.data_ptr(), sl.ctypes.data, Bsz, C.byref(kv.pages),
+                                        logits.data_ptr(), nxt.data_ptr(), _stream(stream)))
+    return logits, nxt

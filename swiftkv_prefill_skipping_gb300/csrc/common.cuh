@@ -1,0 +1,202 @@
+// Shared device definitions of the SwiftKV GB300 library: bf16 helpers, the
+// device status word, and the GEMM epilogues (RoPE + paged KV write, residual
+// add, SwiGLU, plain stores). Every GEMM variant (mma.sync tiles, skinny
+// split-K, tcgen05) hands its fp32 accumulators to `apply_pair`, so all of them
+// produce identical outputs for identical accumulators.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace skv {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kPageSize = 16;
+
+enum StatusBits : int { kStatusBadToken = 1, kStatusBadPage = 2 };
+
+// Epilogue kinds. Column pairing: every GEMM hands columns to the epilogue in
+// pairs (lo, hi = lo + half) inside aligned blocks of 2*half columns, where
+// half = d_head/2 for the RoPE epilogues (rotate-half partners) and 64 for the
+// others (SwiGLU gate/up partners in the 64-row interleaved packing).
+enum EpiKind : int {
+  EPI_STORE_F32 = 0,   // out_f32[m][n] = acc
+  EPI_STORE_BF16 = 1,  // out_bf16[m][n] = bf16(acc)
+  EPI_RESID = 2,       // out_f32[m][n] += acc           (fp32 residual stream)
+  EPI_SWIGLU = 3,      // out_bf16[m][64*(n/128) + n%128] = bf16(silu(acc[n]) * acc[n+64]), n%128 < 64
+  EPI_QKV = 4,         // cols [0,q_cols): Q -> RoPE -> out_bf16; then K (RoPE) and V -> paged cache
+  EPI_WIDE_KV = 5,     // per AcrossKV group: [K | V] -> RoPE on K -> paged caches cache_base + group
+};
+
+struct EpiParams {
+  int kind;
+  int M, N;                  // rows, columns of the GEMM output
+  int ldo;                   // leading dimension of out_f32 / out_bf16 (elements)
+  float* out_f32;
+  bf16* out_bf16;
+  const float* bias;         // [N] or nullptr; added before RoPE
+  int d_head, n_kv;
+  int q_cols;                // EPI_QKV: n_q * d_head (0: no Q columns)
+  const int* positions;      // [M] token position within its sequence
+  const int* slots;          // [M] page*16 + row, or -1 (invalid page: write skipped)
+  const float2* rope_tab;    // [rope_len][d_head/2] (cos, sin) for positions < rope_len
+  int rope_len;
+  const float* inv_freq;     // [d_head/2]
+  bf16* const* k_pools;      // device array [num_caches] of K pools
+  bf16* const* v_pools;      // device array [num_caches] of V pools
+  int cache_base;            // EPI_QKV: the layer's cache; EPI_WIDE_KV: first skipped cache
+};
+
+__device__ __forceinline__ int pair_half(const EpiParams& p) {
+  return (p.kind == EPI_QKV || p.kind == EPI_WIDE_KV) ? (p.d_head >> 1) : 64;
+}
+
+// Column of the lo member of pair index `u` (0 <= u < ncols/2) in a block-aligned range.
+__device__ __forceinline__ int pair_lo(int u, int half) { return (u / half) * (2 * half) + (u % half); }
+
+__device__ __forceinline__ void rope_rotate(const EpiParams& p, int pos, int i, float& a, float& b) {
+  float c, s;
+  if (pos < p.rope_len) {
+    float2 cs = p.rope_tab[(size_t)pos * (p.d_head >> 1) + i];
+    c = cs.x;
+    s = cs.y;
+  } else {
+    sincosf((float)pos * p.inv_freq[i], &s, &c);
+  }
+  float a2 = a * c - b * s;
+  float b2 = b * c + a * s;
+  a = a2;
+  b = b2;
+}
+
+__device__ __forceinline__ void paged_store_pair(bf16* pool, int slot, int n_kv, int head, int d_head,
+                                                 int i, float a, float b) {
+  size_t page = (size_t)(slot >> 4);
+  size_t row = ((page * n_kv + head) * kPageSize + (slot & 15)) * (size_t)d_head;
+  pool[row + i] = __float2bfloat16_rn(a);
+  pool[row + i + (d_head >> 1)] = __float2bfloat16_rn(b);
+}
+
+__device__ __forceinline__ float silu_f(float x) { return x / (1.0f + __expf(-x)); }
+
+// Applies the epilogue to the column pair (n_lo, n_hi = n_lo + half) of row m.
+__device__ __forceinline__ void apply_pair(const EpiParams& p, int m, int n_lo, int n_hi, float a,
+                                           float b) {
+  switch (p.kind) {
+    case EPI_STORE_F32: {
+      float* o = p.out_f32 + (size_t)m * p.ldo;
+      o[n_lo] = a;
+      o[n_hi] = b;
+      break;
+    }
+    case EPI_STORE_BF16: {
+      bf16* o = p.out_bf16 + (size_t)m * p.ldo;
+      o[n_lo] = __float2bfloat16_rn(a);
+      o[n_hi] = __float2bfloat16_rn(b);
+      break;
+    }
+    case EPI_RESID: {
+      float* o = p.out_f32 + (size_t)m * p.ldo;
+      o[n_lo] += a;
+      o[n_hi] += b;
+      break;
+    }
+    case EPI_SWIGLU: {
+      int col = (n_lo >> 7) * 64 + (n_lo & 127);
+      p.out_bf16[(size_t)m * p.ldo + col] = __float2bfloat16_rn(silu_f(a) * b);
+      break;
+    }
+    case EPI_QKV: {
+      if (p.bias) {
+        a += p.bias[n_lo];
+        b += p.bias[n_hi];
+      }
+      const int dh = p.d_head;
+      if (n_lo < p.q_cols) {
+        rope_rotate(p, p.positions[m], n_lo % dh, a, b);
+        bf16* o = p.out_bf16 + (size_t)m * p.ldo;
+        o[n_lo] = __float2bfloat16_rn(a);
+        o[n_hi] = __float2bfloat16_rn(b);
+      } else {
+        int slot = p.slots[m];
+        if (slot < 0) break;
+        int c = n_lo - p.q_cols;
+        const int kvc = p.n_kv * dh;
+        bool is_k = c < kvc;
+        if (!is_k) c -= kvc;
+        int head = c / dh, i = c % dh;
+        if (is_k) rope_rotate(p, p.positions[m], i, a, b);
+        paged_store_pair(is_k ? p.k_pools[p.cache_base] : p.v_pools[p.cache_base], slot, p.n_kv, head,
+                         dh, i, a, b);
+      }
+      break;
+    }
+    case EPI_WIDE_KV: {
+      if (p.bias) {
+        a += p.bias[n_lo];
+        b += p.bias[n_hi];
+      }
+      int slot = p.slots[m];
+      if (slot < 0) break;
+      const int dh = p.d_head;
+      const int kvc = p.n_kv * dh;
+      int grp = n_lo / (2 * kvc);
+      int c = n_lo - grp * 2 * kvc;
+      bool is_k = c < kvc;
+      if (!is_k) c -= kvc;
+      int head = c / dh, i = c % dh;
+      if (is_k) rope_rotate(p, p.positions[m], i, a, b);
+      int cache = p.cache_base + grp;
+      paged_store_pair(is_k ? p.k_pools[cache] : p.v_pools[cache], slot, p.n_kv, head, dh, i, a, b);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// ---------------------------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+}  // namespace skv

@@ -1,0 +1,306 @@
+// Warp-level tensor-core GEMMs (mma.sync m16n8k16 bf16 -> fp32) with the shared
+// epilogues of common.cuh.
+//
+//   C[M][N] = A[M][K] * B[N][K]^T     A: activations, row-major (lda)
+//                                     B: weights, nn.Linear layout [out][in] (ldb = K)
+//
+// gemm_tiled: 128x128x32 CTA tiles, 8 warps (64x32 each), 4-stage cp.async ring,
+//             fp32 tile staged through shared memory for the pairwise epilogue.
+// gemm_skinny: M <= 64 rows (the last-token tail, decode, LM head): streams the
+//             weights once with split-K across CTAs; fp32 partials are reduced in a
+//             fixed order by reduce_epilogue (deterministic), which applies the epilogue.
+#include "common.cuh"
+#include "launch.h"
+
+namespace skv {
+
+namespace {
+
+constexpr int TM = 128, TN = 128, TK = 32, TSTAGES = 4, TTHREADS = 256;
+constexpr int TLD = TK + 8;  // padded smem row (80 B): conflict-free ldmatrix
+constexpr int TEPI_LD = TN + 4;
+constexpr int kTiledSmem = TSTAGES * (TM + TN) * TLD * 2;  // 81920 B
+static_assert(TM * TEPI_LD * 4 <= kTiledSmem, "epilogue tile must fit the ring");
+
+__global__ void __launch_bounds__(TTHREADS) gemm_tiled_kernel(const bf16* __restrict__ A, int lda,
+                                                              const bf16* __restrict__ B, int K,
+                                                              EpiParams ep) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  bf16* sA = reinterpret_cast<bf16*>(smem);
+  bf16* sB = sA + TSTAGES * TM * TLD;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int wm = warp >> 2, wn = warp & 3;  // 2 x 4 warps
+  const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
+  const int M = ep.M;
+  const int ktiles = K / TK;
+
+  auto load_stage = [&](int stage, int kt) {
+    const int k0 = kt * TK;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      int c = tid + i * TTHREADS;  // 0..511
+      int row = c >> 2, kc = c & 3;
+      int gm = m0 + row;
+      const bf16* src = A + (size_t)(gm < M ? gm : 0) * lda + k0 + kc * 8;
+      cp_async16(smem_u32(sA + (stage * TM + row) * TLD + kc * 8), src, gm < M ? 16 : 0);
+      int gn = n0 + row;
+      const bf16* srcb = B + (size_t)(gn < ep.N ? gn : 0) * K + k0 + kc * 8;
+      cp_async16(smem_u32(sB + (stage * TN + row) * TLD + kc * 8), srcb, gn < ep.N ? 16 : 0);
+    }
+  };
+
+  float acc[4][4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < TSTAGES - 1; ++s) {
+    if (s < ktiles) load_stage(s, s);
+    cp_async_commit();
+  }
+
+  for (int kt = 0; kt < ktiles; ++kt) {
+    cp_async_wait<TSTAGES - 2>();
+    __syncthreads();
+    {
+      int nk = kt + TSTAGES - 1;
+      if (nk < ktiles) load_stage(nk % TSTAGES, nk);
+      cp_async_commit();
+    }
+    const int stage = kt % TSTAGES;
+    const bf16* a_base = sA + stage * TM * TLD;
+    const bf16* b_base = sB + stage * TN * TLD;
+#pragma unroll
+    for (int kk = 0; kk < TK; kk += 16) {
+      uint32_t af[4][4], bfr[4][2];
+#pragma unroll
+      for (int mi = 0; mi < 4; ++mi) {
+        int row = wm * 64 + mi * 16 + (lane & 15);
+        int col = kk + (lane >> 4) * 8;
+        ldmatrix_x4(smem_u32(a_base + row * TLD + col), af[mi][0], af[mi][1], af[mi][2], af[mi][3]);
+      }
+#pragma unroll
+      for (int nj = 0; nj < 2; ++nj) {
+        int row = wn * 32 + nj * 16 + (lane & 7) + ((lane >> 4) << 3);
+        int col = kk + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4(smem_u32(b_base + row * TLD + col), bfr[2 * nj][0], bfr[2 * nj][1],
+                    bfr[2 * nj + 1][0], bfr[2 * nj + 1][1]);
+      }
+#pragma unroll
+      for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+        for (int ni = 0; ni < 4; ++ni) mma_bf16_16816(acc[mi][ni], af[mi], bfr[ni]);
+    }
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  float* tile = reinterpret_cast<float*>(smem);
+#pragma unroll
+  for (int mi = 0; mi < 4; ++mi)
+#pragma unroll
+    for (int ni = 0; ni < 4; ++ni) {
+      int r = wm * 64 + mi * 16 + (lane >> 2);
+      int c = wn * 32 + ni * 8 + 2 * (lane & 3);
+      tile[r * TEPI_LD + c] = acc[mi][ni][0];
+      tile[r * TEPI_LD + c + 1] = acc[mi][ni][1];
+      tile[(r + 8) * TEPI_LD + c] = acc[mi][ni][2];
+      tile[(r + 8) * TEPI_LD + c + 1] = acc[mi][ni][3];
+    }
+  __syncthreads();
+  const int half = pair_half(ep);
+  for (int u = tid; u < TM * (TN / 2); u += TTHREADS) {
+    int r = u / (TN / 2), pi = u % (TN / 2);
+    int m = m0 + r;
+    if (m >= M) continue;
+    int lo = pair_lo(pi, half);
+    apply_pair(ep, m, n0 + lo, n0 + lo + half, tile[r * TEPI_LD + lo], tile[r * TEPI_LD + lo + half]);
+  }
+}
+
+// ---------------------------------------------------------------------------- skinny split-K
+
+constexpr int SN = 64, SK = 64, SSTAGES = 4, STHREADS = 128, SLD = SK + 8;
+
+template <int MB>
+__global__ void __launch_bounds__(STHREADS) gemm_skinny_kernel(const bf16* __restrict__ A, int lda,
+                                                               const bf16* __restrict__ B, int K,
+                                                               int M, int N, int kchunk,
+                                                               float* __restrict__ part) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  bf16* sA = reinterpret_cast<bf16*>(smem);            // [SSTAGES][MB*16][SLD]
+  bf16* sB = sA + SSTAGES * MB * 16 * SLD;             // [SSTAGES][SN][SLD]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n0 = blockIdx.x * SN;
+  const int split = blockIdx.y;
+  const int kbeg = split * kchunk;
+  const int ktiles = kchunk / SK;
+
+  auto load_stage = [&](int stage, int kt) {
+    const int k0 = kbeg + kt * SK;
+#pragma unroll
+    for (int i = 0; i < (SN * 8) / STHREADS; ++i) {
+      int c = tid + i * STHREADS;
+      int row = c >> 3, kc = c & 7;
+      cp_async16(smem_u32(sB + (stage * SN + row) * SLD + kc * 8), B + (size_t)(n0 + row) * K + k0 + kc * 8,
+                 16);
+    }
+#pragma unroll
+    for (int i = 0; i < (MB * 16 * 8 + STHREADS - 1) / STHREADS; ++i) {
+      int c = tid + i * STHREADS;
+      if (c < MB * 16 * 8) {
+        int row = c >> 3, kc = c & 7;
+        const bf16* src = A + (size_t)(row < M ? row : 0) * lda + k0 + kc * 8;
+        cp_async16(smem_u32(sA + (stage * MB * 16 + row) * SLD + kc * 8), src, row < M ? 16 : 0);
+      }
+    }
+  };
+
+  float acc[MB][2][4];
+#pragma unroll
+  for (int i = 0; i < MB; ++i)
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[i][j][r] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < SSTAGES - 1; ++s) {
+    if (s < ktiles) load_stage(s, s);
+    cp_async_commit();
+  }
+  for (int kt = 0; kt < ktiles; ++kt) {
+    cp_async_wait<SSTAGES - 2>();
+    __syncthreads();
+    {
+      int nk = kt + SSTAGES - 1;
+      if (nk < ktiles) load_stage(nk % SSTAGES, nk);
+      cp_async_commit();
+    }
+    const int stage = kt % SSTAGES;
+    const bf16* a_base = sA + stage * MB * 16 * SLD;
+    const bf16* b_base = sB + stage * SN * SLD;
+#pragma unroll
+    for (int kk = 0; kk < SK; kk += 16) {
+      uint32_t bfr[2][2];
+      {
+        int row = warp * 16 + (lane & 7) + ((lane >> 4) << 3);
+        int col = kk + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4(smem_u32(b_base + row * SLD + col), bfr[0][0], bfr[0][1], bfr[1][0], bfr[1][1]);
+      }
+#pragma unroll
+      for (int mi = 0; mi < MB; ++mi) {
+        uint32_t af[4];
+        int row = mi * 16 + (lane & 15);
+        int col = kk + (lane >> 4) * 8;
+        ldmatrix_x4(smem_u32(a_base + row * SLD + col), af[0], af[1], af[2], af[3]);
+        mma_bf16_16816(acc[mi][0], af, bfr[0]);
+        mma_bf16_16816(acc[mi][1], af, bfr[1]);
+      }
+    }
+  }
+  cp_async_wait<0>();
+
+  float* out = part + (size_t)split * M * N;
+#pragma unroll
+  for (int mi = 0; mi < MB; ++mi)
+#pragma unroll
+    for (int ni = 0; ni < 2; ++ni) {
+      int r = mi * 16 + (lane >> 2);
+      int c = n0 + warp * 16 + ni * 8 + 2 * (lane & 3);
+      if (r < M) {
+        out[(size_t)r * N + c] = acc[mi][ni][0];
+        out[(size_t)r * N + c + 1] = acc[mi][ni][1];
+      }
+      if (r + 8 < M) {
+        out[(size_t)(r + 8) * N + c] = acc[mi][ni][2];
+        out[(size_t)(r + 8) * N + c + 1] = acc[mi][ni][3];
+      }
+    }
+}
+
+__global__ void reduce_epilogue_kernel(const float* __restrict__ part, int splits, EpiParams ep) {
+  const int M = ep.M, N = ep.N;
+  const int half = pair_half(ep);
+  const size_t total = (size_t)M * (N / 2);
+  for (size_t u = blockIdx.x * (size_t)blockDim.x + threadIdx.x; u < total;
+       u += (size_t)gridDim.x * blockDim.x) {
+    int m = (int)(u / (N / 2));
+    int pi = (int)(u % (N / 2));
+    int lo = pair_lo(pi, half), hi = lo + half;
+    float a = 0.f, b = 0.f;
+    for (int s = 0; s < splits; ++s) {
+      const float* p = part + (size_t)s * M * N + (size_t)m * N;
+      a += p[lo];
+      b += p[hi];
+    }
+    apply_pair(ep, m, lo, hi, a, b);
+  }
+}
+
+}  // namespace
+
+int skinny_splits(int M, int N, int K, int num_sms) {
+  (void)M;
+  int tiles = N / SN;
+  int s = 1;
+  while (tiles * s < 2 * num_sms && K % (SK * s * 2) == 0 && K / (s * 2) >= 256) s *= 2;
+  return s;
+}
+
+size_t skinny_scratch_bytes(int M, int N, int K, int num_sms) {
+  return (size_t)skinny_splits(M, N, K, num_sms) * M * N * sizeof(float);
+}
+
+cudaError_t launch_gemm_tiled(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
+                              cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kTiledSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(ep.N / TN, (ep.M + TM - 1) / TM);
+  gemm_tiled_kernel<<<grid, TTHREADS, kTiledSmem, stream>>>(A, lda, B, K, ep);
+  return cudaGetLastError();
+}
+
+template <int MB>
+static cudaError_t launch_skinny_mb(const bf16* A, int lda, const bf16* B, int K, int M, int N,
+                                    int splits, float* part, cudaStream_t stream) {
+  constexpr int smem = SSTAGES * (MB * 16 + SN) * SLD * 2;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<MB>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid(N / SN, splits);
+  gemm_skinny_kernel<MB><<<grid, STHREADS, smem, stream>>>(A, lda, B, K, M, N, K / splits, part);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_skinny(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
+                               float* scratch, int num_sms, cudaStream_t stream) {
+  const int M = ep.M, N = ep.N;
+  const int splits = skinny_splits(M, N, K, num_sms);
+  cudaError_t e;
+  if (M <= 16) e = launch_skinny_mb<1>(A, lda, B, K, M, N, splits, scratch, stream);
+  else if (M <= 32) e = launch_skinny_mb<2>(A, lda, B, K, M, N, splits, scratch, stream);
+  else if (M <= 48) e = launch_skinny_mb<3>(A, lda, B, K, M, N, splits, scratch, stream);
+  else e = launch_skinny_mb<4>(A, lda, B, K, M, N, splits, scratch, stream);
+  if (e != cudaSuccess) return e;
+  size_t total = (size_t)M * (N / 2);
+  int blocks = (int)((total + 255) / 256);
+  if (blocks > 8 * num_sms) blocks = 8 * num_sms;
+  reduce_epilogue_kernel<<<blocks, 256, 0, stream>>>(scratch, splits, ep);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -1,0 +1,70 @@
+// Internal launchers of the SwiftKV GB300 kernels (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace skv {
+
+// ---- GEMMs (C = A * B^T with an epilogue) -----------------------------------------------
+cudaError_t launch_gemm_tiled(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
+                              cudaStream_t stream);
+int skinny_splits(int M, int N, int K, int num_sms);
+size_t skinny_scratch_bytes(int M, int N, int K, int num_sms);
+cudaError_t launch_gemm_skinny(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
+                               float* scratch, int num_sms, cudaStream_t stream);
+// tcgen05 (TMEM accumulator, TMA-fed) GEMM; returns cudaErrorNotSupported if the shape is not
+// handled, so the caller can fall back to launch_gemm_tiled.
+cudaError_t launch_gemm_tc(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
+                           int num_sms, int* status, cudaStream_t stream);
+
+// ---- bookkeeping ------------------------------------------------------------------------
+constexpr int kBlobInts = 2000;
+struct IntBlob {
+  int n;
+  int v[kBlobInts];
+};
+// dst[0..blob.n) = blob.v (host data carried in the kernel's parameters).
+cudaError_t launch_upload(int* dst, const IntBlob& blob, cudaStream_t stream);
+cudaError_t upload_ints(int* dst, const int* src, int n, cudaStream_t stream);
+
+// positions / slots / last index of a packed prefill batch; validates tokens and pages.
+cudaError_t launch_plan_prefill(const int* cu, int P, int T, const int* tokens, int vocab,
+                                const int* block_table, int max_pages, int num_pages, int* positions,
+                                int* slots, int* last_idx, int* last_pos, int* status,
+                                cudaStream_t stream);
+// decode: one token per sequence at position seq_lens[b].
+cudaError_t launch_plan_decode(const int* seq_lens, int B, const int* tokens, int vocab,
+                               const int* block_table, int max_pages, int num_pages, int* positions,
+                               int* slots, int* status, cudaStream_t stream);
+
+// ---- row kernels -------------------------------------------------------------------------
+// x[t] = embed[tok[t]] (fp32); u[t] = bf16(rmsnorm(x[t]) * gamma)
+cudaError_t launch_embed_rmsnorm(const int* tokens, int T, const bf16* embed, int vocab, int d,
+                                 const float* gamma, float eps, float* x, bf16* u,
+                                 cudaStream_t stream);
+// u[t] = bf16(rmsnorm(x[rows ? rows[t] : t]) * gamma); if x_out, x_out[t] = x[row] (gather).
+// gamma == nullptr means a gain of one.
+cudaError_t launch_rmsnorm(const float* x, const int* rows, int T, int d, const float* gamma,
+                           float eps, bf16* u, float* x_out, cudaStream_t stream);
+cudaError_t launch_argmax(const float* logits, int rows, int V, int* out, cudaStream_t stream);
+// W[n][k] = bf16(float(W[n][k]) * gamma[k]) for n < rows
+cudaError_t launch_scale_columns(bf16* W, int rows, int K, const float* gamma, cudaStream_t stream);
+
+// ---- attention ---------------------------------------------------------------------------
+// Varlen causal GQA attention of packed prompts against their own paged K/V.
+// tiles: [num_tiles] (seq << 16 | q_tile) 64-row query tiles; cu: [P+1] device.
+cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
+                                     const int* block_table, int max_pages, int num_pages,
+                                     const int* cu, const int* tiles, int num_tiles, int n_q,
+                                     int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream);
+// One query row per sequence b at position qpos[b] attending to keys 0..qpos[b] of its paged cache.
+cudaError_t launch_attention_decode(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
+                                    const int* block_table, int max_pages, int num_pages,
+                                    const int* qpos, int B, int n_q, int n_kv, int d_head, bf16* out,
+                                    int ldo, cudaStream_t stream);
+
+}  // namespace skv

@@ -1,0 +1,770 @@
+// C-ABI implementation: model creation and weight packing, the SwiftKV prefill
+// orchestration (plan -> layers 1..l -> boundary norm + wide KV GEMM -> last-token
+// tail -> LM head) and the decode step. One stream, no host synchronisation inside
+// prefill/decode; per-call host data reaches the device through kernel parameters.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "launch.h"
+#include "swiftkv.h"
+
+using namespace skv;
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+#define CK(call)                                                                              \
+  do {                                                                                        \
+    cudaError_t e_ = (call);                                                                  \
+    if (e_ != cudaSuccess) return fail(SWIFTKV_ECUDA, "%s: %s", #call, cudaGetErrorString(e_)); \
+  } while (0)
+
+#define RET(x)                 \
+  do {                         \
+    int r_ = (x);              \
+    if (r_ != SWIFTKV_OK) return r_; \
+  } while (0)
+
+constexpr int kRopeLen = 32768;
+
+struct LayerW {
+  float* g_attn = nullptr;
+  float* g_mlp = nullptr;
+  bf16* wqkv = nullptr;  // full layer: [Nq + 2 Nkv][d]; skipped layer: W_Q only [Nq][d]
+  float* bqkv = nullptr;
+  bf16* wo = nullptr;    // [d][Nq]
+  bf16* wgu = nullptr;   // [2 Fp][d], gate/up interleaved in 64-row blocks
+  bf16* wd = nullptr;    // [d][Fp]
+  bool loaded = false;
+};
+
+struct Workspace {
+  int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens;
+  float *x, *xt, *part, *logits;
+  bf16 *u, *q, *attn, *h, *ut, *qt, *at, *ht;
+};
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+
+struct swiftkv_model {
+  swiftkv_model_config cfg;
+  int l, g, C, G;
+  int Nq, Nkv, Fp, Nwide;
+  int device, num_sms;
+  std::vector<LayerW> layers;
+  bf16 *embed = nullptr, *lm_head = nullptr;
+  float* g_final = nullptr;
+  bf16* w_wide = nullptr;
+  float* b_wide = nullptr;
+  float2* rope_tab = nullptr;
+  float* inv_freq = nullptr;
+  int* status = nullptr;
+  std::vector<void*> allocs;
+  size_t weight_bytes = 0;
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+  bool globals_loaded = false;
+  // profiling (swiftkv_profile_begin/end)
+  bool prof_on = false;
+  struct Rec {
+    std::string name;
+    cudaEvent_t a, b;
+    int kernels;
+    double flops, bytes;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+};
+
+namespace {
+
+int dalloc(swiftkv_model* m, void** p, size_t bytes) {
+  if (bytes == 0) bytes = 16;
+  cudaError_t e = cudaMalloc(p, bytes);
+  if (e != cudaSuccess) {
+    *p = nullptr;
+    cudaGetLastError();
+    return fail(SWIFTKV_EOOM, "cudaMalloc(%zu): %s", bytes, cudaGetErrorString(e));
+  }
+  m->allocs.push_back(*p);
+  m->weight_bytes += bytes;
+  return SWIFTKV_OK;
+}
+
+template <typename T>
+int dalloc_t(swiftkv_model* m, T** p, size_t count) {
+  void* v = nullptr;
+  int r = dalloc(m, &v, count * sizeof(T));
+  *p = static_cast<T*>(v);
+  return r;
+}
+
+int check_lg(int L, int l, int g) {
+  if (l < 1 || l > L) return fail(SWIFTKV_EINVAL_L, "l=%d outside [1, %d]", l, L);
+  if (g < 1 || (L - l) % g != 0) return fail(SWIFTKV_EINVAL_GROUP, "AcrossKV group %d does not divide L-l=%d", g, L - l);
+  return SWIFTKV_OK;
+}
+
+int check_cfg(const swiftkv_model_config* c) {
+  if (!c) return fail(SWIFTKV_EINVAL, "null config");
+  if (c->L < 1 || c->d < 1 || c->n_q < 1 || c->n_kv < 1 || c->ffn < 1 || c->vocab < 1)
+    return fail(SWIFTKV_EINVAL, "non-positive config field");
+  if (c->n_q % c->n_kv) return fail(SWIFTKV_EUNSUPPORTED, "n_q %% n_kv != 0");
+  if (c->n_q / c->n_kv > 8) return fail(SWIFTKV_EUNSUPPORTED, "GQA group > 8");
+  if (c->d_head != 64 && c->d_head != 128) return fail(SWIFTKV_EUNSUPPORTED, "d_head must be 64 or 128");
+  if (c->d % 128 || c->d > 8192) return fail(SWIFTKV_EUNSUPPORTED, "d must be a multiple of 128, <= 8192");
+  if ((c->n_q * c->d_head) % 128) return fail(SWIFTKV_EUNSUPPORTED, "n_q*d_head must be a multiple of 128");
+  if (c->vocab % 128) return fail(SWIFTKV_EUNSUPPORTED, "vocab must be a multiple of 128");
+  if (!(c->rope_theta > 0.f) || !(c->rms_eps > 0.f)) return fail(SWIFTKV_EINVAL, "bad rope_theta / rms_eps");
+  return SWIFTKV_OK;
+}
+
+int h2d(void* dst, const void* src, size_t bytes, cudaStream_t s) {
+  if (!src) return fail(SWIFTKV_EINVAL, "null host weight pointer");
+  CK(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, s));
+  return SWIFTKV_OK;
+}
+
+int cache_of_layer(const swiftkv_model* m, int j) { return j < m->l ? j : m->l + (j - m->l) / m->g; }
+
+// ---------------------------------------------------------------------------- workspace
+
+
+int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t part_bytes, Workspace* w) {
+  const auto& c = m->cfg;
+  const size_t A = 256;
+  size_t sizes[] = {
+      (size_t)(P + 1) * 4,           // cu / seq lens
+      (size_t)std::max(ntiles, 1) * 4,  // tiles
+      (size_t)4 * C * 4,             // pool pointers (2C x 8 bytes)
+      (size_t)T * 4, (size_t)T * 4,  // positions, slots
+      (size_t)P * 4, (size_t)P * 4,  // last idx / pos
+      (size_t)T * 4,                 // tokens (host-buffer entry)
+      (size_t)T * c.d * 4,           // x
+      (size_t)P * c.d * 4,           // xt
+      part_bytes,                    // skinny partials
+      (size_t)P * c.vocab * 4,       // logits (host-buffer entry)
+      (size_t)T * c.d * 2,           // u
+      (size_t)T * m->Nq * 2,         // q
+      (size_t)T * m->Nq * 2,         // attn
+      (size_t)T * m->Fp * 2,         // h
+      (size_t)P * c.d * 2,           // ut
+      (size_t)P * m->Nq * 2,         // qt
+      (size_t)P * m->Nq * 2,         // at
+      (size_t)P * m->Fp * 2,         // ht
+  };
+  const int n = sizeof(sizes) / sizeof(sizes[0]);
+  size_t off[32], total = 0;
+  for (int i = 0; i < n; ++i) {
+    off[i] = total;
+    total += align_up(sizes[i] ? sizes[i] : 16, A);
+  }
+  if (total > m->ws_bytes) {
+    if (m->ws) {
+      cudaFree(m->ws);  // synchronises the device: no enqueued work still uses it
+      m->ws = nullptr;
+      m->ws_bytes = 0;
+    }
+    size_t want = align_up(total + total / 8, 1 << 20);
+    cudaError_t e = cudaMalloc(&m->ws, want);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      return fail(SWIFTKV_EOOM, "workspace cudaMalloc(%zu): %s", want, cudaGetErrorString(e));
+    }
+    m->ws_bytes = want;
+  }
+  char* b = m->ws;
+  w->cu = (int*)(b + off[0]);
+  w->tiles = (int*)(b + off[1]);
+  w->pools = (int*)(b + off[2]);
+  w->positions = (int*)(b + off[3]);
+  w->slots = (int*)(b + off[4]);
+  w->last_idx = (int*)(b + off[5]);
+  w->last_pos = (int*)(b + off[6]);
+  w->tokens = (int*)(b + off[7]);
+  w->x = (float*)(b + off[8]);
+  w->xt = (float*)(b + off[9]);
+  w->part = (float*)(b + off[10]);
+  w->logits = (float*)(b + off[11]);
+  w->u = (bf16*)(b + off[12]);
+  w->q = (bf16*)(b + off[13]);
+  w->attn = (bf16*)(b + off[14]);
+  w->h = (bf16*)(b + off[15]);
+  w->ut = (bf16*)(b + off[16]);
+  w->qt = (bf16*)(b + off[17]);
+  w->at = (bf16*)(b + off[18]);
+  w->ht = (bf16*)(b + off[19]);
+  return SWIFTKV_OK;
+}
+
+size_t skinny_part_bytes(const swiftkv_model* m, int M) {
+  if (M > 64) return 16;
+  const auto& c = m->cfg;
+  size_t mx = 16;
+  int shapes[][2] = {{m->Nq + 2 * m->Nkv, c.d}, {m->Nq, c.d}, {c.d, m->Nq}, {2 * m->Fp, c.d},
+                     {c.d, m->Fp}, {c.vocab, c.d}, {std::max(m->Nwide, 64), c.d}};
+  for (auto& s : shapes) mx = std::max(mx, skinny_scratch_bytes(M, s[0], s[1], m->num_sms));
+  return mx;
+}
+
+// ---------------------------------------------------------------------------- launches
+
+struct Ctx {
+  swiftkv_model* m;
+  Workspace w;
+  cudaStream_t s;
+  const swiftkv_kv_pages* kv;
+  bf16* const* k_dev;  // device arrays of pool pointers
+  bf16* const* v_dev;
+};
+
+cudaEvent_t prof_event(swiftkv_model* m) {
+  if (m->ev_used == m->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    m->ev_pool.push_back(e);
+  }
+  return m->ev_pool[m->ev_used++];
+}
+
+// Brackets one launch site with events on the launch stream while profiling is on.
+struct Prof {
+  swiftkv_model* m;
+  cudaStream_t s;
+  int idx = -1;
+  Prof(swiftkv_model* m_, cudaStream_t s_, const char* name, int kernels, double flops, double bytes)
+      : m(m_), s(s_) {
+    if (!m->prof_on) return;
+    cudaEvent_t a = prof_event(m), b = prof_event(m);
+    if (!a || !b) return;
+    m->recs.push_back({name, a, b, kernels, flops, bytes});
+    idx = (int)m->recs.size() - 1;
+    cudaEventRecord(a, s);
+  }
+  ~Prof() {
+    if (idx >= 0) cudaEventRecord(m->recs[idx].b, s);
+  }
+};
+
+int gemm(Ctx& x, const char* name, const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
+         double flops) {
+  const bool skinny = ep.M <= 64;
+  const double bytes = (double)ep.N * K * 2 + (double)ep.M * K * 2;
+  Prof pr(x.m, x.s, name, skinny ? 2 : 1, flops, bytes);
+  cudaError_t e;
+  if (skinny) e = launch_gemm_skinny(A, lda, B, K, ep, x.w.part, x.m->num_sms, x.s);
+  else e = launch_gemm_tiled(A, lda, B, K, ep, x.s);
+  if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "gemm M=%d N=%d K=%d: %s", ep.M, ep.N, K, cudaGetErrorString(e));
+  return SWIFTKV_OK;
+}
+
+EpiParams epi_base(Ctx& x, int kind, int M, int N) {
+  EpiParams p;
+  memset(&p, 0, sizeof p);
+  p.kind = kind;
+  p.M = M;
+  p.N = N;
+  p.d_head = x.m->cfg.d_head;
+  p.n_kv = x.m->cfg.n_kv;
+  p.rope_tab = x.m->rope_tab;
+  p.rope_len = kRopeLen;
+  p.inv_freq = x.m->inv_freq;
+  p.k_pools = x.k_dev;
+  p.v_pools = x.v_dev;
+  return p;
+}
+
+int norm(Ctx& x, const float* src, const int* rows, int T, const float* gamma, bf16* u, float* xout) {
+  Prof pr(x.m, x.s, "rmsnorm", 1, 0.0, (double)T * x.m->cfg.d * (xout ? 10 : 6));
+  CK(launch_rmsnorm(src, rows, T, x.m->cfg.d, gamma, x.m->cfg.rms_eps, u, xout, x.s));
+  return SWIFTKV_OK;
+}
+
+// Attention output + O projection + MLP of layer j for rows [0, M) of (xres, q), reading
+// the layer's cache; `prefill` selects the varlen prompt kernel, else one query per row.
+int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, bf16* hb, bool prefill,
+               const int* qpos, int ntiles, const char* gname, double attn_flops) {
+  swiftkv_model* m = x.m;
+  const auto& c = m->cfg;
+  const LayerW& L = m->layers[j];
+  const int cidx = cache_of_layer(m, j);
+  const bf16* kp = static_cast<const bf16*>(x.kv->k_pool[cidx]);
+  const bf16* vp = static_cast<const bf16*>(x.kv->v_pool[cidx]);
+  cudaError_t e;
+  {
+  Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode", 1, attn_flops, 0.0);
+  if (prefill)
+    e = launch_attention_prefill(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
+                                 x.w.cu, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
+  else
+    e = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
+                                qpos, M, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
+  }
+  if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "attention layer %d: %s", j, cudaGetErrorString(e));
+  EpiParams eo = epi_base(x, EPI_RESID, M, c.d);
+  eo.ldo = c.d;
+  eo.out_f32 = xres;
+  RET(gemm(x, gname, ab, m->Nq, L.wo, m->Nq, eo, 2.0 * M * c.d * m->Nq));
+  RET(norm(x, xres, nullptr, M, L.g_mlp, ub, nullptr));
+  EpiParams eg = epi_base(x, EPI_SWIGLU, M, 2 * m->Fp);
+  eg.ldo = m->Fp;
+  eg.out_bf16 = hb;
+  RET(gemm(x, gname, ub, c.d, L.wgu, c.d, eg, 2.0 * M * 2 * c.ffn * c.d));
+  EpiParams ed = epi_base(x, EPI_RESID, M, c.d);
+  ed.ldo = c.d;
+  ed.out_f32 = xres;
+  RET(gemm(x, gname, hb, m->Fp, L.wd, m->Fp, ed, 2.0 * M * c.d * c.ffn));
+  return SWIFTKV_OK;
+}
+
+// Q/K/V (full layer: cache_base = j) or Q only (skipped layer) projection with RoPE.
+int qkv(Ctx& x, int j, int M, const bf16* ub, bf16* qb, const int* pos, const int* slots, const char* gname) {
+  swiftkv_model* m = x.m;
+  const LayerW& L = m->layers[j];
+  const bool full = j < m->l;
+  EpiParams e = epi_base(x, EPI_QKV, M, full ? m->Nq + 2 * m->Nkv : m->Nq);
+  e.ldo = m->Nq;
+  e.out_bf16 = qb;
+  e.bias = L.bqkv;
+  e.q_cols = m->Nq;
+  e.positions = pos;
+  e.slots = slots;
+  e.cache_base = j;
+  return gemm(x, gname, ub, m->cfg.d, L.wqkv, m->cfg.d, e, 2.0 * M * e.N * m->cfg.d);
+}
+
+// Boundary: one row-RMS of x_l (gains folded into W_KV) and the wide KV GEMM into the
+// skipped caches.
+int wide_kv(Ctx& x, int M, const float* xres, bf16* ub, const int* pos, const int* slots) {
+  swiftkv_model* m = x.m;
+  RET(norm(x, xres, nullptr, M, nullptr, ub, nullptr));
+  EpiParams e = epi_base(x, EPI_WIDE_KV, M, m->Nwide);
+  e.bias = m->b_wide;
+  e.positions = pos;
+  e.slots = slots;
+  e.cache_base = m->l;
+  return gemm(x, "gemm_wide_kv", ub, m->cfg.d, m->w_wide, m->cfg.d, e, 2.0 * M * m->Nwide * m->cfg.d);
+}
+
+int check_ready(const swiftkv_model* m) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  if (!m->globals_loaded) return fail(SWIFTKV_ESTATE, "globals not loaded");
+  for (int j = 0; j < m->cfg.L; ++j)
+    if (!m->layers[j].loaded) return fail(SWIFTKV_ESTATE, "layer %d not loaded", j);
+  return SWIFTKV_OK;
+}
+
+int check_kv(const swiftkv_model* m, const swiftkv_kv_pages* kv) {
+  if (!kv || !kv->k_pool || !kv->v_pool || !kv->block_table) return fail(SWIFTKV_EINVAL, "null kv pages");
+  if (kv->num_caches != m->C) return fail(SWIFTKV_EINVAL, "num_caches %d != %d", kv->num_caches, m->C);
+  if (kv->page_size != kPageSize) return fail(SWIFTKV_EINVAL, "page_size must be 16");
+  if (kv->num_pages < 1 || kv->max_pages_per_seq < 1) return fail(SWIFTKV_EINVAL, "empty page pool");
+  for (int c = 0; c < m->C; ++c)
+    if (!kv->k_pool[c] || !kv->v_pool[c]) return fail(SWIFTKV_EINVAL, "null pool pointer for cache %d", c);
+  return SWIFTKV_OK;
+}
+
+int upload_pools(Ctx& x) {
+  const int C = x.m->C;
+  std::vector<void*> ptrs(2 * C);
+  for (int c = 0; c < C; ++c) {
+    ptrs[c] = x.kv->k_pool[c];
+    ptrs[C + c] = x.kv->v_pool[c];
+  }
+  CK(upload_ints(x.w.pools, reinterpret_cast<const int*>(ptrs.data()), 4 * C, x.s));
+  x.k_dev = reinterpret_cast<bf16* const*>(x.w.pools);
+  x.v_dev = reinterpret_cast<bf16* const*>(x.w.pools) + C;
+  return SWIFTKV_OK;
+}
+
+}  // namespace
+
+// ============================================================================ C ABI
+
+extern "C" {
+
+const char* swiftkv_last_error(void) { return g_err.c_str(); }
+
+int swiftkv_cache_count(int L, int l, int g) {
+  if (L < 1) return fail(SWIFTKV_EINVAL, "L < 1");
+  RET(check_lg(L, l, g));
+  return l + (L - l) / g;
+}
+
+void swiftkv_free(swiftkv_model* m) {
+  if (!m) return;
+  for (void* p : m->allocs) cudaFree(p);
+  if (m->ws) cudaFree(m->ws);
+  for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+  delete m;
+}
+
+int swiftkv_model_create(const swiftkv_model_config* cfg, int l, int g, swiftkv_model** out) {
+  if (!out) return fail(SWIFTKV_EINVAL, "null out");
+  *out = nullptr;
+  RET(check_cfg(cfg));
+  RET(check_lg(cfg->L, l, g));
+  swiftkv_model* m = new swiftkv_model();
+  m->cfg = *cfg;
+  m->l = l;
+  m->g = g;
+  m->G = (cfg->L - l) / g;
+  m->C = l + m->G;
+  m->Nq = cfg->n_q * cfg->d_head;
+  m->Nkv = cfg->n_kv * cfg->d_head;
+  m->Fp = (cfg->ffn + 63) / 64 * 64;
+  m->Nwide = m->G * 2 * m->Nkv;
+  CK(cudaGetDevice(&m->device));
+  CK(cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device));
+  m->layers.resize(cfg->L);
+  const size_t d = cfg->d;
+  auto bail = [&](int r) {
+    swiftkv_free(m);
+    return r;
+  };
+  int r;
+  for (int j = 0; j < cfg->L; ++j) {
+    LayerW& L = m->layers[j];
+    const int nrows = j < l ? m->Nq + 2 * m->Nkv : m->Nq;
+    if ((r = dalloc_t(m, &L.g_attn, d)) || (r = dalloc_t(m, &L.g_mlp, d)) ||
+        (r = dalloc_t(m, &L.wqkv, (size_t)nrows * d)) || (r = dalloc_t(m, &L.wo, d * m->Nq)) ||
+        (r = dalloc_t(m, &L.wgu, (size_t)2 * m->Fp * d)) || (r = dalloc_t(m, &L.wd, d * m->Fp)))
+      return bail(r);
+    if (cfg->qkv_bias && (r = dalloc_t(m, &L.bqkv, nrows))) return bail(r);
+    if (m->Fp != cfg->ffn) {
+      if (cudaMemset(L.wgu, 0, (size_t)2 * m->Fp * d * 2) != cudaSuccess ||
+          cudaMemset(L.wd, 0, d * m->Fp * 2) != cudaSuccess)
+        return bail(fail(SWIFTKV_ECUDA, "memset"));
+    }
+  }
+  if (m->Nwide > 0) {
+    if ((r = dalloc_t(m, &m->w_wide, (size_t)m->Nwide * d))) return bail(r);
+    if (cfg->qkv_bias && (r = dalloc_t(m, &m->b_wide, m->Nwide))) return bail(r);
+  }
+  if ((r = dalloc_t(m, &m->embed, (size_t)cfg->vocab * d)) || (r = dalloc_t(m, &m->lm_head, (size_t)cfg->vocab * d)) ||
+      (r = dalloc_t(m, &m->g_final, d)) || (r = dalloc_t(m, &m->status, 1)))
+    return bail(r);
+  const int half = cfg->d_head / 2;
+  if ((r = dalloc_t(m, &m->inv_freq, half)) || (r = dalloc_t(m, &m->rope_tab, (size_t)kRopeLen * half)))
+    return bail(r);
+  std::vector<float> inv(half);
+  std::vector<double> invd(half);
+  for (int i = 0; i < half; ++i) {
+    invd[i] = std::pow((double)cfg->rope_theta, -2.0 * i / cfg->d_head);
+    inv[i] = (float)invd[i];
+  }
+  std::vector<float2> tab((size_t)kRopeLen * half);
+  for (int p = 0; p < kRopeLen; ++p)
+    for (int i = 0; i < half; ++i) {
+      double a = p * invd[i];
+      tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  if (cudaMemcpy(m->inv_freq, inv.data(), half * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(m->rope_tab, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(m->status, 0, 4) != cudaSuccess)
+    return bail(fail(SWIFTKV_ECUDA, "rope table upload"));
+  *out = m;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_load_layer(swiftkv_model* m, int j, const swiftkv_layer_weights* w, swiftkv_stream stream) {
+  if (!m || !w) return fail(SWIFTKV_EINVAL, "null argument");
+  const auto& c = m->cfg;
+  if (j < 0 || j >= c.L) return fail(SWIFTKV_EINVAL, "layer %d out of range", j);
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(cudaSetDevice(m->device));
+  LayerW& L = m->layers[j];
+  const size_t d = c.d, Nq = m->Nq, Nkv = m->Nkv, F = c.ffn, Fp = m->Fp;
+  const bool full = j < m->l;
+  const bool rep = !full && (j - m->l) % m->g == 0;
+  if (c.qkv_bias && (!w->bq || ((full || rep) && (!w->bk || !w->bv))))
+    return fail(SWIFTKV_EINVAL, "qkv_bias model needs bq/bk/bv");
+  if ((full || rep) && (!w->wk || !w->wv)) return fail(SWIFTKV_EINVAL, "layer %d needs wk/wv", j);
+  RET(h2d(L.g_attn, w->gamma_attn, d * 4, s));
+  RET(h2d(L.g_mlp, w->gamma_mlp, d * 4, s));
+  RET(h2d(L.wqkv, w->wq, Nq * d * 2, s));
+  if (full) {
+    RET(h2d(L.wqkv + Nq * d, w->wk, Nkv * d * 2, s));
+    RET(h2d(L.wqkv + (Nq + Nkv) * d, w->wv, Nkv * d * 2, s));
+  }
+  if (c.qkv_bias) {
+    RET(h2d(L.bqkv, w->bq, Nq * 4, s));
+    if (full) {
+      RET(h2d(L.bqkv + Nq, w->bk, Nkv * 4, s));
+      RET(h2d(L.bqkv + Nq + Nkv, w->bv, Nkv * 4, s));
+    }
+  }
+  RET(h2d(L.wo, w->wo, d * Nq * 2, s));
+  if (!w->w_gate || !w->w_up || !w->w_down) return fail(SWIFTKV_EINVAL, "null MLP weights");
+  for (size_t blk = 0; blk < Fp / 64; ++blk) {
+    size_t r0 = blk * 64;
+    if (r0 >= F) break;
+    size_t rows = std::min<size_t>(64, F - r0);
+    RET(h2d(L.wgu + (blk * 128) * d, w->w_gate + r0 * d, rows * d * 2, s));
+    RET(h2d(L.wgu + (blk * 128 + 64) * d, w->w_up + r0 * d, rows * d * 2, s));
+  }
+  CK(cudaMemcpy2DAsync(L.wd, Fp * 2, w->w_down, F * 2, F * 2, d, cudaMemcpyHostToDevice, s));
+  if (rep) {
+    const size_t gi = (j - m->l) / m->g;
+    const size_t base = gi * 2 * Nkv;
+    RET(h2d(m->w_wide + base * d, w->wk, Nkv * d * 2, s));
+    RET(h2d(m->w_wide + (base + Nkv) * d, w->wv, Nkv * d * 2, s));
+    CK(launch_scale_columns(m->w_wide + base * d, (int)(2 * Nkv), (int)d, L.g_attn, s));
+    if (c.qkv_bias) {
+      RET(h2d(m->b_wide + base, w->bk, Nkv * 4, s));
+      RET(h2d(m->b_wide + base + Nkv, w->bv, Nkv * 4, s));
+    }
+  }
+  CK(cudaStreamSynchronize(s));
+  L.loaded = true;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_load_globals(swiftkv_model* m, const uint16_t* embed, const float* gamma_final,
+                         const uint16_t* lm_head, swiftkv_stream stream) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(cudaSetDevice(m->device));
+  const size_t V = m->cfg.vocab, d = m->cfg.d;
+  RET(h2d(m->embed, embed, V * d * 2, s));
+  RET(h2d(m->lm_head, lm_head, V * d * 2, s));
+  RET(h2d(m->g_final, gamma_final, d * 4, s));
+  CK(cudaStreamSynchronize(s));
+  m->globals_loaded = true;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_load_weights(const swiftkv_model_config* cfg, const swiftkv_host_weights* w, int l, int g,
+                         swiftkv_stream stream, swiftkv_model** out) {
+  if (!out) return fail(SWIFTKV_EINVAL, "null out");
+  *out = nullptr;
+  if (!w || !w->layers) return fail(SWIFTKV_EINVAL, "null weights");
+  swiftkv_model* m = nullptr;
+  RET(swiftkv_model_create(cfg, l, g, &m));
+  int r = SWIFTKV_OK;
+  for (int j = 0; j < cfg->L && r == SWIFTKV_OK; ++j) r = swiftkv_load_layer(m, j, &w->layers[j], stream);
+  if (r == SWIFTKV_OK) r = swiftkv_load_globals(m, w->embed, w->gamma_final, w->lm_head, stream);
+  if (r != SWIFTKV_OK) {
+    std::string keep = g_err;
+    swiftkv_free(m);
+    g_err = keep;
+    return r;
+  }
+  *out = m;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspace_bytes) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  if (weight_bytes) *weight_bytes = m->weight_bytes;
+  if (workspace_bytes) *workspace_bytes = m->ws_bytes;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_status(swiftkv_model* m, int clear) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  CK(cudaSetDevice(m->device));
+  int v = 0;
+  CK(cudaMemcpy(&v, m->status, 4, cudaMemcpyDeviceToHost));
+  if (clear) CK(cudaMemset(m->status, 0, 4));
+  return v;
+}
+
+int swiftkv_profile_begin(swiftkv_model* m) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  m->recs.clear();
+  m->ev_used = 0;
+  m->prof_on = true;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_profile_end(swiftkv_model* m, swiftkv_profile_entry* out, int max_entries) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  m->prof_on = false;
+  std::vector<swiftkv_profile_entry> agg;
+  for (auto& r : m->recs) {
+    CK(cudaEventSynchronize(r.b));
+    float ms = 0.f;
+    CK(cudaEventElapsedTime(&ms, r.a, r.b));
+    swiftkv_profile_entry* e = nullptr;
+    for (auto& a : agg)
+      if (r.name == a.name) e = &a;
+    if (!e) {
+      agg.push_back(swiftkv_profile_entry{});
+      e = &agg.back();
+      snprintf(e->name, sizeof e->name, "%s", r.name.c_str());
+    }
+    e->calls += 1;
+    e->kernels += r.kernels;
+    e->ms += ms;
+    e->flops += r.flops;
+    e->bytes += r.bytes;
+  }
+  m->recs.clear();
+  m->ev_used = 0;
+  for (int i = 0; i < (int)agg.size() && i < max_entries; ++i) out[i] = agg[i];
+  return (int)agg.size();
+}
+
+static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* cu, int P, int l, int g,
+                        const swiftkv_kv_pages* kv, float* logits, cudaStream_t s, bool host_io) {
+  RET(check_ready(m));
+  if (l != m->l) return fail(SWIFTKV_EINVAL_L, "l=%d but the model was packed for l=%d", l, m->l);
+  if (g != m->g) return fail(SWIFTKV_EINVAL_GROUP, "g=%d but the model was packed for g=%d", g, m->g);
+  if (P < 0 || P > 32767) return fail(SWIFTKV_EINVAL, "num_seqs %d outside [0, 32767]", P);
+  if (P == 0) return SWIFTKV_OK;
+  if (!cu || !tokens || !logits) return fail(SWIFTKV_EINVAL, "null tokens / cu_seqlens / logits");
+  RET(check_kv(m, kv));
+  if (cu[0] != 0) return fail(SWIFTKV_EINVAL_SEQLENS, "cu_seqlens[0] != 0");
+  int maxn = 0;
+  for (int i = 0; i < P; ++i) {
+    int n = cu[i + 1] - cu[i];
+    if (n < 1) return fail(SWIFTKV_EINVAL_SEQLENS, "prompt %d has %d tokens", i, n);
+    if (n > kv->max_pages_per_seq * kPageSize)
+      return fail(SWIFTKV_ENO_PAGES, "prompt %d needs %d pages, block table holds %d", i, (n + 15) / 16,
+                  kv->max_pages_per_seq);
+    maxn = std::max(maxn, n);
+  }
+  const int T = cu[P];
+  if ((long long)T * std::max(m->Fp, m->cfg.d) >= (1LL << 31)) return fail(SWIFTKV_EUNSUPPORTED, "batch too large");
+  CK(cudaSetDevice(m->device));
+
+  std::vector<int> tiles;
+  for (int i = 0; i < P; ++i) {
+    int nt = (cu[i + 1] - cu[i] + 63) / 64;
+    for (int t = 0; t < nt; ++t) tiles.push_back((i << 16) | t);
+  }
+  std::stable_sort(tiles.begin(), tiles.end(), [](int a, int b) { return (a & 0xffff) > (b & 0xffff); });
+
+  Ctx x;
+  x.m = m;
+  x.s = s;
+  x.kv = kv;
+  size_t part = std::max(skinny_part_bytes(m, P), skinny_part_bytes(m, T));
+  RET(ensure_workspace(m, T, P, m->C, (int)tiles.size(), part, &x.w));
+  const int* tok = tokens;
+  if (host_io) {
+    CK(cudaMemcpyAsync(x.w.tokens, tokens, (size_t)T * 4, cudaMemcpyHostToDevice, s));
+    tok = x.w.tokens;
+  }
+  double attn_flops = 0;
+  for (int i = 0; i < P; ++i) {
+    double n = cu[i + 1] - cu[i];
+    attn_flops += 4.0 * m->cfg.n_q * m->cfg.d_head * n * (n + 1) / 2;
+  }
+  {
+  Prof pr(m, s, "plan", 1 + (P + 1 + kBlobInts - 1) / kBlobInts + ((int)tiles.size() + kBlobInts - 1) / kBlobInts +
+          (4 * m->C + kBlobInts - 1) / kBlobInts, 0.0, 0.0);
+  CK(upload_ints(x.w.cu, cu, P + 1, s));
+  CK(upload_ints(x.w.tiles, tiles.data(), (int)tiles.size(), s));
+  RET(upload_pools(x));
+  CK(launch_plan_prefill(x.w.cu, P, T, tok, m->cfg.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
+                         x.w.positions, x.w.slots, x.w.last_idx, x.w.last_pos, m->status, s));
+  }
+  const auto& c = m->cfg;
+  {
+  Prof pr(m, s, "embed_rmsnorm", 1, 0.0, (double)T * c.d * 8);
+  CK(launch_embed_rmsnorm(tok, T, m->embed, c.vocab, c.d, m->layers[0].g_attn, c.rms_eps, x.w.x, x.w.u, s));
+  }
+  // layers 1..l in full for every prompt token
+  for (int j = 0; j < m->l; ++j) {
+    if (j > 0) RET(norm(x, x.w.x, nullptr, T, m->layers[j].g_attn, x.w.u, nullptr));
+    RET(qkv(x, j, T, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_layers"));
+    RET(layer_rest(x, j, T, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, true, nullptr, (int)tiles.size(),
+                   "gemm_layers", attn_flops));
+  }
+  // caches of every skipped layer / AcrossKV group from x_l
+  if (m->G > 0) RET(wide_kv(x, T, x.w.x, x.w.u, x.w.positions, x.w.slots));
+  // last prompt token of each sequence: layers l+1..L
+  RET(norm(x, x.w.x, x.w.last_idx, P, m->l < c.L ? m->layers[m->l].g_attn : m->g_final, x.w.ut, x.w.xt));
+  for (int j = m->l; j < c.L; ++j) {
+    RET(qkv(x, j, P, x.w.ut, x.w.qt, x.w.last_pos, nullptr, "gemm_tail"));
+    RET(layer_rest(x, j, P, x.w.xt, x.w.qt, x.w.at, x.w.ut, x.w.ht, false, x.w.last_pos, 0, "gemm_tail",
+                   4.0 * c.n_q * c.d_head * (double)T));
+    RET(norm(x, x.w.xt, nullptr, P, j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final, x.w.ut, nullptr));
+  }
+  EpiParams el = epi_base(x, EPI_STORE_F32, P, c.vocab);
+  el.ldo = c.vocab;
+  el.out_f32 = host_io ? x.w.logits : logits;
+  RET(gemm(x, "lm_head", x.w.ut, c.d, m->lm_head, c.d, el, 2.0 * P * c.vocab * c.d));
+  if (host_io) {
+    CK(cudaMemcpyAsync(logits, x.w.logits, (size_t)P * c.vocab * 4, cudaMemcpyDeviceToHost, s));
+    CK(cudaStreamSynchronize(s));
+  }
+  CK(cudaGetLastError());
+  return SWIFTKV_OK;
+}
+
+int swiftkv_prefill(swiftkv_model* m, const int32_t* tokens, const int32_t* cu_seqlens, int num_seqs, int l,
+                    int g, const swiftkv_kv_pages* kv, float* logits, swiftkv_stream stream) {
+  return prefill_impl(m, tokens, cu_seqlens, num_seqs, l, g, kv, logits, (cudaStream_t)stream, false);
+}
+
+int swiftkv_prefill_host(swiftkv_model* m, const int32_t* tokens_host, const int32_t* cu_seqlens, int num_seqs,
+                         int l, int g, const swiftkv_kv_pages* kv, float* logits_host, swiftkv_stream stream) {
+  return prefill_impl(m, tokens_host, cu_seqlens, num_seqs, l, g, kv, logits_host, (cudaStream_t)stream, true);
+}
+
+int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* seq_lens, int B,
+                        const swiftkv_kv_pages* kv, float* logits, int32_t* next_tokens, swiftkv_stream stream) {
+  RET(check_ready(m));
+  if (B < 0 || B > 32767) return fail(SWIFTKV_EINVAL, "batch %d outside [0, 32767]", B);
+  if (B == 0) return SWIFTKV_OK;
+  if (!tokens || !seq_lens || !logits) return fail(SWIFTKV_EINVAL, "null tokens / seq_lens / logits");
+  RET(check_kv(m, kv));
+  for (int b = 0; b < B; ++b) {
+    if (seq_lens[b] < 0) return fail(SWIFTKV_EINVAL_SEQLENS, "seq_lens[%d] < 0", b);
+    if (seq_lens[b] + 1 > kv->max_pages_per_seq * kPageSize)
+      return fail(SWIFTKV_ENO_PAGES, "sequence %d has no page for position %d", b, seq_lens[b]);
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  CK(cudaSetDevice(m->device));
+  Ctx x;
+  x.m = m;
+  x.s = s;
+  x.kv = kv;
+  RET(ensure_workspace(m, B, B, m->C, 1, skinny_part_bytes(m, B), &x.w));
+  CK(upload_ints(x.w.cu, seq_lens, B, s));
+  RET(upload_pools(x));
+  const auto& c = m->cfg;
+  CK(launch_plan_decode(x.w.cu, B, tokens, c.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
+                        x.w.positions, x.w.slots, m->status, s));
+  CK(launch_embed_rmsnorm(tokens, B, m->embed, c.vocab, c.d, m->layers[0].g_attn, c.rms_eps, x.w.x, x.w.u, s));
+  for (int j = 0; j < c.L; ++j) {
+    if (j == m->l && m->G > 0) {
+      RET(wide_kv(x, B, x.w.x, x.w.u, x.w.positions, x.w.slots));
+      RET(norm(x, x.w.x, nullptr, B, m->layers[j].g_attn, x.w.u, nullptr));
+    }
+    RET(qkv(x, j, B, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_decode"));
+    RET(layer_rest(x, j, B, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, false, x.w.positions, 0, "gemm_decode", 0.0));
+    RET(norm(x, x.w.x, nullptr, B, j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final, x.w.u, nullptr));
+  }
+  EpiParams el = epi_base(x, EPI_STORE_F32, B, c.vocab);
+  el.ldo = c.vocab;
+  el.out_f32 = logits;
+  RET(gemm(x, "lm_head", x.w.u, c.d, m->lm_head, c.d, el, 2.0 * B * c.vocab * c.d));
+  if (next_tokens) CK(launch_argmax(logits, B, c.vocab, next_tokens, s));
+  CK(cudaGetLastError());
+  return SWIFTKV_OK;
+}
+
+}  // extern "C"

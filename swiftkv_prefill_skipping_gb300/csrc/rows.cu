@@ -1,0 +1,267 @@
+// Row-wise and bookkeeping kernels: parameter-carried uploads, the prefill/decode
+// plan (positions, paged slots, last-token rows), embedding + RMSNorm, RMSNorm
+// (optionally gathering rows), argmax, and the load-time column scaling that folds
+// an RMSNorm gain into the wide W_KV.
+//
+// RMSNorm rows are HBM-bound: one 128-thread CTA per row, 16-byte loads/stores,
+// fp32 statistics, bf16 output.
+#include <cfloat>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace skv {
+
+namespace {
+
+__global__ void upload_kernel(int* dst, IntBlob blob) {
+  for (int i = threadIdx.x + blockIdx.x * blockDim.x; i < blob.n; i += blockDim.x * gridDim.x)
+    dst[i] = blob.v[i];
+}
+
+__global__ void plan_prefill_kernel(const int* __restrict__ cu, int P, int T, const int* __restrict__ tokens,
+                                    int vocab, const int* __restrict__ bt, int max_pages, int num_pages,
+                                    int* positions, int* slots, int* last_idx, int* last_pos, int* status) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += blockDim.x * gridDim.x) {
+    int lo = 0, hi = P - 1;  // largest s with cu[s] <= t
+    while (lo < hi) {
+      int mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    const int s = lo;
+    const int pos = t - cu[s];
+    const int n = cu[s + 1] - cu[s];
+    const int page = bt[(size_t)s * max_pages + (pos >> 4)];
+    const bool ok = page >= 0 && page < num_pages;
+    if (!ok) atomicOr(status, kStatusBadPage);
+    positions[t] = pos;
+    slots[t] = ok ? page * kPageSize + (pos & 15) : -1;
+    if (pos == n - 1) {
+      last_idx[s] = t;
+      last_pos[s] = pos;
+    }
+    const int tok = tokens[t];
+    if (tok < 0 || tok >= vocab) atomicOr(status, kStatusBadToken);
+  }
+}
+
+__global__ void plan_decode_kernel(const int* __restrict__ seq_lens, int B, const int* __restrict__ tokens,
+                                   int vocab, const int* __restrict__ bt, int max_pages, int num_pages,
+                                   int* positions, int* slots, int* status) {
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < B; b += blockDim.x * gridDim.x) {
+    const int pos = seq_lens[b];
+    const int page = bt[(size_t)b * max_pages + (pos >> 4)];
+    const bool ok = page >= 0 && page < num_pages;
+    if (!ok) atomicOr(status, kStatusBadPage);
+    positions[b] = pos;
+    slots[b] = ok ? page * kPageSize + (pos & 15) : -1;
+    const int tok = tokens[b];
+    if (tok < 0 || tok >= vocab) atomicOr(status, kStatusBadToken);
+  }
+}
+
+constexpr int RN_THREADS = 128;
+constexpr int RN_MAXV = 16;  // float4 per thread: d <= 8192
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+#pragma unroll
+  for (int w = 0; w < RN_THREADS / 32; ++w) s += red[w];
+  return s;
+}
+
+__device__ __forceinline__ void store_bf16x4(bf16* dst, float4 v) {
+  uint2 pk;
+  pk.x = pack_bf16(v.x, v.y);
+  pk.y = pack_bf16(v.z, v.w);
+  *reinterpret_cast<uint2*>(dst) = pk;
+}
+
+__global__ void __launch_bounds__(RN_THREADS) embed_rmsnorm_kernel(const int* __restrict__ tokens,
+                                                                   const bf16* __restrict__ embed, int vocab,
+                                                                   int d, const float* __restrict__ gamma,
+                                                                   float eps, float* __restrict__ x,
+                                                                   bf16* __restrict__ u) {
+  __shared__ float red[RN_THREADS / 32];
+  const int t = blockIdx.x;
+  int tok = tokens[t];
+  if (tok < 0 || tok >= vocab) tok = 0;
+  const bf16* e = embed + (size_t)tok * d;
+  const int n4 = d >> 2;
+  float4 v[RN_MAXV];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < RN_MAXV; ++i) {
+    int c = threadIdx.x + i * RN_THREADS;
+    if (c < n4) {
+      uint2 raw = *reinterpret_cast<const uint2*>(e + 4 * c);
+      __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162*>(&raw.x);
+      __nv_bfloat162 p1 = *reinterpret_cast<__nv_bfloat162*>(&raw.y);
+      float2 f0 = __bfloat1622float2(p0), f1 = __bfloat1622float2(p1);
+      v[i] = make_float4(f0.x, f0.y, f1.x, f1.y);
+      ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+      reinterpret_cast<float4*>(x + (size_t)t * d)[c] = v[i];
+    }
+  }
+  const float r = rsqrtf(block_sum(ss, red) / d + eps);
+#pragma unroll
+  for (int i = 0; i < RN_MAXV; ++i) {
+    int c = threadIdx.x + i * RN_THREADS;
+    if (c < n4) {
+      float4 g = reinterpret_cast<const float4*>(gamma)[c];
+      float4 o = make_float4(v[i].x * r * g.x, v[i].y * r * g.y, v[i].z * r * g.z, v[i].w * r * g.w);
+      store_bf16x4(u + (size_t)t * d + 4 * c, o);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(RN_THREADS) rmsnorm_kernel(const float* __restrict__ x,
+                                                             const int* __restrict__ rows, int d,
+                                                             const float* __restrict__ gamma, float eps,
+                                                             bf16* __restrict__ u, float* __restrict__ x_out) {
+  __shared__ float red[RN_THREADS / 32];
+  const int t = blockIdx.x;
+  const int src = rows ? rows[t] : t;
+  const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * d);
+  const int n4 = d >> 2;
+  float4 v[RN_MAXV];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < RN_MAXV; ++i) {
+    int c = threadIdx.x + i * RN_THREADS;
+    if (c < n4) {
+      v[i] = xr[c];
+      ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+      if (x_out) reinterpret_cast<float4*>(x_out + (size_t)t * d)[c] = v[i];
+    }
+  }
+  const float r = rsqrtf(block_sum(ss, red) / d + eps);
+#pragma unroll
+  for (int i = 0; i < RN_MAXV; ++i) {
+    int c = threadIdx.x + i * RN_THREADS;
+    if (c < n4) {
+      float4 g = gamma ? reinterpret_cast<const float4*>(gamma)[c] : make_float4(1.f, 1.f, 1.f, 1.f);
+      float4 o = make_float4(v[i].x * r * g.x, v[i].y * r * g.y, v[i].z * r * g.z, v[i].w * r * g.w);
+      store_bf16x4(u + (size_t)t * d + 4 * c, o);
+    }
+  }
+}
+
+__global__ void argmax_kernel(const float* __restrict__ logits, int V, int* __restrict__ out) {
+  __shared__ float sv[32];
+  __shared__ int si[32];
+  const float* row = logits + (size_t)blockIdx.x * V;
+  float best = -FLT_MAX;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < V; i += blockDim.x) {
+    float v = row[i];
+    if (v > best) {  // strided scan visits indices in increasing order: keeps the first maximum
+      best = v;
+      bi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float v2 = __shfl_xor_sync(0xffffffffu, best, o);
+    int i2 = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (v2 > best || (v2 == best && i2 < bi)) {
+      best = v2;
+      bi = i2;
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sv[warp] = best;
+    si[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
+      if (sv[w] > best || (sv[w] == best && si[w] < bi)) {
+        best = sv[w];
+        bi = si[w];
+      }
+    out[blockIdx.x] = bi == 0x7fffffff ? 0 : bi;
+  }
+}
+
+__global__ void scale_columns_kernel(bf16* W, size_t total, int K, const float* __restrict__ gamma) {
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x)
+    W[i] = __float2bfloat16_rn(__bfloat162float(W[i]) * gamma[i % K]);
+}
+
+}  // namespace
+
+cudaError_t launch_upload(int* dst, const IntBlob& blob, cudaStream_t stream) {
+  if (blob.n <= 0) return cudaSuccess;
+  upload_kernel<<<(blob.n + 255) / 256, 256, 0, stream>>>(dst, blob);
+  return cudaGetLastError();
+}
+
+cudaError_t upload_ints(int* dst, const int* src, int n, cudaStream_t stream) {
+  IntBlob blob;
+  for (int off = 0; off < n; off += kBlobInts) {
+    blob.n = n - off < kBlobInts ? n - off : kBlobInts;
+    for (int i = 0; i < blob.n; ++i) blob.v[i] = src[off + i];
+    cudaError_t e = launch_upload(dst + off, blob, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_plan_prefill(const int* cu, int P, int T, const int* tokens, int vocab,
+                                const int* block_table, int max_pages, int num_pages, int* positions,
+                                int* slots, int* last_idx, int* last_pos, int* status,
+                                cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  int blocks = (T + 255) / 256;
+  plan_prefill_kernel<<<blocks, 256, 0, stream>>>(cu, P, T, tokens, vocab, block_table, max_pages,
+                                                   num_pages, positions, slots, last_idx, last_pos,
+                                                   status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan_decode(const int* seq_lens, int B, const int* tokens, int vocab,
+                               const int* block_table, int max_pages, int num_pages, int* positions,
+                               int* slots, int* status, cudaStream_t stream) {
+  if (B <= 0) return cudaSuccess;
+  plan_decode_kernel<<<(B + 255) / 256, 256, 0, stream>>>(seq_lens, B, tokens, vocab, block_table,
+                                                          max_pages, num_pages, positions, slots, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_embed_rmsnorm(const int* tokens, int T, const bf16* embed, int vocab, int d,
+                                 const float* gamma, float eps, float* x, bf16* u,
+                                 cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  embed_rmsnorm_kernel<<<T, RN_THREADS, 0, stream>>>(tokens, embed, vocab, d, gamma, eps, x, u);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const float* x, const int* rows, int T, int d, const float* gamma,
+                           float eps, bf16* u, float* x_out, cudaStream_t stream) {
+  if (T <= 0) return cudaSuccess;
+  rmsnorm_kernel<<<T, RN_THREADS, 0, stream>>>(x, rows, d, gamma, eps, u, x_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_argmax(const float* logits, int rows, int V, int* out, cudaStream_t stream) {
+  if (rows <= 0) return cudaSuccess;
+  argmax_kernel<<<rows, 1024, 0, stream>>>(logits, V, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_columns(bf16* W, int rows, int K, const float* gamma, cudaStream_t stream) {
+  size_t total = (size_t)rows * K;
+  if (total == 0) return cudaSuccess;
+  scale_columns_kernel<<<1024, 256, 0, stream>>>(W, total, K, gamma);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

@@ -1,0 +1,64 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path and the oracle on the
+same seeded inputs and compare them at the stated tolerances."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+from oracle import model as OM
+
+KV_REL_TOL = 1e-2      # per cache and K/V tensor: ||gpu - ref||_2 / ||ref||_2
+LOGIT_ABS_TOL = 5e-2   # last-token logits, max |gpu - ref|
+
+
+def rel_l2(a, b) -> float:
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def run_gpu_prefill(shape, l, g, batch, gain_std=0.0, seed=0, model=None):
+    import torch
+    from swiftkv_prefill_skipping_gb300 import api
+    m = model or api.load_synthetic(shape, l, g, seed=seed, gain_std=gain_std)
+    kv = api.KVCache(m, batch.num_pages, batch.block_table)
+    tok = torch.as_tensor(batch.tokens, device="cuda")
+    logits = api.prefill(m, tok, batch.cu_seqlens, kv)
+    torch.cuda.synchronize()
+    return m, kv, logits
+
+
+def oracle_prefill(shape, l, g, batch, prompts=None, gain_std=0.0, seed=0, cache_layers=True):
+    w = oracle.synth_weights(shape, seed=seed, gain_std=gain_std, cache_layers=cache_layers)
+    cfg = oracle.config_of(shape)
+    idx = range(len(batch.lens)) if prompts is None else prompts
+    toks = [batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]] for s in idx]
+    caches, logits = OM.swiftkv_prefill(cfg, w, toks, l, g)
+    return list(idx), caches, logits, w
+
+
+def compare_prefill(kv, logits_gpu, batch, idx, caches, logits_ref, num_caches):
+    """Returns (worst KV relative error, worst logit abs error) over the prompts in idx."""
+    worst_kv, worst_lg = 0.0, 0.0
+    lg = logits_gpu.float().cpu().numpy()
+    for i, s in enumerate(idx):
+        n = int(batch.lens[s])
+        for c in range(num_caches):
+            for which, t in (("k", 0), ("v", 1)):
+                got = kv.gather(c, s, n, which).float().cpu().numpy()
+                worst_kv = max(worst_kv, rel_l2(got, caches[i][c][t]))
+        worst_lg = max(worst_lg, float(np.abs(lg[s] - logits_ref[i]).max()))
+    return worst_kv, worst_lg
+
+
+def untouched_rows_are_zero(kv, batch) -> bool:
+    """Bookkeeping: nothing was written outside the sequences' own (page, row) slots."""
+    import torch
+    used = torch.zeros(kv.k.shape[1] * 16, dtype=torch.bool)
+    for s, n in enumerate(batch.lens):
+        for p in range(int(n)):
+            used[int(batch.block_table[s][p // 16]) * 16 + p % 16] = True
+    k = kv.k.float().abs().sum(dim=(2, 4)).permute(1, 2, 0).reshape(-1, kv.k.shape[0]).cpu()
+    v = kv.v.float().abs().sum(dim=(2, 4)).permute(1, 2, 0).reshape(-1, kv.v.shape[0]).cpu()
+    return bool((k[~used] == 0).all() and (v[~used] == 0).all() and (k[used] > 0).all())
