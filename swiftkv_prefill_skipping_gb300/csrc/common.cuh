@@ -15,7 +15,7 @@ typedef __nv_bfloat16 bf16;
 
 constexpr int kPageSize = 16;
 
-enum StatusBits : int { kStatusBadToken = 1, kStatusBadPage = 2 };
+enum StatusBits : int { kStatusBadToken = 1, kStatusBadPage = 2, kStatusTimeout = 4 };
 
 // Epilogue kinds. Column pairing: every GEMM hands columns to the epilogue in
 // pairs (lo, hi = lo + half) inside aligned blocks of 2*half columns, where
@@ -150,6 +150,116 @@ __device__ __forceinline__ void apply_pair(const EpiParams& p, int m, int n_lo, 
       if (is_k) rope_rotate(p, p.positions[m], i, a, b);
       int cache = p.cache_base + grp;
       paged_store_pair(is_k ? p.k_pools[cache] : p.v_pools[cache], slot, p.n_kv, head, dh, i, a, b);
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+// ---------------------------------------------------------------------------- 32-column chunks
+
+__device__ __forceinline__ uint32_t pack_bf16_(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// dst must be 16-byte aligned
+__device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 8) {
+    uint4 u;
+    u.x = pack_bf16_(v[i], v[i + 1]);
+    u.y = pack_bf16_(v[i + 2], v[i + 3]);
+    u.z = pack_bf16_(v[i + 4], v[i + 5]);
+    u.w = pack_bf16_(v[i + 6], v[i + 7]);
+    *reinterpret_cast<uint4*>(dst + i) = u;
+  }
+}
+
+// Same epilogue as apply_pair for the 32 pairs (n_lo + i, n_hi + i), i < 32, with
+// 16-byte vector stores. A chunk never straddles a Q/K/V region or a head because
+// half is a multiple of 32 and region widths are multiples of d_head.
+__device__ __forceinline__ void apply_chunk32(const EpiParams& p, int m, int n_lo, int n_hi, float* a,
+                                              float* b) {
+  switch (p.kind) {
+    case EPI_STORE_F32: {
+      float* o = p.out_f32 + (size_t)m * p.ldo;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        *reinterpret_cast<float4*>(o + n_lo + i) = make_float4(a[i], a[i + 1], a[i + 2], a[i + 3]);
+        *reinterpret_cast<float4*>(o + n_hi + i) = make_float4(b[i], b[i + 1], b[i + 2], b[i + 3]);
+      }
+      break;
+    }
+    case EPI_RESID: {
+      float* o = p.out_f32 + (size_t)m * p.ldo;
+#pragma unroll
+      for (int i = 0; i < 32; i += 4) {
+        float4 x = *reinterpret_cast<float4*>(o + n_lo + i);
+        float4 y = *reinterpret_cast<float4*>(o + n_hi + i);
+        x.x += a[i]; x.y += a[i + 1]; x.z += a[i + 2]; x.w += a[i + 3];
+        y.x += b[i]; y.y += b[i + 1]; y.z += b[i + 2]; y.w += b[i + 3];
+        *reinterpret_cast<float4*>(o + n_lo + i) = x;
+        *reinterpret_cast<float4*>(o + n_hi + i) = y;
+      }
+      break;
+    }
+    case EPI_STORE_BF16: {
+      bf16* o = p.out_bf16 + (size_t)m * p.ldo;
+      store_bf16x32(o + n_lo, a);
+      store_bf16x32(o + n_hi, b);
+      break;
+    }
+    case EPI_SWIGLU: {
+#pragma unroll
+      for (int i = 0; i < 32; ++i) a[i] = silu_f(a[i]) * b[i];
+      store_bf16x32(p.out_bf16 + (size_t)m * p.ldo + (n_lo >> 7) * 64 + (n_lo & 127), a);
+      break;
+    }
+    case EPI_QKV:
+    case EPI_WIDE_KV: {
+      if (p.bias) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          a[i] += p.bias[n_lo + i];
+          b[i] += p.bias[n_hi + i];
+        }
+      }
+      const int dh = p.d_head;
+      const int kvc = p.n_kv * dh;
+      if (p.kind == EPI_QKV && n_lo < p.q_cols) {
+        const int pos = p.positions[m], i0 = n_lo % dh;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rope_rotate(p, pos, i0 + i, a[i], b[i]);
+        bf16* o = p.out_bf16 + (size_t)m * p.ldo;
+        store_bf16x32(o + n_lo, a);
+        store_bf16x32(o + n_hi, b);
+        break;
+      }
+      const int slot = p.slots[m];
+      if (slot < 0) break;
+      int c, cache;
+      if (p.kind == EPI_QKV) {
+        c = n_lo - p.q_cols;
+        cache = p.cache_base;
+      } else {
+        int grp = n_lo / (2 * kvc);
+        c = n_lo - grp * 2 * kvc;
+        cache = p.cache_base + grp;
+      }
+      const bool is_k = c < kvc;
+      if (!is_k) c -= kvc;
+      const int head = c / dh, i0 = c % dh;
+      if (is_k) {
+        const int pos = p.positions[m];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) rope_rotate(p, pos, i0 + i, a[i], b[i]);
+      }
+      bf16* pool = is_k ? p.k_pools[cache] : p.v_pools[cache];
+      bf16* row = pool + ((size_t)(slot >> 4) * p.n_kv + head) * kPageSize * dh + (size_t)(slot & 15) * dh;
+      store_bf16x32(row + i0, a);
+      store_bf16x32(row + i0 + (dh >> 1), b);
       break;
     }
     default:
