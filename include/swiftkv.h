@@ -59,7 +59,8 @@ enum swiftkv_error {
 /* Bits of the device status word. */
 enum swiftkv_status_bits {
   SWIFTKV_STATUS_BAD_TOKEN = 1, /* a token id outside [0, vocab): row 0 was used */
-  SWIFTKV_STATUS_BAD_PAGE = 2   /* a block-table entry outside [0, num_pages): access skipped */
+  SWIFTKV_STATUS_BAD_PAGE = 2,  /* a block-table entry outside [0, num_pages): access skipped */
+  SWIFTKV_STATUS_TIMEOUT = 4    /* a bounded wait inside a kernel expired; that kernel's output is invalid */
 };
 
 /* Shape of the decoder (Llama / Qwen family: RMSNorm, GQA attention with RoPE,
@@ -184,6 +185,20 @@ int swiftkv_status(swiftkv_model* m, int clear);
 
 /* Bytes of device memory the model holds for weights and for workspace. */
 int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspace_bytes);
+
+/* Kernel family for GEMMs with more than 64 rows: 0 = tcgen05 with TMEM accumulators fed
+ * by TMA (default), 1 = warp-level mma.sync tiles (kept as a cross-check). GEMMs with at
+ * most 64 rows always use the skinny split-K kernel. */
+int swiftkv_set_gemm_impl(swiftkv_model* m, int impl);
+
+/* Kernel self-test entry (no model needed): C = A * B^T on the current device.
+ *   A  device bf16 [M][K] row-major; B device bf16 [N][K] row-major; C device float [M][N]
+ *   impl 0 = tcgen05, 1 = mma.sync tiles, 2 = skinny split-K (M <= 64; allocates and frees
+ *   its own scratch and synchronises the device)
+ *   status  device int or NULL: receives SWIFTKV_STATUS_TIMEOUT if a bounded wait expired
+ * Requires K % 64 == 0 and N % 128 == 0. */
+int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,
+                      swiftkv_stream stream);
 
 /* Per-kernel-class timing of the model's own launches, for roofline reporting.
  * swiftkv_profile_begin clears the records and, until swiftkv_profile_end, brackets

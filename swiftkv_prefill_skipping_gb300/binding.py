@@ -21,11 +21,13 @@ ERRORS = {
 }
 STATUS_BAD_TOKEN = 1
 STATUS_BAD_PAGE = 2
+STATUS_TIMEOUT = 4
 
 # every symbol include/swiftkv.h declares
 EXPORTS = ("swiftkv_cache_count", "swiftkv_model_create", "swiftkv_load_layer", "swiftkv_load_globals",
            "swiftkv_load_weights", "swiftkv_prefill", "swiftkv_prefill_host", "swiftkv_decode_step",
-           "swiftkv_status", "swiftkv_memory", "swiftkv_profile_begin", "swiftkv_profile_end",
+           "swiftkv_status", "swiftkv_memory", "swiftkv_set_gemm_impl", "swiftkv_gemm_bf16",
+           "swiftkv_profile_begin", "swiftkv_profile_end",
            "swiftkv_last_error", "swiftkv_free")
 
 
@@ -83,6 +85,8 @@ def lib(path: str | None = None):
             L.swiftkv_decode_step.argtypes = [vp, vp, vp, i, C.POINTER(KVPages), vp, vp, vp]
             L.swiftkv_status.argtypes = [vp, i]
             L.swiftkv_memory.argtypes = [vp, C.POINTER(sz), C.POINTER(sz)]
+            L.swiftkv_set_gemm_impl.argtypes = [vp, i]
+            L.swiftkv_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
             L.swiftkv_profile_begin.argtypes = [vp]
             L.swiftkv_profile_end.argtypes = [vp, C.POINTER(ProfileEntry), i]
             L.swiftkv_last_error.restype = C.c_char_p

@@ -1,0 +1,337 @@
+// Blackwell (sm_103a) tensor-core GEMM: tcgen05.mma with the accumulator in
+// tensor memory (TMEM), operands staged by TMA, warp-specialised and persistent.
+//
+//   C[M][N] = A[M][K] * B[N][K]^T  (bf16 in, fp32 accumulate), epilogue from common.cuh
+//
+// CTA = 6 warps, one CTA per SM (192 KB shared memory):
+//   warp 0     TMA producer: 4-stage ring of (A 128x64, B 256x64) bf16 tiles, 128B swizzle
+//   warp 1     allocates 512 TMEM columns; one lane issues tcgen05.mma (M=128, N=256, K=16)
+//              into one of two 256-column fp32 accumulators, and tcgen05.commit frees
+//              ring stages / publishes a finished accumulator
+//   warps 2-5  epilogue: tcgen05.ld 32 rows x 32 columns per warp, fused epilogue, 16-byte
+//              stores; the accumulator is released as soon as it has been read, so the
+//              epilogue of tile i overlaps the main loop of tile i+1
+// Tiles are visited m-fastest so concurrently running CTAs share the weight tile in L2.
+//
+// Every mbarrier wait is bounded (2 s of %globaltimer). On a timeout the CTA raises
+// kStatusTimeout in the status word, stops issuing work, waits (bounded) for its own
+// TMA copies and MMAs in flight, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace skv {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;          // 16 KB
+constexpr int B_BYTES = BN * BK * 2;          // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 2 * BN;             // two accumulators
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+struct Ctrl {
+  uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], fin;
+  uint32_t tmem_base;
+  int abort;
+  int pending[STAGES];
+};
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (int)sizeof(Ctrl);
+
+// kind::f16 instruction descriptor: D fp32, A/B bf16, both K-major, N = BN, M = BM.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                           ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, int bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait; false if the CTA is aborting or the wait timed out (then it aborts).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kTimeoutNs) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accum) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accum)
+      : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, rows of 128 B (64 bf16) in the
+// 128-byte swizzle written by TMA, 8-row core groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (16 B; unused with swizzle)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+// 32 lanes x 32 consecutive fp32 columns; the wait is in the same statement so the
+// registers are complete when the statement ends.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                             const __grid_constant__ CUtensorMap tmB,
+                                                             EpiParams ep, int K, int* status) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + STAGES * STAGE_BYTES);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = ep.M, N = ep.N;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int num_tiles = m_tiles * ((N + BN - 1) / BN);
+  const int kblocks = K / BK;
+  volatile int* abort_flag = &ctl->abort;
+
+  auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
+  auto empty = [&](int s) { return smem_u32(&ctl->empty[s]); };
+  auto tfull = [&](int a) { return smem_u32(&ctl->tfull[a]); };
+  auto tempty = [&](int a) { return smem_u32(&ctl->tempty[a]); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+      ctl->pending[s] = -1;
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 128);
+    }
+    mbar_init(smem_u32(&ctl->fin), 1);
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
+        const int mt = t % m_tiles, nt = t / m_tiles;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
+          mbar_expect_tx(full(stage), STAGE_BYTES);
+          ctl->pending[stage] = (int)phase;
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+          tma_load_2d(sa, &tmA, kb * BK, mt * BM, full(stage));
+          tma_load_2d(sa + A_BYTES, &tmB, kb * BK, nt * BN, full(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(tempty(acc), aph ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full(stage), phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ctl->pending[stage] = -1;
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma(d, sdesc(sa + kk * 32), sdesc(sa + A_BYTES + kk * 32), (kb | kk) != 0);
+          tc_commit(empty(stage));
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit(tfull(acc));
+      }
+    }
+  } else {
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = pair_half(ep);
+    int it = 0;
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      const int mt = t % m_tiles, nt = t / m_tiles;
+      if (!mbar_wait(tfull(acc), aph, abort_flag)) break;
+      tc_fence_after();
+      const int row = mt * BM + q * 32 + lane;
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      for (int b0 = 0; b0 < BN; b0 += 2 * half) {
+        const int ncol = nt * BN + b0;
+        if (ncol >= N) break;
+        for (int c = 0; c < half; c += 32) {
+          float lo[32], hi[32];
+          tmem_ld32(tb + b0 + c, lo);
+          tmem_ld32(tb + b0 + half + c, hi);
+          if (row < M) apply_chunk32(ep, row, ncol + c, ncol + half + c, lo, hi);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty(acc));
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      atomicOr(status, kStatusTimeout);
+      for (int s = 0; s < STAGES; ++s) {  // TMA copies still in flight into this CTA's ring
+        const int ph = ctl->pending[s];
+        if (ph < 0) continue;
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(full(s), (uint32_t)ph) && global_ns() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+    if (threadIdx.x == 32) {  // MMAs this thread issued
+      tc_commit(smem_u32(&ctl->fin));
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(smem_u32(&ctl->fin), 0) && global_ns() - t0 < kTimeoutNs) {
+      }
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encoder() {
+  if (g_encode) return true;
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+          cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// Row-major bf16 [rows][cols] with leading dimension ld (elements), box 64 x box_rows.
+bool make_map(CUtensorMap* map, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box,
+                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep, int num_sms,
+                           int* status, cudaStream_t stream) {
+  if (ep.M < 1 || ep.N < 1 || K < BK || K % BK || ep.N % 128 || lda % 8 ||
+      (reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
+    return cudaErrorNotSupported;
+  if (!get_encoder()) return cudaErrorNotSupported;
+  CUtensorMap ta, tb;
+  if (!make_map(&ta, A, ep.M, K, lda, BM) || !make_map(&tb, B, ep.N, K, K, BN)) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int tiles = ((ep.M + BM - 1) / BM) * ((ep.N + BN - 1) / BN);
+  const int grid = tiles < num_sms ? tiles : num_sms;
+  gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, ep, K, status);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

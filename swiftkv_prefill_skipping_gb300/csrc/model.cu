@@ -82,6 +82,7 @@ struct swiftkv_model {
   char* ws = nullptr;
   size_t ws_bytes = 0;
   bool globals_loaded = false;
+  int gemm_impl = 0;  // 0 tcgen05, 1 mma.sync tiles (GEMMs with > 64 rows)
   // profiling (swiftkv_profile_begin/end)
   bool prof_on = false;
   struct Rec {
@@ -271,8 +272,13 @@ int gemm(Ctx& x, const char* name, const bf16* A, int lda, const bf16* B, int K,
   const double bytes = (double)ep.N * K * 2 + (double)ep.M * K * 2;
   Prof pr(x.m, x.s, name, skinny ? 2 : 1, flops, bytes);
   cudaError_t e;
-  if (skinny) e = launch_gemm_skinny(A, lda, B, K, ep, x.w.part, x.m->num_sms, x.s);
-  else e = launch_gemm_tiled(A, lda, B, K, ep, x.s);
+  if (skinny) {
+    e = launch_gemm_skinny(A, lda, B, K, ep, x.w.part, x.m->num_sms, x.s);
+  } else {
+    e = cudaErrorNotSupported;
+    if (x.m->gemm_impl == 0) e = launch_gemm_tc(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s);
+    if (e == cudaErrorNotSupported) e = launch_gemm_tiled(A, lda, B, K, ep, x.s);
+  }
   if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "gemm M=%d N=%d K=%d: %s", ep.M, ep.N, K, cudaGetErrorString(e));
   return SWIFTKV_OK;
 }
@@ -587,6 +593,63 @@ int swiftkv_status(swiftkv_model* m, int clear) {
   CK(cudaMemcpy(&v, m->status, 4, cudaMemcpyDeviceToHost));
   if (clear) CK(cudaMemset(m->status, 0, 4));
   return v;
+}
+
+int swiftkv_set_gemm_impl(swiftkv_model* m, int impl) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  if (impl != 0 && impl != 1) return fail(SWIFTKV_EINVAL, "gemm impl %d", impl);
+  m->gemm_impl = impl;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,
+                      swiftkv_stream stream) {
+  if (!A || !B || !C || M < 1 || N < 1 || K < 1) return fail(SWIFTKV_EINVAL, "bad gemm arguments");
+  if (K % 64 || N % 128) return fail(SWIFTKV_EUNSUPPORTED, "gemm needs K %% 64 == 0 and N %% 128 == 0");
+  cudaStream_t s = (cudaStream_t)stream;
+  int dev = 0, sms = 0;
+  CK(cudaGetDevice(&dev));
+  CK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  EpiParams ep;
+  memset(&ep, 0, sizeof ep);
+  ep.kind = EPI_STORE_F32;
+  ep.M = M;
+  ep.N = N;
+  ep.ldo = N;
+  ep.out_f32 = C;
+  int* st = status;
+  int* own = nullptr;
+  if (!st) {
+    CK(cudaMalloc(&own, 4));
+    CK(cudaMemset(own, 0, 4));
+    st = own;
+  }
+  cudaError_t e = cudaSuccess;
+  const bf16* a = static_cast<const bf16*>(A);
+  const bf16* b = static_cast<const bf16*>(B);
+  if (impl == 0) {
+    e = launch_gemm_tc(a, K, b, K, ep, sms, st, s);
+  } else if (impl == 1) {
+    e = launch_gemm_tiled(a, K, b, K, ep, s);
+  } else if (impl == 2) {
+    if (M > 64) e = cudaErrorNotSupported;
+    else {
+      float* scratch = nullptr;
+      e = cudaMalloc(&scratch, skinny_scratch_bytes(M, N, K, sms));
+      if (e == cudaSuccess) e = launch_gemm_skinny(a, K, b, K, ep, scratch, sms, s);
+      cudaDeviceSynchronize();
+      if (scratch) cudaFree(scratch);
+    }
+  } else {
+    e = cudaErrorInvalidValue;
+  }
+  if (own) {
+    cudaDeviceSynchronize();
+    cudaFree(own);
+  }
+  if (e != cudaSuccess) return fail(e == cudaErrorNotSupported ? SWIFTKV_EUNSUPPORTED : SWIFTKV_ECUDA,
+                                    "gemm impl %d: %s", impl, cudaGetErrorString(e));
+  return SWIFTKV_OK;
 }
 
 int swiftkv_profile_begin(swiftkv_model* m) {

@@ -170,3 +170,23 @@ def test_host_side_errors():
     m.l = 2
     out = api.prefill(m, tok, [0], kv)                       # no prompts: no-op
     assert out.shape[0] == 0
+
+
+def test_gemm_families_agree_within_oracle_tolerance():
+    """The whole prefill with tcgen05 GEMMs and with mma.sync GEMMs: both within the
+    oracle tolerances, and close to each other."""
+    from swiftkv_prefill_skipping_gb300 import binding
+    lens = [300, 129, 77]
+    batch = synth.prompt_batch(SMALL128.vocab, 3, 0, 0, lens=lens)
+    idx, caches, ref_logits, _ = oracle_prefill(SMALL128, 3, 1, batch, gain_std=0.1)
+    out = {}
+    for impl in (0, 1):
+        from swiftkv_prefill_skipping_gb300 import api
+        m = api.load_synthetic(SMALL128, 3, 1, gain_std=0.1)
+        binding.check(binding.lib().swiftkv_set_gemm_impl(m.handle, impl))
+        _, kv, logits = run_gpu_prefill(SMALL128, 3, 1, batch, model=m)
+        kv_err, lg_err = compare_prefill(kv, logits, batch, idx, caches, ref_logits, m.num_caches)
+        assert kv_err <= KV_REL_TOL and lg_err <= LOGIT_ABS_TOL, (impl, kv_err, lg_err)
+        assert m.status() == 0
+        out[impl] = logits.cpu().numpy()
+    assert float(np.abs(out[0] - out[1]).max()) <= LOGIT_ABS_TOL
