@@ -200,6 +200,24 @@ int swiftkv_set_gemm_impl(swiftkv_model* m, int impl);
 int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,
                       swiftkv_stream stream);
 
+/* swiftkv_gemm_bf16 with impl 2 (skinny split-K, M <= 64) for callers that may not
+ * allocate device memory, e.g. a host that reserves the GPU's memory for its own pools
+ * (a serving engine holding nearly all of HBM for its KV cache) or that cannot accept
+ * the device-wide synchronisation of cudaFree mid-pipeline. It has no counterpart in
+ * the SwiftKV paper; it is a deployment convenience of this library.
+ *   A  device bf16 [M][K]; B device bf16 [N][K]; C device float [M][N] (caller-owned)
+ *   Needs 1 <= M <= 64, K % 64 == 0, N % 128 == 0.
+ * Calls no cudaMalloc/cudaFree: the split-K scratch is a fixed 8 MiB device array in the
+ * library (one per GPU that loads it, held until the process exits). A shape whose
+ * scratch (splits * M * N * 4 bytes) exceeds 8 MiB returns SWIFTKV_EUNSUPPORTED without
+ * launching anything. The first call on a device looks the array's address up
+ * (cudaGetSymbolAddress, with that device current); make that first call before any
+ * stream capture. All calls on a device share the one array and it keeps the last
+ * call's contents: calls whose kernels overlap on the GPU (different streams without
+ * ordering) race on it and must be serialised by the caller. */
+int swiftkv_gemm_skinny_noalloc(const void* A, const void* B, float* C, int M, int N, int K,
+                                swiftkv_stream stream);
+
 /* Per-kernel-class timing of the model's own launches, for roofline reporting.
  * swiftkv_profile_begin clears the records and, until swiftkv_profile_end, brackets
  * every launch the model enqueues with a pair of CUDA events recorded on the launch's

@@ -9,6 +9,9 @@
 
 namespace skv {
 
+// Records `msg` as the calling thread's swiftkv_last_error() and returns `code`.
+int set_error(int code, const char* msg);
+
 // ---- GEMMs (C = A * B^T with an epilogue) -----------------------------------------------
 cudaError_t launch_gemm_tiled(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
                               cudaStream_t stream);

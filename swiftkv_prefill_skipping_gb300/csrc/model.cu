@@ -64,6 +64,10 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+namespace skv {
+int set_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace skv
+
 struct swiftkv_model {
   swiftkv_model_config cfg;
   int l, g, C, G;
