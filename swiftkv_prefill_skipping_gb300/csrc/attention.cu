@@ -191,14 +191,21 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
   }
 }
 
-constexpr int DTHREADS = 128, DWARPS = DTHREADS / 32, DMAXG = 8;
+constexpr int DTHREADS = 256, DWARPS = DTHREADS / 32, DMAXG = 8;
 
+// One CTA per (sequence b, KV head): 8 warps walk the keys 32 at a time. In a round,
+// lane i owns key k0 + i: it reads that key's K row (contiguous d_head*2 bytes) and
+// computes the scores of every query head of the GQA group against it; one warp
+// max/sum per head updates the running softmax; then the warp sweeps the round's 32
+// V rows (coalesced, lane = 4 dims at d_head 128) with each key's probability
+// broadcast by shuffle. Warps are merged through shared memory at the end.
 template <int D>
 __global__ void __launch_bounds__(DTHREADS) attn_decode_kernel(
     const bf16* __restrict__ q, int ldq, const bf16* __restrict__ kpool, const bf16* __restrict__ vpool,
     const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ qpos, int n_q,
     int n_kv, bf16* __restrict__ out, int ldo, float scale_log2) {
-  constexpr int DPL = D / 32;  // dims per lane (4 or 2)
+  constexpr int DPL = D / 32;  // dims per lane in the PV sweep
+  __shared__ float s_q[DMAXG][D];
   __shared__ float s_m[DWARPS][DMAXG], s_l[DWARPS][DMAXG];
   __shared__ float s_o[DWARPS][DMAXG][D];
   const int b = blockIdx.x, kvh = blockIdx.y;
@@ -206,42 +213,104 @@ __global__ void __launch_bounds__(DTHREADS) attn_decode_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nkeys = qpos[b] + 1;
 
-  float qv[DMAXG][DPL], o[DMAXG][DPL], m[DMAXG], l[DMAXG];
+  for (int i = threadIdx.x; i < G * D; i += DTHREADS) {
+    int g = i / D, dim = i % D;
+    s_q[g][dim] = __bfloat162float(q[(size_t)b * ldq + (kvh * G + g) * D + dim]) * scale_log2;
+  }
+  __syncthreads();
+
+  float m[DMAXG], l[DMAXG], o[DMAXG][DPL];
 #pragma unroll
   for (int g = 0; g < DMAXG; ++g) {
     m[g] = -FLT_MAX;
     l[g] = 0.f;
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      o[g][i] = 0.f;
-      qv[g][i] = g < G ? __bfloat162float(q[(size_t)b * ldq + (kvh * G + g) * D + lane * DPL + i]) : 0.f;
-    }
+    for (int i = 0; i < DPL; ++i) o[g][i] = 0.f;
   }
-  for (int k = warp; k < nkeys; k += DWARPS) {
-    const int page = bt[(size_t)b * max_pages + (k >> 4)];
-    if (page < 0 || page >= num_pages) continue;
-    const size_t off = (((size_t)page * n_kv + kvh) * kPageSize + (k & 15)) * D + lane * DPL;
-    float kr[DPL], vr[DPL];
+  const int* btrow = bt + (size_t)b * max_pages;
+  for (int k0 = warp * 32; k0 < nkeys; k0 += DWARPS * 32) {
+    const int k = k0 + lane;
+    int page = k < nkeys ? btrow[k >> 4] : -1;
+    const bool ok = page >= 0 && page < num_pages;
+    const size_t rowoff = ok ? (((size_t)page * n_kv + kvh) * kPageSize + (k & 15)) * D : 0;
+    float sc[DMAXG];
 #pragma unroll
-    for (int i = 0; i < DPL; ++i) {
-      kr[i] = __bfloat162float(kpool[off + i]);
-      vr[i] = __bfloat162float(vpool[off + i]);
+    for (int g = 0; g < DMAXG; ++g) sc[g] = 0.f;
+    if (ok) {
+      const uint4* kr = reinterpret_cast<const uint4*>(kpool + rowoff);
+#pragma unroll 4
+      for (int c = 0; c < D / 8; ++c) {
+        uint4 raw = kr[c];
+        const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+        float kf[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(h2[e]);
+          kf[2 * e] = f.x;
+          kf[2 * e + 1] = f.y;
+        }
+#pragma unroll
+        for (int g = 0; g < DMAXG; ++g) {
+          if (g < G) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sc[g] += s_q[g][c * 8 + e] * kf[e];
+          }
+        }
+      }
+    }
+    float p[DMAXG];
+#pragma unroll
+    for (int g = 0; g < DMAXG; ++g) {
+      if (g >= G) break;
+      float v = ok ? sc[g] : -INFINITY;
+      float mx = v;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      const float mn = fmaxf(m[g], mx);
+      const float al = exp2f(m[g] - mn);
+      p[g] = exp2f(v - mn);
+      float ps = p[g];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+      m[g] = mn;
+      l[g] = l[g] * al + ps;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) o[g][i] *= al;
+    }
+    const int kcount = min(32, nkeys - k0);
+    // issue all 32 V-row loads of the round before consuming any of them
+    float vr[32][DPL];
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) {
+      const int pg = __shfl_sync(0xffffffffu, page, kk);
+      if (kk < kcount && pg >= 0 && pg < num_pages) {
+        const bf16* vrow = vpool + (((size_t)pg * n_kv + kvh) * kPageSize + ((k0 + kk) & 15)) * D + lane * DPL;
+        if constexpr (DPL == 4) {
+          uint2 raw = *reinterpret_cast<const uint2*>(vrow);
+          float2 f0 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.x));
+          float2 f1 = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&raw.y));
+          vr[kk][0] = f0.x;
+          vr[kk][1] = f0.y;
+          vr[kk][2] = f1.x;
+          vr[kk][3] = f1.y;
+        } else {
+#pragma unroll
+          for (int i = 0; i < DPL; ++i) vr[kk][i] = __bfloat162float(vrow[i]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) vr[kk][i] = 0.f;
+      }
     }
 #pragma unroll
     for (int g = 0; g < DMAXG; ++g) {
       if (g >= G) break;
-      float sdot = 0.f;
 #pragma unroll
-      for (int i = 0; i < DPL; ++i) sdot += qv[g][i] * kr[i];
+      for (int kk = 0; kk < 32; ++kk) {
+        const float pk = __shfl_sync(0xffffffffu, p[g], kk);
 #pragma unroll
-      for (int off2 = 16; off2 > 0; off2 >>= 1) sdot += __shfl_xor_sync(0xffffffffu, sdot, off2);
-      sdot *= scale_log2;
-      float mn = fmaxf(m[g], sdot);
-      float al = exp2f(m[g] - mn), p = exp2f(sdot - mn);
-      m[g] = mn;
-      l[g] = l[g] * al + p;
-#pragma unroll
-      for (int i = 0; i < DPL; ++i) o[g][i] = o[g][i] * al + p * vr[i];
+        for (int i = 0; i < DPL; ++i) o[g][i] += pk * vr[kk][i];
+      }
     }
   }
 #pragma unroll

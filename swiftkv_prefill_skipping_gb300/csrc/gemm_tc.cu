@@ -11,7 +11,7 @@
 //   warps 2-5  epilogue: tcgen05.ld 32 rows x 32 columns per warp, fused epilogue, 16-byte
 //              stores; the accumulator is released as soon as it has been read, so the
 //              epilogue of tile i overlaps the main loop of tile i+1
-// Tiles are visited m-fastest so concurrently running CTAs share the weight tile in L2.
+// Tiles are visited in groups of m-tiles (see tile_coords) for L2 reuse.
 //
 // Every mbarrier wait is bounded (2 s of %globaltimer). On a timeout the CTA raises
 // kStatusTimeout in the status word, stops issuing work, waits (bounded) for its own
@@ -134,6 +134,20 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Tile order: groups of GROUP_M m-tiles; inside a group the m index runs fastest, then n.
+// The CTAs running at any moment then share one activation panel (GROUP_M x 128 rows,
+// 16 MB at K = 4096) that stays resident in L2 while the group sweeps every weight tile.
+constexpr int GROUP_M = 16;
+
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
+  const int per_group = GROUP_M * n_tiles;
+  const int g = t / per_group;
+  const int r = t - g * per_group;
+  const int gm = min(GROUP_M, m_tiles - g * GROUP_M);
+  mt = g * GROUP_M + r % gm;
+  nt = r / gm;
+}
+
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB,
                                                              EpiParams ep, int K, int* status) {
@@ -145,7 +159,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = ep.M, N = ep.N;
   const int m_tiles = (M + BM - 1) / BM;
-  const int num_tiles = m_tiles * ((N + BN - 1) / BN);
+  const int n_tiles = (N + BN - 1) / BN;
+  const int num_tiles = m_tiles * n_tiles;
   const int kblocks = K / BK;
   volatile int* abort_flag = &ctl->abort;
 
@@ -187,7 +202,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
-        const int mt = t % m_tiles, nt = t / m_tiles;
+        int mt, nt;
+        tile_coords(t, m_tiles, n_tiles, mt, nt);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
           mbar_expect_tx(full(stage), STAGE_BYTES);
@@ -241,7 +257,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      const int mt = t % m_tiles, nt = t / m_tiles;
+      int mt, nt;
+      tile_coords(t, m_tiles, n_tiles, mt, nt);
       if (!mbar_wait(tfull(acc), aph, abort_flag)) break;
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
