@@ -48,15 +48,39 @@ def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma, F64)
 
 
+# Accumulation type of the linear layers. float64 is the definition; tests switch it to
+# float32 (with `accumulate_in`) to measure the rounding floor that any implementation
+# accumulating in float32 faces against the float64 definition.
+_LINEAR_ACC = [F64]
+
+
+class accumulate_in:
+    """Context manager: run the linear layers' dot products in `dtype` (inputs are
+    bfloat16 values, exact in float32), everything else unchanged."""
+
+    def __init__(self, dtype):
+        self.dtype = dtype
+
+    def __enter__(self):
+        _LINEAR_ACC.append(self.dtype)
+        return self
+
+    def __exit__(self, *exc):
+        _LINEAR_ACC.pop()
+        return False
+
+
 def linear(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None,
            block: int = 8192) -> np.ndarray:
     """x @ w.T (+ b), w in nn.Linear layout [out][in]; w may be stored as float32
     (bfloat16 values) and is widened to float64 one block of output rows at a time."""
+    acc = _LINEAR_ACC[-1]
     x = np.asarray(x, dtype=F64)
+    xa = x.astype(acc)
     n_out = w.shape[0]
     out = np.empty(x.shape[:-1] + (n_out,), dtype=F64)
     for i in range(0, n_out, block):
-        out[..., i:i + block] = x @ np.asarray(w[i:i + block], dtype=F64).T
+        out[..., i:i + block] = xa @ np.asarray(w[i:i + block], dtype=acc).T
     if b is not None:
         out += np.asarray(b, F64)
     return out

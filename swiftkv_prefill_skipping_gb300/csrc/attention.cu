@@ -3,8 +3,9 @@
 // attn_prefill_kernel: varlen prompts, one CTA per (64-row query tile, query head).
 //   Q tile and double-buffered 64-key K/V tiles are staged in XOR-swizzled shared
 //   memory with cp.async; each (page, head) block of 16 keys is 16*d_head*2
-//   contiguous bytes. S = Q K^T and O += P V run on mma.sync bf16 tensor cores with
-//   fp32 accumulation; softmax is online (running max / sum in the log2 domain).
+//   contiguous bytes. S = Q K^T runs on mma.sync bf16 tensor cores, O += P V on fp16
+//   ones (V converted once per tile in shared memory, P kept at fp16 precision), both
+//   with fp32 accumulation; softmax is online (running max / sum in the log2 domain).
 //   Query tiles arrive longest-first (heaviest causal tiles scheduled first).
 // attn_decode_kernel: one query per sequence (decode tokens and the last prompt
 //   token of the SwiftKV tail), one CTA per (sequence, KV head) computing all query
@@ -90,6 +91,22 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     }
     const bf16* kb_s = sK + (kb & 1) * ABKV * D;
     const bf16* vb_s = sV + (kb & 1) * ABKV * D;
+    // V tile bf16 -> fp16 in place (exact inside fp16's normal range) so that P V can
+    // take P at fp16 precision: P in [0, 1] keeps 11 significant bits instead of 8.
+    {
+      uint4* vt = reinterpret_cast<uint4*>(sV + (kb & 1) * ABKV * D);
+      for (int c = tid; c < ABKV * D / 8; c += ATHREADS) {
+        uint4 raw = vt[c];
+        uint32_t* w = reinterpret_cast<uint32_t*>(&raw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
+          w[e] = pack_f16(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
+        }
+        vt[c] = raw;
+      }
+      __syncthreads();
+    }
 
     float sc[ABKV / 8][4];
 #pragma unroll
@@ -157,18 +174,18 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
 #pragma unroll
     for (int kk = 0; kk < ABKV / 16; ++kk) {
       uint32_t pa[4];
-      pa[0] = pack_bf16(sc[2 * kk][0], sc[2 * kk][1]);
-      pa[1] = pack_bf16(sc[2 * kk][2], sc[2 * kk][3]);
-      pa[2] = pack_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-      pa[3] = pack_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+      pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
+      pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
+      pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
+      pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
         uint32_t b0[2], b1[2];
         int row = kk * 16 + (lane & 15);
         int ch = dp * 2 + (lane >> 4);
         ldmatrix_x4_trans(smem_u32(vb_s + swz(row, ch)), b0[0], b0[1], b1[0], b1[1]);
-        mma_bf16_16816(o[2 * dp], pa, b0);
-        mma_bf16_16816(o[2 * dp + 1], pa, b1);
+        mma_f16_16816(o[2 * dp], pa, b0);
+        mma_f16_16816(o[2 * dp + 1], pa, b1);
       }
     }
     __syncthreads();

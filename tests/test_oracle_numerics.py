@@ -121,3 +121,17 @@ def test_silu_special_values():
     np.testing.assert_allclose(M.silu(np.float64(1.0)), 1.0 / (1.0 + math.exp(-1.0)), rtol=1e-15)
     x = torch.linspace(-8, 8, 101, dtype=torch.float64)
     np.testing.assert_allclose(M.silu(x.numpy()), torch.nn.functional.silu(x).numpy(), rtol=1e-14)
+
+
+def test_accumulate_in_float32_switch():
+    """The precision switch used to measure the float32-accumulation floor: inside it the
+    linear layer equals a float32 matmul of the same (bfloat16-valued) operands."""
+    x = M.bf16(rng.standard_normal((5, 64)))
+    w = M.bf16(rng.standard_normal((7, 64))).astype(np.float32)
+    exact = M.linear(x, w)
+    with M.accumulate_in(np.float32):
+        f32 = M.linear(x, w)
+    assert np.array_equal(f32, (x.astype(np.float32) @ w.T).astype(np.float64))
+    assert not np.array_equal(f32, exact)
+    np.testing.assert_allclose(f32, exact, rtol=1e-5, atol=1e-5)
+    assert np.array_equal(M.linear(x, w), exact)      # switch restored
