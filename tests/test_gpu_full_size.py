@@ -109,7 +109,6 @@ def _run_workload(name, decode_steps=0):
             assert e <= max(KV_REL_TOL, 1.5 * f), (name, step, c, e, f)
     assert m.status() == 0
     m.free()
-    return kv_err, lg_err
 
 
 def test_llama8b_l16_full_workload():
