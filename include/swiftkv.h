@@ -191,6 +191,10 @@ int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspa
  * most 64 rows always use the skinny split-K kernel. */
 int swiftkv_set_gemm_impl(swiftkv_model* m, int impl);
 
+/* Kernel family for the prompt tokens' attention: 0 = tcgen05 with TMA-staged paged K/V
+ * (default; d_head 128), 1 = warp-level mma.sync (always used for d_head 64). */
+int swiftkv_set_attention_impl(swiftkv_model* m, int impl);
+
 /* Kernel self-test entry (no model needed): C = A * B^T on the current device.
  *   A  device bf16 [M][K] row-major; B device bf16 [N][K] row-major; C device float [M][N]
  *   impl 0 = tcgen05, 1 = mma.sync tiles, 2 = skinny split-K (M <= 64; allocates and frees

@@ -48,26 +48,39 @@ def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma, F64)
 
 
-# Accumulation type of the linear layers. float64 is the definition; tests switch it to
-# float32 (with `accumulate_in`) to measure the rounding floor that any implementation
-# accumulating in float32 faces against the float64 definition.
+# Precision modes. float64 everywhere is the definition. Tests evaluate the same model at
+# a lower declared precision to measure the rounding floor any implementation with that
+# precision faces against the definition:
+#   _LINEAR_ACC  accumulation type of the linear layers' dot products;
+#   _P_ROUND     rounding applied to the unnormalised softmax weights before they meet V
+#                (None = exact; the normalising sum always uses the unrounded weights).
 _LINEAR_ACC = [F64]
+_P_ROUND = [None]
 
 
 class accumulate_in:
     """Context manager: run the linear layers' dot products in `dtype` (inputs are
-    bfloat16 values, exact in float32), everything else unchanged."""
+    bfloat16 values, exact in float32) and, if `p_round` is given, round the softmax
+    weights with it before the weighted sum of V; everything else unchanged."""
 
-    def __init__(self, dtype):
+    def __init__(self, dtype, p_round=None):
         self.dtype = dtype
+        self.p_round = p_round
 
     def __enter__(self):
         _LINEAR_ACC.append(self.dtype)
+        _P_ROUND.append(self.p_round)
         return self
 
     def __exit__(self, *exc):
         _LINEAR_ACC.pop()
+        _P_ROUND.pop()
         return False
+
+
+def fp16(x) -> np.ndarray:
+    """Round to the nearest IEEE half-precision value (ties to even), as float64."""
+    return np.asarray(x, dtype=F64).astype(np.float16).astype(F64)
 
 
 def linear(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None,
@@ -122,8 +135,12 @@ def causal_gqa_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.
         s = np.where(allowed, s, -np.inf)
         s = s - s.max(axis=1, keepdims=True)
         p = np.exp(s)
-        p = p / p.sum(axis=1, keepdims=True)
-        out[:, h, :] = p @ v[:, kv, :]
+        rnd = _P_ROUND[-1]
+        if rnd is None:
+            p = p / p.sum(axis=1, keepdims=True)
+            out[:, h, :] = p @ v[:, kv, :]
+        else:
+            out[:, h, :] = (rnd(p) @ v[:, kv, :]) / p.sum(axis=1, keepdims=True)
     return out
 
 

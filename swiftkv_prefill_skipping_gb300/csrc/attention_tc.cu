@@ -1,0 +1,379 @@
+// Varlen causal GQA flash attention on tcgen05 (sm_103a), d_head = 128, reading K/V
+// straight out of the paged cache with TMA.
+//
+// One CTA = 128 query rows of one prompt x one query head, 8 warps:
+//   warp 0     TMA producer: the Q tile once (two 64-column halves, 128B swizzle), then
+//              per 64-key block the K and V rows of its four 16-token pages (each page
+//              row block is contiguous in the pool) into a 3-stage ring
+//   warp 1     allocates TMEM; one lane issues S = Q K^T (M=128, N=64, K=128) into one of
+//              two 64-column S buffers, and O_blk = P V (M=128, N=128, K=64; fp16 operands,
+//              V used as an MN-major operand in the cache's own row layout) into one of two
+//              128-column buffers; S of block j+1 is issued before P V of block j so the
+//              tensor core works while the softmax warps do
+//   warps 2-5  one thread per query row: tcgen05.ld its S row, causal/length mask, online
+//              softmax in the log2 domain, P (fp16) into shared memory in the swizzled
+//              K-major layout the MMA reads; then O = O * alpha + O_blk in registers from
+//              the previous block's P V result; finally O / l to global memory
+// All mbarrier waits are bounded; on a timeout the CTA flags kStatusTimeout, drains its
+// own TMA copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cfloat>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tc_common.cuh"
+
+namespace skv {
+
+namespace {
+
+using namespace tc;
+
+constexpr int D = 128;          // head dim
+constexpr int BQ = 128;         // query rows per CTA
+constexpr int BKV = 64;         // keys per block (4 pages)
+constexpr int KV_STAGES = 3;
+constexpr int THREADS = 256;
+constexpr int Q_BYTES = BQ * D * 2;            // 32 KB (two 16 KB halves)
+constexpr int KV_HALF = BKV * 64 * 2;          // 8 KB: 64 keys x 64 dims
+constexpr int K_BYTES = 2 * KV_HALF;           // 16 KB
+constexpr int STAGE_BYTES = 2 * K_BYTES;       // K + V
+constexpr int P_BYTES = BQ * BKV * 2;          // 16 KB
+constexpr int TMEM_COLS = 512;                 // S: 2 x 64, O blocks: 2 x 128
+constexpr int S_COL = 0, O_COL = 128;
+
+struct Ctrl {
+  uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], v_ready[KV_STAGES], s_full[2], s_empty[2],
+      p_full[2], o_full[2], o_empty[2], fin;
+  uint32_t tmem_base;
+  int abort;
+  int pending[KV_STAGES + 1];
+};
+constexpr int SMEM_BYTES = 1024 + Q_BYTES + KV_STAGES * STAGE_BYTES + 2 * P_BYTES + (int)sizeof(Ctrl);
+
+constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);  // Q (K-major) x K (K-major)
+constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true, true);  // P (K-major) x V (MN-major), fp16
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
+    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+    const __grid_constant__ CUtensorMap tmV, const int* __restrict__ bt, int max_pages, int num_pages,
+    const int* __restrict__ cu, const int* __restrict__ tiles, int n_q, int n_kv, bf16* __restrict__ out,
+    int ldo, float scale_log2, int* status) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sKV = sQ + Q_BYTES;
+  const uint32_t sP = sKV + KV_STAGES * STAGE_BYTES;
+  unsigned char* sP_gen = smem + Q_BYTES + KV_STAGES * STAGE_BYTES;
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + Q_BYTES + KV_STAGES * STAGE_BYTES + 2 * P_BYTES);
+  volatile int* abort_flag = &ctl->abort;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tile = tiles[blockIdx.x];
+  const int s = tile >> 16, qt = tile & 0xffff;
+  const int h = blockIdx.y, kvh = h / (n_q / n_kv);
+  const int seq0 = cu[s], n = cu[s + 1] - seq0;
+  const int q0 = qt * BQ;
+  const int kv_end = min(n, q0 + BQ);
+  const int nblk = (kv_end + BKV - 1) / BKV;
+  const int pool_rows = num_pages * n_kv * kPageSize;
+
+  auto bar = [&](uint64_t& b) { return smem_u32(&b); };
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(ctl->q_full), 1);
+    for (int i = 0; i < KV_STAGES; ++i) {
+      mbar_init(bar(ctl->kv_full[i]), 1);
+      mbar_init(bar(ctl->kv_empty[i]), 1);
+      mbar_init(bar(ctl->v_ready[i]), 64);
+      ctl->pending[i] = -1;
+    }
+    ctl->pending[KV_STAGES] = -1;
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(ctl->s_full[i]), 1);
+      mbar_init(bar(ctl->s_empty[i]), 128);
+      mbar_init(bar(ctl->p_full[i]), 128);
+      mbar_init(bar(ctl->o_full[i]), 1);
+      mbar_init(bar(ctl->o_empty[i]), 128);
+    }
+    mbar_init(bar(ctl->fin), 1);
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // Q: rows seq0+q0 .. +127 of this head's 128 columns (rows past the prompt are masked later)
+      mbar_expect_tx(bar(ctl->q_full), Q_BYTES);
+      ctl->pending[KV_STAGES] = 0;
+      tma_load_2d(sQ, &tmQ, h * D, seq0 + q0, bar(ctl->q_full));
+      tma_load_2d(sQ + Q_BYTES / 2, &tmQ, h * D + 64, seq0 + q0, bar(ctl->q_full));
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int j = 0; j < nblk; ++j) {
+        if (!mbar_wait(bar(ctl->kv_empty[stage]), phase ^ 1, abort_flag)) break;
+        mbar_expect_tx(bar(ctl->kv_full[stage]), STAGE_BYTES);
+        ctl->pending[stage] = (int)phase;
+        const uint32_t sk = sKV + stage * STAGE_BYTES, sv = sk + K_BYTES;
+#pragma unroll
+        for (int pg = 0; pg < BKV / kPageSize; ++pg) {
+          const int key = j * BKV + pg * kPageSize;
+          int page = key < n ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
+          // a page outside the pool reads rows past the tensor's end: TMA fills zeros
+          const int row = (page >= 0 && page < num_pages) ? (page * n_kv + kvh) * kPageSize : pool_rows;
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_load_2d(sk + hf * KV_HALF + pg * 2048, &tmK, hf * 64, row, bar(ctl->kv_full[stage]));
+            tma_load_2d(sv + hf * KV_HALF + pg * 2048, &tmV, hf * 64, row, bar(ctl->kv_full[stage]));
+          }
+        }
+        if (++stage == KV_STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = mbar_wait(bar(ctl->q_full), 0, abort_flag);
+      if (ok) ctl->pending[KV_STAGES] = -1;
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % KV_STAGES;
+        const uint32_t ph = (uint32_t)((j / KV_STAGES) & 1);
+        if (!mbar_wait(bar(ctl->kv_full[st]), ph, abort_flag)) return false;
+        ctl->pending[st] = -1;
+        const int sb = j & 1;
+        if (!mbar_wait(bar(ctl->s_empty[sb]), (uint32_t)(((j >> 1) & 1) ^ 1), abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t sk = sKV + st * STAGE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32;
+          const uint32_t koff = (kk >> 2) * KV_HALF + (kk & 3) * 32;
+          tc_mma(tmem + S_COL + sb * BKV, sdesc(sQ + off), sdesc(sk + koff), IDESC_S, kk != 0);
+        }
+        tc_commit(bar(ctl->s_full[sb]));
+        return true;
+      };
+      if (ok && nblk > 0) ok = issue_s(0);
+      for (int j = 0; ok && j < nblk; ++j) {
+        if (j + 1 < nblk && !issue_s(j + 1)) break;
+        const int pb = j & 1;
+        const uint32_t ph = (uint32_t)((j >> 1) & 1);
+        if (!mbar_wait(bar(ctl->p_full[pb]), ph, abort_flag)) break;
+        if (!mbar_wait(bar(ctl->o_empty[pb]), ph ^ 1, abort_flag)) break;
+        const int st = j % KV_STAGES;
+        if (!mbar_wait(bar(ctl->v_ready[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) break;
+        tc_fence_after();
+        const uint32_t sv = sKV + st * STAGE_BYTES + K_BYTES;
+        const uint32_t pbase = sP + pb * P_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BKV / 16; ++kk) {
+          // P: K-major, rows of 64 keys; V: MN-major, 64-dim halves 8 KB apart, 8-key groups 1 KB apart
+          tc_mma(tmem + O_COL + pb * D, sdesc(pbase + kk * 32), sdesc_sw128(sv + kk * 2048, KV_HALF, 1024),
+                 IDESC_O, kk != 0);
+        }
+        tc_commit(bar(ctl->o_full[pb]));
+        tc_commit(bar(ctl->kv_empty[st]));
+      }
+    }
+  } else if (warp >= 6) {
+    // V converters: each arrived V tile bf16 -> fp16 in place (exact inside fp16's normal
+    // range, clamped to +-65504) so that P V runs with P at fp16 precision
+    const int t = threadIdx.x - 192;
+    for (int j = 0; j < nblk; ++j) {
+      const int st = j % KV_STAGES;
+      if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) break;
+      uint4* vt = reinterpret_cast<uint4*>(smem + Q_BYTES + st * STAGE_BYTES + K_BYTES);
+#pragma unroll 4
+      for (int c = t; c < K_BYTES / 16; c += 64) {
+        uint4 rw = vt[c];
+        uint32_t* w = reinterpret_cast<uint32_t*>(&rw);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
+          w[e] = pack_f16(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
+        }
+        vt[c] = rw;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(ctl->v_ready[st]));
+    }
+  } else {
+    // softmax / output warps: thread <-> query row
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int qpos = q0 + r;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    float o[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) o[i] = 0.f;
+    float m = -FLT_MAX, l = 0.f, alpha_prev = 1.f;
+    bool ok = true;
+
+    auto accumulate = [&](int j, float alpha) -> bool {
+      const int ob = j & 1;
+      if (!mbar_wait(bar(ctl->o_full[ob]), (uint32_t)((j >> 1) & 1), abort_flag)) return false;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < D; c += 32) {
+        float t[32];
+        tmem_ld32(tmem + lane_off + O_COL + ob * D + c, t);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c + i] = o[c + i] * alpha + t[i];
+      }
+      tc_fence_before();
+      mbar_arrive(bar(ctl->o_empty[ob]));
+      return true;
+    };
+
+    for (int j = 0; j < nblk; ++j) {
+      const int sb = j & 1;
+      if (!mbar_wait(bar(ctl->s_full[sb]), (uint32_t)((j >> 1) & 1), abort_flag)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sc[BKV];
+      tmem_ld32(tmem + lane_off + S_COL + sb * BKV, sc);
+      tmem_ld32(tmem + lane_off + S_COL + sb * BKV + 32, sc + 32);
+      tc_fence_before();
+      mbar_arrive(bar(ctl->s_empty[sb]));
+      float mx = -FLT_MAX;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) {
+        const int key = j * BKV + i;
+        sc[i] = (key <= qpos && key < n) ? sc[i] * scale_log2 : -INFINITY;
+        mx = fmaxf(mx, sc[i]);
+      }
+      const float mn = fmaxf(m, mx);
+      const float alpha = exp2f(m - mn);
+      float rs = 0.f;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) {
+        sc[i] = exp2f(sc[i] - mn);
+        rs += sc[i];
+      }
+      m = mn;
+      l = l * alpha + rs;
+      // P row -> shared memory, 128B-swizzled K-major (row r: 8 chunks of 8 bf16)
+      unsigned char* prow = sP_gen + sb * P_BYTES + r * 128;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint4 u;
+        u.x = pack_f16(sc[8 * c], sc[8 * c + 1]);
+        u.y = pack_f16(sc[8 * c + 2], sc[8 * c + 3]);
+        u.z = pack_f16(sc[8 * c + 4], sc[8 * c + 5]);
+        u.w = pack_f16(sc[8 * c + 6], sc[8 * c + 7]);
+        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(bar(ctl->p_full[sb]));
+      // the previous block's P V is folded in with the scale it was computed under
+      if (j > 0 && !accumulate(j - 1, alpha_prev)) {
+        ok = false;
+        break;
+      }
+      alpha_prev = alpha;
+    }
+    if (ok && nblk > 0) ok = accumulate(nblk - 1, alpha_prev);
+    if (ok && qpos < n) {
+      const float inv = 1.f / l;
+      bf16* dst = out + (size_t)(seq0 + qpos) * ldo + h * D;
+#pragma unroll
+      for (int c = 0; c < D; c += 8) {
+        uint4 u;
+        u.x = pack_bf16(o[c] * inv, o[c + 1] * inv);
+        u.y = pack_bf16(o[c + 2] * inv, o[c + 3] * inv);
+        u.z = pack_bf16(o[c + 4] * inv, o[c + 5] * inv);
+        u.w = pack_bf16(o[c + 6] * inv, o[c + 7] * inv);
+        *reinterpret_cast<uint4*>(dst + c) = u;
+      }
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      atomicOr(status, kStatusTimeout);
+      for (int i = 0; i <= KV_STAGES; ++i) {
+        const int ph = ctl->pending[i];
+        if (ph < 0) continue;
+        const uint32_t b = i < KV_STAGES ? bar(ctl->kv_full[i]) : bar(ctl->q_full);
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(b, (uint32_t)ph) && global_ns() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+    if (threadIdx.x == 32) {
+      tc_commit(bar(ctl->fin));
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(bar(ctl->fin), 0) && global_ns() - t0 < kTimeoutNs) {
+      }
+    }
+    __syncthreads();
+  }
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+}
+
+}  // namespace
+
+cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
+                                        const int* block_table, int max_pages, int num_pages, const int* cu,
+                                        const int* tiles, int num_tiles, int n_q, int n_kv, int d_head, bf16* out,
+                                        int ldo, int* status, cudaStream_t stream) {
+  if (num_tiles <= 0) return cudaSuccess;
+  if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8) return cudaErrorNotSupported;
+  CUtensorMap mq, mk, mv;
+  const int pool_rows = num_pages * n_kv * kPageSize;
+  if (!tma_map_bf16_2d(&mq, q, T, n_q * D, ldq, 64, BQ, true) ||
+      !tma_map_bf16_2d(&mk, k_pool, pool_rows, D, D, 64, kPageSize, true) ||
+      !tma_map_bf16_2d(&mv, v_pool, pool_rows, D, D, 64, kPageSize, true))
+    return cudaErrorNotSupported;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+  dim3 grid(num_tiles, n_q);
+  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, block_table, max_pages, num_pages, cu, tiles,
+                                                        n_q, n_kv, out, ldo, scale_log2, status);
+  return cudaGetLastError();
+}
+
+}  // namespace skv

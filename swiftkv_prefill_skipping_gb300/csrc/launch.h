@@ -64,6 +64,12 @@ cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool,
                                      const int* block_table, int max_pages, int num_pages,
                                      const int* cu, const int* tiles, int num_tiles, int n_q,
                                      int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream);
+// Same on tcgen05 (d_head 128 only; cudaErrorNotSupported otherwise). tiles are 128-row tiles;
+// T = rows of q. status receives kStatusTimeout if a bounded wait expires.
+cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
+                                        const int* block_table, int max_pages, int num_pages, const int* cu,
+                                        const int* tiles, int num_tiles, int n_q, int n_kv, int d_head, bf16* out,
+                                        int ldo, int* status, cudaStream_t stream);
 // One query row per sequence b at position qpos[b] attending to keys 0..qpos[b] of its paged cache.
 cudaError_t launch_attention_decode(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                     const int* block_table, int max_pages, int num_pages,

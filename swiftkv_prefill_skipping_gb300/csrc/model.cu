@@ -87,6 +87,7 @@ struct swiftkv_model {
   size_t ws_bytes = 0;
   bool globals_loaded = false;
   int gemm_impl = 0;  // 0 tcgen05, 1 mma.sync tiles (GEMMs with > 64 rows)
+  int attn_impl = 0;  // 0 tcgen05 when d_head == 128, 1 mma.sync
   // profiling (swiftkv_profile_begin/end)
   bool prof_on = false;
   struct Rec {
@@ -240,6 +241,7 @@ struct Ctx {
   const swiftkv_kv_pages* kv;
   bf16* const* k_dev;  // device arrays of pool pointers
   bf16* const* v_dev;
+  bool tc_attn = false;  // prefill attention on tcgen05 (128-row query tiles)
 };
 
 cudaEvent_t prof_event(swiftkv_model* m) {
@@ -322,7 +324,11 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   cudaError_t e;
   {
   Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode", 1, attn_flops, 0.0);
-  if (prefill)
+  if (prefill && x.tc_attn)
+    e = launch_attention_prefill_tc(qb, m->Nq, M, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
+                                    x.kv->num_pages, x.w.cu, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq,
+                                    m->status, x.s);
+  else if (prefill)
     e = launch_attention_prefill(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
                                  x.w.cu, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
   else
@@ -606,6 +612,13 @@ int swiftkv_set_gemm_impl(swiftkv_model* m, int impl) {
   return SWIFTKV_OK;
 }
 
+int swiftkv_set_attention_impl(swiftkv_model* m, int impl) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  if (impl != 0 && impl != 1) return fail(SWIFTKV_EINVAL, "attention impl %d", impl);
+  m->attn_impl = impl;
+  return SWIFTKV_OK;
+}
+
 int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,
                       swiftkv_stream stream) {
   if (!A || !B || !C || M < 1 || N < 1 || K < 1) return fail(SWIFTKV_EINVAL, "bad gemm arguments");
@@ -715,9 +728,11 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   if ((long long)T * std::max(m->Fp, m->cfg.d) >= (1LL << 31)) return fail(SWIFTKV_EUNSUPPORTED, "batch too large");
   CK(cudaSetDevice(m->device));
 
+  const bool tc_attn = m->attn_impl == 0 && m->cfg.d_head == 128;
+  const int tile_rows = tc_attn ? 128 : 64;
   std::vector<int> tiles;
   for (int i = 0; i < P; ++i) {
-    int nt = (cu[i + 1] - cu[i] + 63) / 64;
+    int nt = (cu[i + 1] - cu[i] + tile_rows - 1) / tile_rows;
     for (int t = 0; t < nt; ++t) tiles.push_back((i << 16) | t);
   }
   std::stable_sort(tiles.begin(), tiles.end(), [](int a, int b) { return (a & 0xffff) > (b & 0xffff); });
@@ -726,6 +741,7 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   x.m = m;
   x.s = s;
   x.kv = kv;
+  x.tc_attn = tc_attn;
   size_t part = std::max(skinny_part_bytes(m, P), skinny_part_bytes(m, T));
   RET(ensure_workspace(m, T, P, m->C, (int)tiles.size(), part, &x.w));
   const int* tok = tokens;

@@ -12,11 +12,11 @@ Tolerance at full depth. Rounding to bfloat16 at every linear-layer input amplif
 difference between two evaluations: a perturbation far below one bf16 ulp flips a few
 roundings, the flips perturb the next GEMM by ~sqrt(perturbation * ulp), and within a
 layer or two two correct evaluations differ at the bf16 floor; each further layer adds
-to it. The oracle measures this floor itself: the same prompt with its linear layers
-accumulated in float32 (the GPU's accumulator precision) instead of float64. At 16+
-random-init layers that floor already exceeds 1e-2 (KV, relative L2) and 5e-2 (logits,
-max-abs), so here each cache must satisfy err <= max(1e-2, 1.5 * floor) and the logits
-err <= max(5e-2, 1.5 * floor). The stated tolerances apply unchanged at the shallow
+to it. The oracle measures this floor itself: the same prompt evaluated at the GPU path's
+declared precision (linear layers accumulated in float32, softmax weights rounded to fp16
+before they meet V) instead of float64. At 16+ random-init layers that floor already
+exceeds 1e-2 (KV, relative L2) and 5e-2 (logits, max-abs), so here each cache must satisfy
+err <= max(1e-2, 1.5 * floor) and the logits err <= max(5e-2, 1.5 * floor). The stated tolerances apply unchanged at the shallow
 shapes of test_gpu_parity.py. Llama-3.1-70B (141 GB of weights) runs with SWIFTKV_TEST_70B=1.
 """
 import os
@@ -65,7 +65,7 @@ def _run_workload(name, decode_steps=0):
     cfg = oracle.config_of(w.shape)
     wts = _oracle_weights(w.shape)
     caches, ref = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
-    with OM.accumulate_in(np.float32):
+    with OM.accumulate_in(np.float32, OM.fp16):
         caches32, ref32 = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
     lg = logits[s].float().cpu().numpy()
     lg_err, lg_floor = float(np.abs(lg - ref).max()), float(np.abs(ref32 - ref).max())
@@ -94,7 +94,7 @@ def _run_workload(name, decode_steps=0):
     for step in range(decode_steps):
         nxt = OM.greedy(lg_ref)
         cache, lg_ref = OM.swiftkv_decode_step(cfg, wts, cache, nxt, w.l, w.g)
-        with OM.accumulate_in(np.float32):
+        with OM.accumulate_in(np.float32, OM.fp16):
             cache32, lg32 = OM.swiftkv_decode_step(cfg, wts, cache32, nxt, w.l, w.g)
         toks_b = torch.zeros(len(batch.lens), dtype=torch.int32, device="cuda")
         toks_b[s] = nxt

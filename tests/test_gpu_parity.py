@@ -190,3 +190,22 @@ def test_gemm_families_agree_within_oracle_tolerance():
         assert m.status() == 0
         out[impl] = logits.cpu().numpy()
     assert float(np.abs(out[0] - out[1]).max()) <= LOGIT_ABS_TOL
+
+
+def test_attention_families_agree_within_oracle_tolerance():
+    """Prompt attention on tcgen05 (default at d_head 128) and on mma.sync: both within
+    the oracle tolerances, with prompts that end inside, at and past 128-row tiles."""
+    from swiftkv_prefill_skipping_gb300 import api, binding
+    lens = [300, 129, 128, 1, 77, 257]
+    batch = synth.prompt_batch(SMALL128.vocab, len(lens), 0, 0, lens=lens)
+    idx, caches, ref_logits, _ = oracle_prefill(SMALL128, 4, 1, batch, gain_std=0.1)
+    out = {}
+    for impl in (0, 1):
+        m = api.load_synthetic(SMALL128, 4, 1, gain_std=0.1)
+        binding.check(binding.lib().swiftkv_set_attention_impl(m.handle, impl))
+        _, kv, logits = run_gpu_prefill(SMALL128, 4, 1, batch, model=m)
+        kv_err, lg_err = compare_prefill(kv, logits, batch, idx, caches, ref_logits, m.num_caches)
+        assert kv_err <= KV_REL_TOL and lg_err <= LOGIT_ABS_TOL, (impl, kv_err, lg_err)
+        assert m.status() == 0
+        out[impl] = logits.cpu().numpy()
+    assert float(np.abs(out[0] - out[1]).max()) <= LOGIT_ABS_TOL

@@ -135,3 +135,25 @@ def test_accumulate_in_float32_switch():
     assert not np.array_equal(f32, exact)
     np.testing.assert_allclose(f32, exact, rtol=1e-5, atol=1e-5)
     assert np.array_equal(M.linear(x, w), exact)      # switch restored
+
+
+def test_precision_mode_rounds_softmax_weights_before_v():
+    """Inside accumulate_in(float32, fp16) attention uses fp16-rounded unnormalised weights
+    against V and the exact sum as denominator; brute force on a tiny case."""
+    n_q, d_h = 2, 4
+    q = rng.standard_normal((3, n_q, d_h))
+    k = rng.standard_normal((3, 1, d_h))
+    v = rng.standard_normal((3, 1, d_h))
+    pos = np.arange(3)
+    with M.accumulate_in(np.float32, M.fp16):
+        got = M.causal_gqa_attention(q, k, v, pos, pos)
+    for h in range(n_q):
+        for i in range(3):
+            s = [float(q[i, h] @ k[t, 0]) / math.sqrt(d_h) for t in range(i + 1)]
+            e = [math.exp(a - max(s)) for a in s]
+            num = sum(float(np.float16(e[t])) * v[t, 0] for t in range(i + 1))
+            np.testing.assert_allclose(got[i, h], num / sum(e), rtol=1e-12)
+    exact = M.causal_gqa_attention(q, k, v, pos, pos)
+    assert not np.array_equal(got, exact)
+    np.testing.assert_allclose(got, exact, rtol=2e-3, atol=2e-3)
+    assert M.fp16(1 + 2 ** -11) == 1.0 and M.fp16(1 + 3 * 2 ** -11) == 1 + 2 ** -9   # ties to even
