@@ -61,6 +61,11 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   nt = r / gm;
 }
 
+// MC: CTAs per cluster along M. With MC == 2 the two CTAs of a cluster compute m-tiles
+// 2p and 2p+1 of the same n-tile; each loads its own A tile and half of the shared B tile,
+// multicast into both CTAs, so each SM reads 32 KB instead of 48 KB from L2 per stage. A
+// ring stage is refilled only when both CTAs' MMAs have released it.
+template <int MC>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB,
                                                              EpiParams ep, int K, int* status) {
@@ -73,7 +78,11 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   const int M = ep.M, N = ep.N;
   const int m_tiles = (M + BM - 1) / BM;
   const int n_tiles = (N + BN - 1) / BN;
-  const int num_tiles = m_tiles * n_tiles;
+  // scheduling unit: MC vertically adjacent m-tiles of one n-tile
+  const int m_units = (m_tiles + MC - 1) / MC;
+  const int num_units = m_units * n_tiles;
+  const int crank = MC > 1 ? (int)cluster_ctarank() : 0;
+  const int first_unit = blockIdx.x / MC, unit_stride = gridDim.x / MC;
   const int kblocks = K / BK;
   volatile int* abort_flag = &ctl->abort;
 
@@ -85,7 +94,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), 1);
+      mbar_init(empty(s), MC);
       ctl->pending[s] = -1;
     }
     for (int a = 0; a < 2; ++a) {
@@ -107,6 +116,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
+  if (MC > 1) cluster_sync();  // the peer's barriers exist before anything is multicast to it
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -114,16 +124,23 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x) {
-        int mt, nt;
-        tile_coords(t, m_tiles, n_tiles, mt, nt);
+      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride) {
+        int mu, nt;
+        tile_coords(u, m_units, n_tiles, mu, nt);
+        const int mt = mu * MC + crank;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
           mbar_expect_tx(full(stage), STAGE_BYTES);
           ctl->pending[stage] = (int)phase;
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           tma_load_2d(sa, &tmA, kb * BK, mt * BM, full(stage));
-          tma_load_2d(sa + A_BYTES, &tmB, kb * BK, nt * BN, full(stage));
+          if (MC == 1) {
+            tma_load_2d(sa + A_BYTES, &tmB, kb * BK, nt * BN, full(stage));
+          } else {
+            constexpr int part = BN / MC;
+            tma_load_2d_mc(sa + A_BYTES + crank * part * BK * 2, &tmB, kb * BK, nt * BN + crank * part, full(stage),
+                           (uint16_t)((1u << MC) - 1));
+          }
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -135,7 +152,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     if (lane == 0) {
       int stage = 0, it = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < num_tiles && !*abort_flag; t += gridDim.x, ++it) {
+      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride, ++it) {
         const int acc = it & 1;
         const uint32_t aph = (it >> 1) & 1;
         if (!mbar_wait(tempty(acc), aph ^ 1, abort_flag)) break;
@@ -153,7 +170,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma(d, sdesc(sa + kk * 32), sdesc(sa + A_BYTES + kk * 32), IDESC, (kb | kk) != 0);
-          tc_commit(empty(stage));
+          if (MC == 1) tc_commit(empty(stage));
+          else tc_commit_mc(empty(stage), (uint16_t)((1u << MC) - 1));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -167,11 +185,12 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int half = pair_half(ep);
     int it = 0;
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++it) {
+    for (int u = first_unit; u < num_units; u += unit_stride, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      int mt, nt;
-      tile_coords(t, m_tiles, n_tiles, mt, nt);
+      int mu, nt;
+      tile_coords(u, m_units, n_tiles, mu, nt);
+      const int mt = mu * MC + crank;
       if (!mbar_wait(tfull(acc), aph, abort_flag)) break;
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
@@ -214,27 +233,269 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  if (MC > 1) cluster_sync();  // no CTA leaves while its peer may still multicast into it
+}
+
+
+// ---------------------------------------------------------------------------- CTA pairs
+//
+// 2-SM variant: a cluster of two CTAs computes a 256 x 256 tile with tcgen05.mma.cta_group::2
+// (M = 256, N = 256). CTA r stages rows r*128.. of the A tile and rows r*128.. of the B tile
+// (32 KB per stage instead of 48 KB), so each SM writes 64 B/clk into shared memory and the
+// tensor core reads 64 B/clk from it: together within shared-memory bandwidth, where the
+// 1-SM 128 x 256 tile needs ~192 B/clk. The even CTA issues the MMAs; both CTAs' TMA loads
+// complete on its ring barriers; its commits are multicast to both CTAs; each CTA reads
+// its own 128 accumulator rows from its own TMEM and releases them on the even CTA's barrier.
+constexpr int P_STAGES = 6;
+constexpr int P_STAGE_BYTES = 2 * BM * BK * 2;  // A half 16 KB + B half 16 KB
+struct CtrlPair {
+  uint64_t full[P_STAGES], empty[P_STAGES], tfull[2], tempty[2], fin;
+  uint32_t tmem_base;
+  int abort;
+  int pending[P_STAGES];
+};
+constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + (int)sizeof(CtrlPair);
+constexpr uint32_t IDESC_PAIR = tc::make_idesc(2 * BM, BN, false, false);
+
+
+__global__ void __launch_bounds__(THREADS, 1) gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                                                                  const __grid_constant__ CUtensorMap tmB,
+                                                                  EpiParams ep, int K, int* status) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  CtrlPair* ctl = reinterpret_cast<CtrlPair*>(smem + P_STAGES * P_STAGE_BYTES);
+  const uint32_t sbase = smem_u32(smem);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = ep.M, N = ep.N;
+  const int m_tiles = (M + BM - 1) / BM;
+  const int n_tiles = (N + BN - 1) / BN;
+  const int m_units = (m_tiles + 1) / 2;
+  const int num_units = m_units * n_tiles;
+  const int kblocks = K / BK;
+  const int crank = (int)cluster_ctarank();
+  const bool leader = crank == 0;
+  const int first_unit = blockIdx.x / 2, unit_stride = gridDim.x / 2;
+  volatile int* abort_flag = &ctl->abort;
+
+  auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
+  auto empty = [&](int s) { return smem_u32(&ctl->empty[s]); };
+  auto tfull = [&](int a) { return smem_u32(&ctl->tfull[a]); };
+  auto tempty = [&](int a) { return smem_u32(&ctl->tempty[a]); };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P_STAGES; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+      ctl->pending[s] = -1;
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull(a), 1);
+      mbar_init(tempty(a), 256);
+    }
+    mbar_init(smem_u32(&ctl->fin), 1);
+    ctl->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // one warp of each CTA of the pair allocates collectively
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride) {
+        int mu, nt;
+        tile_coords(u, m_units, n_tiles, mu, nt);
+        const int mt = mu * 2 + crank;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
+          const uint32_t fb = mapa_shared(full(stage), 0);
+          if (leader) {
+            mbar_expect_tx(full(stage), 2 * P_STAGE_BYTES);
+            ctl->pending[stage] = (int)phase;
+          }
+          const uint32_t sa = sbase + stage * P_STAGE_BYTES;
+          tma_load_2d_pair(sa, &tmA, kb * BK, mt * BM, fb);
+          tma_load_2d_pair(sa + BM * BK * 2, &tmB, kb * BK, nt * BN + crank * BM, fb);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {
+      int stage = 0, it = 0;
+      uint32_t phase = 0;
+      for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride, ++it) {
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(tempty(acc), aph ^ 1, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(full(stage), phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ctl->pending[stage] = -1;
+          tc_fence_after();
+          const uint32_t sa = sbase + stage * P_STAGE_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            tc_mma_pair(d, sdesc(sa + kk * 32), sdesc(sa + BM * BK * 2 + kk * 32), IDESC_PAIR, (kb | kk) != 0);
+          tc_commit_pair_mc(empty(stage), 0x3);
+          if (++stage == P_STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc_commit_pair_mc(tfull(acc), 0x3);
+      }
+    }
+  } else {
+    const int q = warp & 3;
+    const int half = pair_half(ep);
+    int it = 0;
+    for (int u = first_unit; u < num_units; u += unit_stride, ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      int mu, nt;
+      tile_coords(u, m_units, n_tiles, mu, nt);
+      const int mt = mu * 2 + crank;
+      if (!mbar_wait(tfull(acc), aph, abort_flag)) break;
+      tc_fence_after();
+      const int row = mt * BM + q * 32 + lane;
+      const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      for (int b0 = 0; b0 < BN; b0 += 2 * half) {
+        const int ncol = nt * BN + b0;
+        if (ncol >= N) break;
+        for (int c = 0; c < half; c += 32) {
+          float lo[32], hi[32];
+          tmem_ld32(tb + b0 + c, lo);
+          tmem_ld32(tb + b0 + half + c, hi);
+          if (row < M) apply_chunk32(ep, row, ncol + c, ncol + half + c, lo, hi);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
+    }
+  }
+
+  __syncthreads();
+  if (*abort_flag) {
+    if (threadIdx.x == 0) {
+      atomicOr(status, kStatusTimeout);
+      for (int s = 0; s < P_STAGES; ++s) {
+        const int ph = ctl->pending[s];
+        if (ph < 0) continue;
+        const uint64_t t0 = global_ns();
+        while (!mbar_try_wait(full(s), (uint32_t)ph) && global_ns() - t0 < kTimeoutNs) {
+        }
+      }
+    }
+    if (threadIdx.x == 32 && leader) {
+      tc_commit_pair_mc(smem_u32(&ctl->fin), 0x3);
+    }
+    if (threadIdx.x == 32) {
+      const uint64_t t0 = global_ns();
+      while (!mbar_try_wait(smem_u32(&ctl->fin), 0) && global_ns() - t0 < kTimeoutNs) {
+      }
+    }
+    __syncthreads();
+  }
+  cluster_sync();  // the leader's MMAs into both CTAs' TMEM are done before either frees it
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+  cluster_sync();
 }
 
 }  // namespace
 
+template <int MC>
+static cudaError_t launch_tc_mc(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& ep, int K,
+                                int num_sms, int* status, cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int m_units = ((ep.M + BM - 1) / BM + MC - 1) / MC;
+  const int units = m_units * ((ep.N + BN - 1) / BN);
+  const int clusters = units < num_sms / MC ? units : num_sms / MC;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * MC);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = MC;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MC>, ta, tb, ep, K, status);
+}
+
+static cudaError_t launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& ep, int K,
+                                  int num_sms, int* status, cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const int m_units = ((ep.M + BM - 1) / BM + 1) / 2;
+  const int units = m_units * ((ep.N + BN - 1) / BN);
+  const int clusters = units < num_sms / 2 ? units : num_sms / 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * 2);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = P_SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, ta, tb, ep, K, status);
+}
+
 cudaError_t launch_gemm_tc(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep, int num_sms,
-                           int* status, cudaStream_t stream) {
+                           int* status, cudaStream_t stream, int mode) {
   if (ep.M < 1 || ep.N < 1 || K < BK || K % BK || ep.N % 128 || lda % 8 ||
       (reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
     return cudaErrorNotSupported;
   CUtensorMap ta, tb;
-  if (!tma_map_bf16_2d(&ta, A, ep.M, K, lda, BK, BM, true) || !tma_map_bf16_2d(&tb, B, ep.N, K, K, BK, BN, true))
+  const int b_rows = mode == 0 ? BN : BN / 2;
+  if (!tma_map_bf16_2d(&ta, A, ep.M, K, lda, BK, BM, true) || !tma_map_bf16_2d(&tb, B, ep.N, K, K, BK, b_rows, true))
     return cudaErrorNotSupported;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
-  const int tiles = ((ep.M + BM - 1) / BM) * ((ep.N + BN - 1) / BN);
-  const int grid = tiles < num_sms ? tiles : num_sms;
-  gemm_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, ep, K, status);
+  cudaError_t e;
+  if (mode == 2) e = launch_tc_pair(ta, tb, ep, K, num_sms, status, stream);
+  else if (mode == 1) e = launch_tc_mc<2>(ta, tb, ep, K, num_sms, status, stream);
+  else e = launch_tc_mc<1>(ta, tb, ep, K, num_sms, status, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -21,8 +21,10 @@ cudaError_t launch_gemm_skinny(const bf16* A, int lda, const bf16* B, int K, con
                                float* scratch, int num_sms, cudaStream_t stream);
 // tcgen05 (TMEM accumulator, TMA-fed) GEMM; returns cudaErrorNotSupported if the shape is not
 // handled, so the caller can fall back to launch_gemm_tiled.
+// mode 0: one CTA per 128 x 256 tile; 1: CTA pairs share the weight tile through TMA
+// multicast; 2: CTA pairs run tcgen05.mma.cta_group::2 on 256 x 256 tiles.
 cudaError_t launch_gemm_tc(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
-                           int num_sms, int* status, cudaStream_t stream);
+                           int num_sms, int* status, cudaStream_t stream, int mode = 0);
 
 // ---- bookkeeping ------------------------------------------------------------------------
 constexpr int kBlobInts = 2000;

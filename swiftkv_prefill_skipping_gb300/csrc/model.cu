@@ -86,7 +86,7 @@ struct swiftkv_model {
   char* ws = nullptr;
   size_t ws_bytes = 0;
   bool globals_loaded = false;
-  int gemm_impl = 0;  // 0 tcgen05, 1 mma.sync tiles (GEMMs with > 64 rows)
+  int gemm_impl = 0;  // 0 tcgen05 CTA pairs, 1 mma.sync tiles, 2 tcgen05 single CTA (GEMMs with > 64 rows)
   int attn_impl = 0;  // 0 tcgen05 when d_head == 128, 1 mma.sync
   // profiling (swiftkv_profile_begin/end)
   bool prof_on = false;
@@ -282,7 +282,8 @@ int gemm(Ctx& x, const char* name, const bf16* A, int lda, const bf16* B, int K,
     e = launch_gemm_skinny(A, lda, B, K, ep, x.w.part, x.m->num_sms, x.s);
   } else {
     e = cudaErrorNotSupported;
-    if (x.m->gemm_impl == 0) e = launch_gemm_tc(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s);
+    if (x.m->gemm_impl == 0) e = launch_gemm_tc(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s, 2);
+    else if (x.m->gemm_impl == 2) e = launch_gemm_tc(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s, 0);
     if (e == cudaErrorNotSupported) e = launch_gemm_tiled(A, lda, B, K, ep, x.s);
   }
   if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "gemm M=%d N=%d K=%d: %s", ep.M, ep.N, K, cudaGetErrorString(e));
@@ -607,7 +608,7 @@ int swiftkv_status(swiftkv_model* m, int clear) {
 
 int swiftkv_set_gemm_impl(swiftkv_model* m, int impl) {
   if (!m) return fail(SWIFTKV_EINVAL, "null model");
-  if (impl != 0 && impl != 1) return fail(SWIFTKV_EINVAL, "gemm impl %d", impl);
+  if (impl < 0 || impl > 2) return fail(SWIFTKV_EINVAL, "gemm impl %d", impl);
   m->gemm_impl = impl;
   return SWIFTKV_OK;
 }
@@ -644,8 +645,8 @@ int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int 
   cudaError_t e = cudaSuccess;
   const bf16* a = static_cast<const bf16*>(A);
   const bf16* b = static_cast<const bf16*>(B);
-  if (impl == 0) {
-    e = launch_gemm_tc(a, K, b, K, ep, sms, st, s);
+  if (impl == 0 || impl == 3 || impl == 4) {
+    e = launch_gemm_tc(a, K, b, K, ep, sms, st, s, impl == 0 ? 0 : (impl == 3 ? 1 : 2));
   } else if (impl == 1) {
     e = launch_gemm_tiled(a, K, b, K, ep, s);
   } else if (impl == 2) {

@@ -180,7 +180,7 @@ def test_gemm_families_agree_within_oracle_tolerance():
     batch = synth.prompt_batch(SMALL128.vocab, 3, 0, 0, lens=lens)
     idx, caches, ref_logits, _ = oracle_prefill(SMALL128, 3, 1, batch, gain_std=0.1)
     out = {}
-    for impl in (0, 1):
+    for impl in (0, 1, 2):
         from swiftkv_prefill_skipping_gb300 import api
         m = api.load_synthetic(SMALL128, 3, 1, gain_std=0.1)
         binding.check(binding.lib().swiftkv_set_gemm_impl(m.handle, impl))
