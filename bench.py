@@ -380,7 +380,7 @@ def run_ours(args, w, rank, world, local_rank):
 
 def traffic_per_launch(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or None when the
-    summary is absent or was taken on a different build of the kernel's source."""
+    summary is absent or was taken on a different build of the kernel's sources."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.md")
     if not os.path.exists(p):
         return None
@@ -389,15 +389,19 @@ def traffic_per_launch(kernel: str):
     with open(p) as f:
         for line in f:
             if line.startswith("traffic|"):
-                _, name, src, digest, bytes_ = line.strip().split("|")
-                rows[name] = (src, digest, float(bytes_))
+                _, name, srcs, digest, bytes_ = line.strip().split("|")
+                rows[name] = (srcs.split("+"), digest, float(bytes_))
     if kernel not in rows:
         return None
-    src, digest, b = rows[kernel]
-    path = os.path.join(ROOT, src)
-    if not os.path.exists(path) or hashlib.sha256(open(path, "rb").read()).hexdigest()[:16] != digest:
-        return None
-    return b
+    srcs, digest, b = rows[kernel]
+    h = hashlib.sha256()
+    for src in srcs:
+        path = os.path.join(ROOT, src)
+        if not os.path.exists(path):
+            return None
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return b if h.hexdigest()[:16] == digest else None
 
 
 def main():
