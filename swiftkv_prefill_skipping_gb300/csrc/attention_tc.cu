@@ -6,14 +6,16 @@
 //              per 64-key block the K and V rows of its four 16-token pages (each page
 //              row block is contiguous in the pool) into a 3-stage ring
 //   warp 1     allocates TMEM; one lane issues S = Q K^T (M=128, N=64, K=128) into one of
-//              two 64-column S buffers, and O_blk = P V (M=128, N=128, K=64; fp16 operands,
-//              V used as an MN-major operand in the cache's own row layout) into one of two
-//              128-column buffers; S of block j+1 is issued before P V of block j so the
+//              two 64-column S buffers, and O += P V (M=128, N=128, K=64; fp16 operands,
+//              V used as an MN-major operand in the cache's own row layout) into one
+//              128-column accumulator; S of block j+1 is issued before P V of block j so the
 //              tensor core works while the softmax warps do
-//   warps 2-5  one thread per query row: tcgen05.ld its S row, causal/length mask, online
-//              softmax in the log2 domain, P (fp16) into shared memory in the swizzled
-//              K-major layout the MMA reads; then O = O * alpha + O_blk in registers from
-//              the previous block's P V result; finally O / l to global memory
+//   warps 2-5  one thread per query row: tcgen05.ld its S row, causal/length mask (only on
+//              blocks that cross the diagonal or the prompt end), online softmax in the log2
+//              domain with a running max allowed to lag by up to 2^8 (O, accumulated across
+//              blocks in TMEM by the MMA, is rescaled in place only when it moves further),
+//              P (fp16) into shared memory in the swizzled K-major layout the MMA reads;
+//              finally O / l from TMEM to global memory
 // All mbarrier waits are bounded; on a timeout the CTA flags kStatusTimeout, drains its
 // own TMA copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
@@ -41,12 +43,13 @@ constexpr int KV_HALF = BKV * 64 * 2;          // 8 KB: 64 keys x 64 dims
 constexpr int K_BYTES = 2 * KV_HALF;           // 16 KB
 constexpr int STAGE_BYTES = 2 * K_BYTES;       // K + V
 constexpr int P_BYTES = BQ * BKV * 2;          // 16 KB
-constexpr int TMEM_COLS = 512;                 // S: 2 x 64, O blocks: 2 x 128
+constexpr int TMEM_COLS = 256;                 // S: 2 x 64, O: 128 (accumulated across blocks)
 constexpr int S_COL = 0, O_COL = 128;
+constexpr float kStaleMax = 8.f;               // log2 headroom before O is rescaled
 
 struct Ctrl {
   uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], v_ready[KV_STAGES], s_full[2], s_empty[2],
-      p_full[2], o_full[2], o_empty[2], fin;
+      p_full[2], pv_done[2], fin;
   uint32_t tmem_base;
   int abort;
   int pending[KV_STAGES + 1];
@@ -71,6 +74,28 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Stores 32 consecutive fp32 columns of this thread's TMEM lane and waits for the store.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  uint32_t r[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(v[i]);
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n"
+      "tcgen05.wait::st.sync.aligned;\n" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+      "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+      "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
@@ -113,8 +138,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
       mbar_init(bar(ctl->s_full[i]), 1);
       mbar_init(bar(ctl->s_empty[i]), 128);
       mbar_init(bar(ctl->p_full[i]), 128);
-      mbar_init(bar(ctl->o_full[i]), 1);
-      mbar_init(bar(ctl->o_empty[i]), 128);
+      mbar_init(bar(ctl->pv_done[i]), 1);
     }
     mbar_init(bar(ctl->fin), 1);
     ctl->abort = 0;
@@ -192,7 +216,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
         const int pb = j & 1;
         const uint32_t ph = (uint32_t)((j >> 1) & 1);
         if (!mbar_wait(bar(ctl->p_full[pb]), ph, abort_flag)) break;
-        if (!mbar_wait(bar(ctl->o_empty[pb]), ph ^ 1, abort_flag)) break;
         const int st = j % KV_STAGES;
         if (!mbar_wait(bar(ctl->v_ready[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) break;
         tc_fence_after();
@@ -201,10 +224,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk) {
           // P: K-major, rows of 64 keys; V: MN-major, 64-dim halves 8 KB apart, 8-key groups 1 KB apart
-          tc_mma(tmem + O_COL + pb * D, sdesc(pbase + kk * 32), sdesc_sw128(sv + kk * 2048, KV_HALF, 1024),
-                 IDESC_O, kk != 0);
+          tc_mma(tmem + O_COL, sdesc(pbase + kk * 32), sdesc_sw128(sv + kk * 2048, KV_HALF, 1024), IDESC_O,
+                 (j | kk) != 0);
         }
-        tc_commit(bar(ctl->o_full[pb]));
+        tc_commit(bar(ctl->pv_done[pb]));
         tc_commit(bar(ctl->kv_empty[st]));
       }
     }
@@ -231,31 +254,18 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
       mbar_arrive(bar(ctl->v_ready[st]));
     }
   } else {
-    // softmax / output warps: thread <-> query row
+    // softmax / output warps: thread <-> query row. O accumulates in TMEM across blocks; the
+    // probabilities use a running max that may lag the true one by up to 2^kStaleMax (they
+    // then stay <= 256, fine for fp16); only when a row's max moves further is O rescaled,
+    // by the warp, in TMEM, after the previous block's P V has landed.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int qpos = q0 + r;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    float o[D];
-#pragma unroll
-    for (int i = 0; i < D; ++i) o[i] = 0.f;
-    float m = -FLT_MAX, l = 0.f, alpha_prev = 1.f;
+    float m = -INFINITY, l = 0.f;
     bool ok = true;
-
-    auto accumulate = [&](int j, float alpha) -> bool {
-      const int ob = j & 1;
-      if (!mbar_wait(bar(ctl->o_full[ob]), (uint32_t)((j >> 1) & 1), abort_flag)) return false;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        float t[32];
-        tmem_ld32(tmem + lane_off + O_COL + ob * D + c, t);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c + i] = o[c + i] * alpha + t[i];
-      }
-      tc_fence_before();
-      mbar_arrive(bar(ctl->o_empty[ob]));
-      return true;
+    auto wait_pv = [&](int j) -> bool {
+      return mbar_wait(bar(ctl->pv_done[j & 1]), (uint32_t)((j >> 1) & 1), abort_flag);
     };
 
     for (int j = 0; j < nblk; ++j) {
@@ -270,24 +280,53 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
       tmem_ld32(tmem + lane_off + S_COL + sb * BKV + 32, sc + 32);
       tc_fence_before();
       mbar_arrive(bar(ctl->s_empty[sb]));
-      float mx = -FLT_MAX;
+      const bool interior = (j + 1) * BKV - 1 <= q0 && (j + 1) * BKV <= n;  // no key masked in any row
+      if (!interior) {
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) {
-        const int key = j * BKV + i;
-        sc[i] = (key <= qpos && key < n) ? sc[i] * scale_log2 : -INFINITY;
-        mx = fmaxf(mx, sc[i]);
+        for (int i = 0; i < BKV; ++i) {
+          const int key = j * BKV + i;
+          if (key > qpos || key >= n) sc[i] = -INFINITY;
+        }
       }
-      const float mn = fmaxf(m, mx);
-      const float alpha = exp2f(m - mn);
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, sc[i]);
+      mx *= scale_log2;
+      const bool move = mx > m + kStaleMax;
+      if (__any_sync(0xffffffffu, move)) {
+        const float mn = move ? mx : m;
+        const float factor = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+        if (j > 0) {  // O holds blocks 0..j-1: wait for the last of them, rescale the warp's rows
+          if (!wait_pv(j - 1)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            float t[32];
+            tmem_ld32(tmem + lane_off + O_COL + c, t);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) t[i] *= factor;
+            tmem_st32(tmem + lane_off + O_COL + c, t);
+          }
+        }
+        l *= factor;
+        m = mn;
+      }
+      const float mneg = -m;
       float rs = 0.f;
 #pragma unroll
       for (int i = 0; i < BKV; ++i) {
-        sc[i] = exp2f(sc[i] - mn);
+        sc[i] = ex2_approx(fmaf(sc[i], scale_log2, mneg));
         rs += sc[i];
       }
-      m = mn;
-      l = l * alpha + rs;
-      // P row -> shared memory, 128B-swizzled K-major (row r: 8 chunks of 8 bf16)
+      l += rs;
+      // P buffer sb was last read by the P V of block j-2
+      if (j >= 2 && !wait_pv(j - 2)) {
+        ok = false;
+        break;
+      }
       unsigned char* prow = sP_gen + sb * P_BYTES + r * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
@@ -299,26 +338,29 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
         *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
       }
       fence_proxy_async_smem();
+      tc_fence_before();
       mbar_arrive(bar(ctl->p_full[sb]));
-      // the previous block's P V is folded in with the scale it was computed under
-      if (j > 0 && !accumulate(j - 1, alpha_prev)) {
-        ok = false;
-        break;
-      }
-      alpha_prev = alpha;
     }
-    if (ok && nblk > 0) ok = accumulate(nblk - 1, alpha_prev);
-    if (ok && qpos < n) {
+    if (ok && nblk > 0) ok = wait_pv(nblk - 1);
+    if (ok) {
+      tc_fence_after();
       const float inv = 1.f / l;
-      bf16* dst = out + (size_t)(seq0 + qpos) * ldo + h * D;
+      bf16* dst = out + (size_t)(seq0 + min(qpos, n - 1)) * ldo + h * D;
 #pragma unroll
-      for (int c = 0; c < D; c += 8) {
-        uint4 u;
-        u.x = pack_bf16(o[c] * inv, o[c + 1] * inv);
-        u.y = pack_bf16(o[c + 2] * inv, o[c + 3] * inv);
-        u.z = pack_bf16(o[c + 4] * inv, o[c + 5] * inv);
-        u.w = pack_bf16(o[c + 6] * inv, o[c + 7] * inv);
-        *reinterpret_cast<uint4*>(dst + c) = u;
+      for (int c = 0; c < D; c += 32) {
+        float t[32];
+        tmem_ld32(tmem + lane_off + O_COL + c, t);
+        if (qpos < n) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 u;
+            u.x = pack_bf16(t[e] * inv, t[e + 1] * inv);
+            u.y = pack_bf16(t[e + 2] * inv, t[e + 3] * inv);
+            u.z = pack_bf16(t[e + 4] * inv, t[e + 5] * inv);
+            u.w = pack_bf16(t[e + 6] * inv, t[e + 7] * inv);
+            *reinterpret_cast<uint4*>(dst + c + e) = u;
+          }
+        }
       }
     }
   }
