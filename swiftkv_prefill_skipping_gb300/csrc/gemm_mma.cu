@@ -6,9 +6,12 @@
 //
 // gemm_tiled: 128x128x32 CTA tiles, 8 warps (64x32 each), 4-stage cp.async ring,
 //             fp32 tile staged through shared memory for the pairwise epilogue.
-// gemm_skinny: M <= 64 rows (the last-token tail, decode, LM head): streams the
-//             weights once with split-K across CTAs; fp32 partials are reduced in a
-//             fixed order by reduce_epilogue (deterministic), which applies the epilogue.
+// gemv:       M <= 64 rows (the last-token tail, decode, LM head): one CTA per pair of
+//             16-column strips over the whole K, warps split K, fixed-order reduction in
+//             shared memory; what the model uses for its M <= 64 GEMMs.
+// gemm_skinny: the same rows with split-K across CTAs and fp32 partials in global scratch,
+//             reduced in a fixed order by reduce_epilogue (used by the allocation-free entry
+//             point and as a cross-check).
 #include "common.cuh"
 #include "launch.h"
 
@@ -242,7 +245,144 @@ __global__ void reduce_epilogue_kernel(const float* __restrict__ part, int split
   }
 }
 
+
+// ---------------------------------------------------------------------------- skinny, no split-K
+//
+// gemv_kernel: M <= 64 rows (the last-token tail, decode, LM head) streaming the weights
+// once at HBM rate. A CTA owns two 16-column strips that are `half` apart, so RoPE and SwiGLU
+// partners (n, n + half) stay inside the CTA; its 4 warps take interleaved 64-deep k-tiles,
+// each with its own 4-stage cp.async ring, and their partial sums are added in a fixed order
+// in shared memory before the epilogue. One launch, no global scratch, deterministic.
+constexpr int GV_STAGES = 4, GV_LD = 64 + 8;
+
+template <int MB>
+__global__ void __launch_bounds__(128) gemv_kernel(const bf16* __restrict__ A, int lda,
+                                                   const bf16* __restrict__ B, int K, EpiParams ep) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int WROWS = 32, AROWS = MB * 16;
+  constexpr int STAGE = (WROWS + AROWS) * GV_LD;  // bf16 elements per stage per warp
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int M = ep.M;
+  const int half = pair_half(ep);
+  const int strips = half / 16;
+  const int blk = blockIdx.x / strips, strip = blockIdx.x % strips;
+  const int col_lo = blk * 2 * half + strip * 16;  // local cols 0..15 -> col_lo.., 16..31 -> col_lo+half..
+  bf16* ring = reinterpret_cast<bf16*>(smem) + warp * GV_STAGES * STAGE;
+  const int ktiles = K / 64;
+  const int my_tiles = ktiles > warp ? (ktiles - warp + 3) / 4 : 0;
+
+  auto load = [&](int stage, int i) {
+    const int k0 = (warp + 4 * i) * 64;
+    bf16* sw = ring + stage * STAGE;
+    bf16* sa = sw + WROWS * GV_LD;
+#pragma unroll
+    for (int c = 0; c < (WROWS * 8) / 32; ++c) {  // 256 chunks of 16 B
+      const int id = c * 32 + lane, row = id >> 3, kc = id & 7;
+      const int n = row < 16 ? col_lo + row : col_lo + half + (row - 16);
+      cp_async16(smem_u32(sw + row * GV_LD + kc * 8), B + (size_t)n * K + k0 + kc * 8, 16);
+    }
+#pragma unroll
+    for (int c = 0; c < (AROWS * 8) / 32; ++c) {
+      const int id = c * 32 + lane, row = id >> 3, kc = id & 7;
+      const bf16* src = A + (size_t)(row < M ? row : 0) * lda + k0 + kc * 8;
+      cp_async16(smem_u32(sa + row * GV_LD + kc * 8), src, row < M ? 16 : 0);
+    }
+  };
+
+  float acc[MB][4][4];
+#pragma unroll
+  for (int a = 0; a < MB; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[a][b][c] = 0.f;
+
+#pragma unroll
+  for (int s = 0; s < GV_STAGES - 1; ++s) {
+    if (s < my_tiles) load(s, s);
+    cp_async_commit();
+  }
+  for (int i = 0; i < my_tiles; ++i) {
+    cp_async_wait<GV_STAGES - 2>();
+    __syncwarp();
+    if (i + GV_STAGES - 1 < my_tiles) load((i + GV_STAGES - 1) % GV_STAGES, i + GV_STAGES - 1);
+    cp_async_commit();
+    const bf16* sw = ring + (i % GV_STAGES) * STAGE;
+    const bf16* sa = sw + WROWS * GV_LD;
+#pragma unroll
+    for (int kk = 0; kk < 64; kk += 16) {
+      uint32_t bfr[4][2];
+#pragma unroll
+      for (int nj = 0; nj < 2; ++nj) {
+        const int row = nj * 16 + (lane & 7) + ((lane >> 4) << 3);
+        const int col = kk + ((lane >> 3) & 1) * 8;
+        ldmatrix_x4(smem_u32(sw + row * GV_LD + col), bfr[2 * nj][0], bfr[2 * nj][1], bfr[2 * nj + 1][0],
+                    bfr[2 * nj + 1][1]);
+      }
+#pragma unroll
+      for (int mi = 0; mi < MB; ++mi) {
+        uint32_t af[4];
+        const int row = mi * 16 + (lane & 15);
+        const int col = kk + (lane >> 4) * 8;
+        ldmatrix_x4(smem_u32(sa + row * GV_LD + col), af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nb = 0; nb < 4; ++nb) mma_bf16_16816(acc[mi][nb], af, bfr[nb]);
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+  // partial sums -> shared memory [warp][row][32], then a fixed-order sum over the warps
+  float* red = reinterpret_cast<float*>(smem);
+#pragma unroll
+  for (int mi = 0; mi < MB; ++mi)
+#pragma unroll
+    for (int nb = 0; nb < 4; ++nb) {
+      const int r = mi * 16 + (lane >> 2), c = nb * 8 + 2 * (lane & 3);
+      float* base = red + (warp * AROWS) * 32;
+      base[r * 32 + c] = acc[mi][nb][0];
+      base[r * 32 + c + 1] = acc[mi][nb][1];
+      base[(r + 8) * 32 + c] = acc[mi][nb][2];
+      base[(r + 8) * 32 + c + 1] = acc[mi][nb][3];
+    }
+  __syncthreads();
+  for (int u = threadIdx.x; u < M * 16; u += 128) {
+    const int m = u >> 4, c = u & 15;
+    float a = 0.f, b = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      a += red[(w * AROWS + m) * 32 + c];
+      b += red[(w * AROWS + m) * 32 + 16 + c];
+    }
+    apply_pair(ep, m, col_lo + c, col_lo + half + c, a, b);
+  }
+}
+
+template <int MB>
+static cudaError_t launch_gemv_mb(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
+                                  cudaStream_t stream) {
+  constexpr int smem = 4 * GV_STAGES * (32 + MB * 16) * GV_LD * 2;
+  static_assert(4 * MB * 16 * 32 * 4 <= smem, "reduction buffer must fit the rings");
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  gemv_kernel<MB><<<ep.N / 32, 128, smem, stream>>>(A, lda, B, K, ep);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_gemv(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep, cudaStream_t stream) {
+  if (ep.M < 1 || ep.M > 64 || K % 64 || ep.N % 128) return cudaErrorNotSupported;
+  if (ep.M <= 16) return launch_gemv_mb<1>(A, lda, B, K, ep, stream);
+  if (ep.M <= 32) return launch_gemv_mb<2>(A, lda, B, K, ep, stream);
+  if (ep.M <= 48) return launch_gemv_mb<3>(A, lda, B, K, ep, stream);
+  return launch_gemv_mb<4>(A, lda, B, K, ep, stream);
+}
 
 int skinny_splits(int M, int N, int K, int num_sms) {
   (void)M;

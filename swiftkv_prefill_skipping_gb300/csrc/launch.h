@@ -19,6 +19,8 @@ int skinny_splits(int M, int N, int K, int num_sms);
 size_t skinny_scratch_bytes(int M, int N, int K, int num_sms);
 cudaError_t launch_gemm_skinny(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
                                float* scratch, int num_sms, cudaStream_t stream);
+// M <= 64 without split-K: each CTA streams 32 weight rows over the full K (no scratch).
+cudaError_t launch_gemv(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep, cudaStream_t stream);
 // tcgen05 (TMEM accumulator, TMA-fed) GEMM; returns cudaErrorNotSupported if the shape is not
 // handled, so the caller can fall back to launch_gemm_tiled.
 // mode 0: one CTA per 128 x 256 tile; 1: CTA pairs share the weight tile through TMA

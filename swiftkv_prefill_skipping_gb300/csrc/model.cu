@@ -276,10 +276,11 @@ int gemm(Ctx& x, const char* name, const bf16* A, int lda, const bf16* B, int K,
          double flops) {
   const bool skinny = ep.M <= 64;
   const double bytes = (double)ep.N * K * 2 + (double)ep.M * K * 2;
-  Prof pr(x.m, x.s, name, skinny ? 2 : 1, flops, bytes);
+  Prof pr(x.m, x.s, name, 1, flops, bytes);
   cudaError_t e;
   if (skinny) {
-    e = launch_gemm_skinny(A, lda, B, K, ep, x.w.part, x.m->num_sms, x.s);
+    e = launch_gemv(A, lda, B, K, ep, x.s);
+    if (e == cudaErrorNotSupported) e = launch_gemm_skinny(A, lda, B, K, ep, x.w.part, x.m->num_sms, x.s);
   } else {
     e = cudaErrorNotSupported;
     if (x.m->gemm_impl == 0) e = launch_gemm_tc(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s, 2);
@@ -649,6 +650,8 @@ int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int 
     e = launch_gemm_tc(a, K, b, K, ep, sms, st, s, impl == 0 ? 0 : (impl == 3 ? 1 : 2));
   } else if (impl == 1) {
     e = launch_gemm_tiled(a, K, b, K, ep, s);
+  } else if (impl == 5) {
+    e = M > 64 ? cudaErrorNotSupported : launch_gemv(a, K, b, K, ep, s);
   } else if (impl == 2) {
     if (M > 64) e = cudaErrorNotSupported;
     else {

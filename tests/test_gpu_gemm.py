@@ -57,3 +57,13 @@ def test_tcgen05_is_deterministic():
     c1, _ = _run(0, 777, 1024, 1024, seed=3)
     c2, _ = _run(0, 777, 1024, 1024, seed=3)
     assert torch.equal(c1, c2)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (16, 1024, 512), (64, 128, 14336), (37, 2048, 704),
+                                   (48, 128256, 256)])
+def test_gemv_matches_torch_fp32(M, N, K):
+    import torch
+    Cm, ref = _run(5, M, N, K)
+    assert not torch.isnan(Cm).any()
+    err = (Cm - ref).abs().max().item() / ref.abs().max().item()
+    assert err < 2e-5, (M, N, K, err)
