@@ -121,34 +121,51 @@ __global__ void __launch_bounds__(RN_THREADS) embed_rmsnorm_kernel(const int* __
   }
 }
 
+// One row per CTA; each thread owns 8-element chunks (two 16-byte fp32 loads, one 16-byte
+// bf16 store), so every global access is a full 16-byte vector.
 __global__ void __launch_bounds__(RN_THREADS) rmsnorm_kernel(const float* __restrict__ x,
                                                              const int* __restrict__ rows, int d,
                                                              const float* __restrict__ gamma, float eps,
                                                              bf16* __restrict__ u, float* __restrict__ x_out) {
   __shared__ float red[RN_THREADS / 32];
+  constexpr int MAXC = RN_MAXV / 2;  // 8-element chunks per thread: d <= 8192
   const int t = blockIdx.x;
   const int src = rows ? rows[t] : t;
   const float4* xr = reinterpret_cast<const float4*>(x + (size_t)src * d);
-  const int n4 = d >> 2;
-  float4 v[RN_MAXV];
+  const int n8 = d >> 3;
+  float4 v[MAXC][2];
   float ss = 0.f;
 #pragma unroll
-  for (int i = 0; i < RN_MAXV; ++i) {
-    int c = threadIdx.x + i * RN_THREADS;
-    if (c < n4) {
-      v[i] = xr[c];
-      ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-      if (x_out) reinterpret_cast<float4*>(x_out + (size_t)t * d)[c] = v[i];
+  for (int i = 0; i < MAXC; ++i) {
+    const int c = threadIdx.x + i * RN_THREADS;
+    if (c < n8) {
+      v[i][0] = xr[2 * c];
+      v[i][1] = xr[2 * c + 1];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+        ss += v[i][h].x * v[i][h].x + v[i][h].y * v[i][h].y + v[i][h].z * v[i][h].z + v[i][h].w * v[i][h].w;
+      if (x_out) {
+        reinterpret_cast<float4*>(x_out + (size_t)t * d)[2 * c] = v[i][0];
+        reinterpret_cast<float4*>(x_out + (size_t)t * d)[2 * c + 1] = v[i][1];
+      }
     }
   }
   const float r = rsqrtf(block_sum(ss, red) / d + eps);
 #pragma unroll
-  for (int i = 0; i < RN_MAXV; ++i) {
-    int c = threadIdx.x + i * RN_THREADS;
-    if (c < n4) {
-      float4 g = gamma ? reinterpret_cast<const float4*>(gamma)[c] : make_float4(1.f, 1.f, 1.f, 1.f);
-      float4 o = make_float4(v[i].x * r * g.x, v[i].y * r * g.y, v[i].z * r * g.z, v[i].w * r * g.w);
-      store_bf16x4(u + (size_t)t * d + 4 * c, o);
+  for (int i = 0; i < MAXC; ++i) {
+    const int c = threadIdx.x + i * RN_THREADS;
+    if (c < n8) {
+      float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
+      if (gamma) {
+        g0 = reinterpret_cast<const float4*>(gamma)[2 * c];
+        g1 = reinterpret_cast<const float4*>(gamma)[2 * c + 1];
+      }
+      uint4 pk;
+      pk.x = pack_bf16(v[i][0].x * r * g0.x, v[i][0].y * r * g0.y);
+      pk.y = pack_bf16(v[i][0].z * r * g0.z, v[i][0].w * r * g0.w);
+      pk.z = pack_bf16(v[i][1].x * r * g1.x, v[i][1].y * r * g1.y);
+      pk.w = pack_bf16(v[i][1].z * r * g1.z, v[i][1].w * r * g1.w);
+      *reinterpret_cast<uint4*>(u + (size_t)t * d + 8 * c) = pk;
     }
   }
 }
