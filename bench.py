@@ -104,9 +104,43 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- workload
 
-def workload_batch(w, rank: int):
+def workload_batch(w, rank: int, reserve_tokens: int = 0):
+    """Each replica prefills its own prompts (weak scaling): the input seed depends on the rank."""
     return synth.prompt_batch(w.shape.vocab, w.num_prompts, w.len_lo, w.len_hi, w.page_size,
-                              seed=synth.SEED_INPUTS + 1000 * rank)
+                              reserve_tokens=reserve_tokens, seed=synth.SEED_INPUTS + 1000 * rank)
+
+
+def replica_barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the timing rule: the slowest replica sets the time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device=None) -> float:
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def whole_job_throughput(units_all_ranks: float, steps: int, seconds: float) -> float:
+    """Units all ranks processed (per step, summed over ranks) divided by the max-over-ranks
+    elapsed time."""
+    return units_all_ranks * steps / seconds
 
 
 def gen_weights(w, keep_raw: bool):
@@ -226,7 +260,8 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks, peak_src = load_peaks()
-    batch = workload_batch(w, rank)
+    n_dec_req = args.decode_steps if args.decode_steps is not None else w.decode_steps
+    batch = workload_batch(w, rank, reserve_tokens=n_dec_req + 1 if n_dec_req > 0 else 0)
     T, P = int(batch.cu_seqlens[-1]), int(len(batch.lens))
     want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
 
@@ -253,8 +288,7 @@ def run_ours(args, w, rank, world, local_rank):
         api.prefill(model, tokens, batch.cu_seqlens, kv, logits=logits, stream=stream)
 
     def barrier():
-        if world > 1:
-            dist.barrier()
+        replica_barrier(world)
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -280,13 +314,10 @@ def run_ours(args, w, rank, world, local_rank):
     n_ent = binding.check(binding.lib().swiftkv_profile_end(model.handle, entries, 64))
     clocks = sampler.stop()
     barrier()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / args.steps
-    value = T * args.steps * world / (ms / 1e3)
+    T_all = sum_over_ranks(T, world, dev)
+    value = whole_job_throughput(T_all, args.steps, ms / 1e3)
 
     prof = {}
     for i in range(n_ent):
@@ -296,8 +327,8 @@ def run_ours(args, w, rank, world, local_rank):
     launches = sum(v["kernels"] for v in prof.values())
 
     fl = FL.prefill_flops(w.shape, batch.lens, w.l, w.g)
-    dense_tflops = fl["dense_equiv"] * args.steps * world / (ms / 1e3) / 1e12
-    exec_tflops = fl["executed"] * args.steps * world / (ms / 1e3) / 1e12
+    dense_tflops = sum_over_ranks(fl["dense_equiv"], world, dev) * args.steps / (ms / 1e3) / 1e12
+    exec_tflops = sum_over_ranks(fl["executed"], world, dev) * args.steps / (ms / 1e3) / 1e12
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
 
@@ -333,14 +364,33 @@ def run_ours(args, w, rank, world, local_rank):
         t1 = time.perf_counter()
         for _ in range(args.steps):
             api.prefill_host(model, h_tok_np, batch.cu_seqlens, kv, logits=h_log_np, stream=stream)
-        el = time.perf_counter() - t1
-        if world > 1:
-            t = torch.tensor([el], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            el = float(t.item())
-        e2e = {"value": T * args.steps * world / el, "unit": "tokens/s",
+        el = max_over_ranks(time.perf_counter() - t1, world, dev)
+        e2e = {"value": whole_job_throughput(T_all, args.steps, el), "unit": "tokens/s",
                "h2d_bytes_per_step": T * 4 + (P + 1) * 4, "d2h_bytes_per_step": P * w.shape.vocab * 4,
                "ms_per_step": 1e3 * el / args.steps}
+
+    # decode from the filled caches (greedy, every sequence one token per step): TPOT
+    decode = None
+    n_dec = args.decode_steps if args.decode_steps is not None else w.decode_steps
+    if n_dec > 0:
+        if batch.block_table.shape[1] * 16 < int(batch.lens.max()) + n_dec:
+            raise RuntimeError("block table too small for the decode steps")
+        api.prefill(model, tokens, batch.cu_seqlens, kv, logits=logits, stream=stream)
+        nxt = torch.argmax(logits, dim=-1).to(torch.int32)
+        lens = [int(x) for x in batch.lens]
+        api.decode_step(model, nxt, lens, kv, stream=stream)           # warm-up step
+        lens = [x + 1 for x in lens]
+        torch.cuda.synchronize()
+        d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d0.record(stream)
+        for _ in range(n_dec):
+            _, nxt = api.decode_step(model, nxt, lens, kv, stream=stream)
+            lens = [x + 1 for x in lens]
+        d1.record(stream)
+        torch.cuda.synchronize()
+        tpot = max_over_ranks(d0.elapsed_time(d1) / n_dec, world, dev)
+        decode = {"steps": n_dec, "batch": P, "tpot_ms": tpot, "ttft_ms": ms_per_step,
+                  "decode_tokens_per_s": P * 1e3 / tpot}
 
     cpu = None
     if want_cpu:
@@ -367,6 +417,7 @@ def run_ours(args, w, rank, world, local_rank):
             "executed_tflops": exec_tflops,
             "executed_frac_of_peak": {"burst": exec_tflops / peak_burst, "sustained": exec_tflops / peak_sus},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "decode": decode,
             "clocks": clocks,
             "kernels": {k: {"ms_per_step": v["ms"] / args.steps, "calls_per_step": v["calls"] / args.steps,
                             "tflops": (v["flops"] / (v["ms"] / 1e3) / 1e12) if v["flops"] else None,
@@ -415,6 +466,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="greedy decode steps timed after the prefill (default: the workload's own)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -153,6 +153,8 @@ WORKLOADS = {
     w.name: w for w in [
         Workload("tiny_l2", TINY, l=2, g=1, num_prompts=1, len_lo=128, len_hi=128, decode_steps=8),
         Workload("llama8b_l16", LLAMA8B, l=16, g=1, num_prompts=16, len_lo=500, len_hi=1000),
+        # the same prompts through the ordinary model (l = L): the baseline SwiftKV is measured against
+        Workload("llama8b_full", LLAMA8B, l=32, g=1, num_prompts=16, len_lo=500, len_hi=1000),
         Workload("llama8b_l24", LLAMA8B, l=24, g=1, num_prompts=32, len_lo=500, len_hi=1000),
         Workload("llama8b_l24_g2", LLAMA8B, l=24, g=2, num_prompts=32, len_lo=500, len_hi=1000),
         Workload("llama8b_l16_g2", LLAMA8B, l=16, g=2, num_prompts=32, len_lo=500, len_hi=1000),

@@ -115,7 +115,7 @@ def test_llama8b_l16_full_workload():
     _run_workload("llama8b_l16")
 
 
-@pytest.mark.parametrize("name", ["llama8b_l24", "llama8b_l24_g2", "llama8b_l16_g2"])
+@pytest.mark.parametrize("name", ["llama8b_l24", "llama8b_l24_g2", "llama8b_l16_g2", "llama8b_full"])
 def test_llama8b_acrosskv_and_l24_workloads(name):
     _run_workload(name)
 
