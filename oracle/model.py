@@ -405,6 +405,53 @@ def swiftkv_decode_step(cfg: Config, w: Weights, caches: List[KV], token: int, l
     return out, lm_head(cfg, w, x)[0]
 
 
+def swiftkv_forward_one(cfg: Config, w: Weights, caches: Optional[List[KV]], tokens: Sequence[int], l: int,
+                        g: int = 1) -> Tuple[List[KV], np.ndarray]:
+    """One chunk of a sequence whose caches already hold its first ctx tokens (caches None
+    or empty for ctx = 0): the serving forward of [S] 3.4 "Inference Implementation in
+    Production Serving Frameworks" / [P] 3.5, where every token of the chunk runs layers
+    0..l-1 (attending to the cached prefix and to the chunk causally), the caches of every
+    skipped layer / AcrossKV group are computed for the chunk's tokens from x_l, and only
+    the chunk's last token continues through layers l..L-1. A decode token is a chunk of
+    one token; a prompt may be fed in several chunks. Returns the extended caches and the
+    last token's logits [V]."""
+    check_lg(cfg.L, l, g)
+    tokens = np.asarray(tokens)
+    n = len(tokens)
+    if n == 0:
+        raise ValueError("empty chunk")
+    C = num_caches(cfg.L, l, g)
+    if caches:
+        ctx = caches[0][0].shape[0]
+        out: List[KV] = list(caches)
+    else:
+        ctx = 0
+        empty = np.zeros((0, cfg.n_kv, cfg.d_h))
+        out = [(empty, empty)] * C
+    pos = np.arange(ctx, ctx + n)
+    kpos = np.arange(ctx + n)
+
+    def append(c: int, kv: KV) -> None:
+        out[c] = (np.concatenate([out[c][0], kv[0]]), np.concatenate([out[c][1], kv[1]]))
+
+    x = w.embed(tokens)
+    for j in range(l):
+        lw = w.layer(j)
+        q, kv = qkv_proj(cfg, lw, x, pos)
+        append(j, kv)
+        x = attn_out(cfg, lw, x, q, out[j], pos, kpos)
+        x = mlp(cfg, lw, x)
+    for c in range(l, C):
+        append(c, swiftkv_kv(cfg, w.layer(representative(c, l, g)), x, pos))
+    xt, pt = x[n - 1:], pos[n - 1:]
+    for j in range(l, cfg.L):
+        lw = w.layer(j)
+        q = q_proj(cfg, lw, xt, pt)
+        xt = attn_out(cfg, lw, xt, q, out[cache_of_layer(j, l, g)], pt, kpos)
+        xt = mlp(cfg, lw, xt)
+    return out, lm_head(cfg, w, xt)[0]
+
+
 def greedy(logits: np.ndarray) -> int:
     """Greedy next token: the lowest index among the maxima."""
     return int(np.argmax(logits))

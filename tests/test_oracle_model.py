@@ -227,3 +227,29 @@ def test_qkv_bias_is_added_before_rope():
     np.testing.assert_array_equal(caches[0][0], M.bf16(M.rope(kb, pos, cfg.rope_theta)))
     kb_after = M.rope(kb - lw.bk.reshape(1, 1, 32), pos, cfg.rope_theta) + lw.bk.reshape(1, 1, 32)
     assert not np.allclose(caches[0][0][1:], M.bf16(kb_after[1:]))
+
+
+def test_forward_chunks_equal_whole_prompt_and_decode(w_gain, tokens):
+    """The serving forward: a prompt fed as chunks gives the caches and last logits of the
+    whole prompt; a one-token chunk is a decode step; a chunk with no prefix is prefill."""
+    l, g = 2, 2
+    c_all, lg_all = M.swiftkv_prefill_one(CFG, w_gain, tokens, l, g)
+    c0, lg0 = M.swiftkv_forward_one(CFG, w_gain, None, tokens, l, g)
+    for a, b in zip(c0, c_all):
+        np.testing.assert_allclose(a[0], b[0], **TOL)
+    np.testing.assert_allclose(lg0, lg_all, **TOL)
+    cc, lgc = None, None
+    for a, b in [(0, 5), (5, 6), (6, 31), (31, len(tokens))]:
+        cc, lgc = M.swiftkv_forward_one(CFG, w_gain, cc, tokens[a:b], l, g)
+    for a, b in zip(cc, c_all):
+        np.testing.assert_allclose(a[0], b[0], **TOL)
+        np.testing.assert_allclose(a[1], b[1], **TOL)
+    np.testing.assert_allclose(lgc, lg_all, **TOL)
+    nxt = M.greedy(lg_all)
+    c_dec, lg_dec = M.swiftkv_decode_step(CFG, w_gain, c_all, nxt, l, g)
+    c_fw, lg_fw = M.swiftkv_forward_one(CFG, w_gain, c_all, [nxt], l, g)
+    np.testing.assert_allclose(lg_fw, lg_dec, **TOL)
+    for a, b in zip(c_fw, c_dec):
+        np.testing.assert_allclose(a[0], b[0], **TOL)
+    with pytest.raises(ValueError):
+        M.swiftkv_forward_one(CFG, w_gain, c_all, [], l, g)
