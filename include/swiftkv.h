@@ -166,6 +166,30 @@ int swiftkv_prefill_host(swiftkv_model* m, const int32_t* tokens_host, const int
                          int num_seqs, int l, int acrosskv_group, const swiftkv_kv_pages* kv,
                          float* logits_host, swiftkv_stream stream);
 
+/* Serving forward over a batch that mixes prompt chunks and decode tokens ("SwiftKV"
+ * blog and paper, section on the inference implementation in production serving
+ * frameworks: with chunked prefill and decode tokens batched together, every token runs
+ * the first l layers against its sequence's cached prefix, the skipped layers' KV is
+ * projected from x_l, and only the tokens whose logits are needed, the last of each
+ * chunk, run layers l+1..L).
+ *   tokens      device int32 [T], T = cu_seqlens[num_seqs]; chunk s is
+ *               tokens[cu_seqlens[s] .. cu_seqlens[s+1]), every chunk >= 1 token
+ *   cu_seqlens  HOST int32 [num_seqs + 1], cu_seqlens[0] == 0
+ *   ctx_lens    HOST int32 [num_seqs] or NULL (all 0): tokens sequence s already has in
+ *               every cache (positions 0..ctx_lens[s]-1, written by earlier calls with the
+ *               same block table row). Chunk token i sits at position ctx_lens[s] + i,
+ *               writes its K/V there in every cache and attends to positions
+ *               0..ctx_lens[s] + i. A decode token is a chunk of 1 with ctx_lens[s] equal
+ *               to the sequence's length; a fresh prompt is a chunk with ctx_lens[s] = 0.
+ *   kv, l, acrosskv_group, logits, stream  as for swiftkv_prefill; logits of row s are
+ *               those of chunk s's last token (for a chunk that does not end its prompt
+ *               they are computed and may be ignored).
+ * ctx_lens[s] + n_s must fit the block table row (else SWIFTKV_ENO_PAGES); a negative
+ * ctx_lens[s] is SWIFTKV_EINVAL_SEQLENS. With ctx_lens NULL this is swiftkv_prefill. */
+int swiftkv_forward(swiftkv_model* m, const int32_t* tokens, const int32_t* cu_seqlens,
+                    const int32_t* ctx_lens, int num_seqs, int l, int acrosskv_group,
+                    const swiftkv_kv_pages* kv, float* logits, swiftkv_stream stream);
+
 /* One decode token for each of `batch` sequences ("SwiftKV" summary, section 3.2:
  * decode tokens run every layer). Sequence b holds seq_lens[b] cached tokens; its
  * new token (position seq_lens[b]) writes its K/V at that position into every cache

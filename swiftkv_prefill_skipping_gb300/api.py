@@ -125,6 +125,18 @@ class KVCache:
                                model.num_caches, num_pages, 16, self.block_table.data_ptr(),
                                self.block_table.shape[1])
 
+    def view(self, rows: Sequence[int]) -> "KVCache":
+        """The same pools with block table rows `rows` (in that order): a batch that holds
+        only some of the sequences, or holds them in another order."""
+        out = object.__new__(KVCache)
+        out.num_pages, out.k, out.v, out._kp, out._vp = self.num_pages, self.k, self.v, self._kp, self._vp
+        out.block_table = self.block_table[torch.as_tensor(list(rows), dtype=torch.long,
+                                                           device=self.block_table.device)].contiguous()
+        out.pages = B.KVPages(C.cast(self._kp, C.POINTER(C.c_void_p)), C.cast(self._vp, C.POINTER(C.c_void_p)),
+                              self.pages.num_caches, self.num_pages, 16, out.block_table.data_ptr(),
+                              out.block_table.shape[1])
+        return out
+
     def gather(self, c: int, s: int, n: int, which: str = "k") -> torch.Tensor:
         """Cache c's first n rows of sequence s, [n, n_kv, d_h] (test/inspection helper)."""
         pool = self.k[c] if which == "k" else self.v[c]
@@ -156,6 +168,24 @@ def prefill_host(model: Model, tokens: np.ndarray, cu_seqlens: Sequence[int], kv
         logits = np.empty((P, model.shape.vocab), dtype=np.float32)
     B.check(B.lib().swiftkv_prefill_host(model.handle, _ptr(tokens), cu.ctypes.data, P, model.l, model.g,
                                          C.byref(kv.pages), _ptr(logits), _stream(stream)))
+    return logits
+
+
+def forward(model: Model, tokens: torch.Tensor, cu_seqlens: Sequence[int], ctx_lens: Optional[Sequence[int]],
+            kv: KVCache, logits: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Serving forward over prompt chunks and decode tokens: chunk s follows ctx_lens[s]
+    tokens already in kv (None: none); returns [P, V] logits of each chunk's last token."""
+    cu = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+    P = len(cu) - 1
+    ctx = None if ctx_lens is None else np.ascontiguousarray(ctx_lens, dtype=np.int32)
+    if ctx is not None and len(ctx) != P:
+        raise ValueError(f"ctx_lens has {len(ctx)} entries for {P} chunks")
+    if logits is None:
+        logits = torch.empty((P, model.shape.vocab), dtype=torch.float32, device=kv.k.device)
+    tokens = tokens.to(torch.int32).contiguous()
+    B.check(B.lib().swiftkv_forward(model.handle, tokens.data_ptr(), cu.ctypes.data,
+                                    None if ctx is None else ctx.ctypes.data, P, model.l, model.g,
+                                    C.byref(kv.pages), logits.data_ptr(), _stream(stream)))
     return logits
 
 

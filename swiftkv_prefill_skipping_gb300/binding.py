@@ -25,7 +25,8 @@ STATUS_TIMEOUT = 4
 
 # every symbol include/swiftkv.h declares
 EXPORTS = ("swiftkv_cache_count", "swiftkv_model_create", "swiftkv_load_layer", "swiftkv_load_globals",
-           "swiftkv_load_weights", "swiftkv_prefill", "swiftkv_prefill_host", "swiftkv_decode_step",
+           "swiftkv_load_weights", "swiftkv_prefill", "swiftkv_prefill_host", "swiftkv_forward",
+           "swiftkv_decode_step",
            "swiftkv_status", "swiftkv_memory", "swiftkv_set_gemm_impl", "swiftkv_set_attention_impl", "swiftkv_gemm_bf16",
            "swiftkv_gemm_skinny_noalloc",
            "swiftkv_profile_begin", "swiftkv_profile_end",
@@ -83,6 +84,7 @@ def lib(path: str | None = None):
                                                C.POINTER(vp)]
             L.swiftkv_prefill.argtypes = [vp, vp, vp, i, i, i, C.POINTER(KVPages), vp, vp]
             L.swiftkv_prefill_host.argtypes = [vp, vp, vp, i, i, i, C.POINTER(KVPages), vp, vp]
+            L.swiftkv_forward.argtypes = [vp, vp, vp, vp, i, i, i, C.POINTER(KVPages), vp, vp]
             L.swiftkv_decode_step.argtypes = [vp, vp, vp, i, C.POINTER(KVPages), vp, vp, vp]
             L.swiftkv_status.argtypes = [vp, i]
             L.swiftkv_memory.argtypes = [vp, C.POINTER(sz), C.POINTER(sz)]

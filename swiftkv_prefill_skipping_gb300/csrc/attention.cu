@@ -25,7 +25,8 @@ template <int D>
 __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     const bf16* __restrict__ q, int ldq, const bf16* __restrict__ kpool, const bf16* __restrict__ vpool,
     const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ cu,
-    const int* __restrict__ tiles, int n_q, int n_kv, bf16* __restrict__ out, int ldo, float scale_log2) {
+    const int* __restrict__ ctx, const int* __restrict__ tiles, int n_q, int n_kv, bf16* __restrict__ out, int ldo,
+    float scale_log2) {
   constexpr int CH = D / 8;  // 16-byte chunks per row
   extern __shared__ __align__(128) unsigned char smem[];
   bf16* sQ = reinterpret_cast<bf16*>(smem);
@@ -38,6 +39,8 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
   const int h = blockIdx.y, kvh = h / (n_q / n_kv);
   const int seq0 = cu[s], n = cu[s + 1] - seq0;
   const int q0 = qt * ABQ;
+  // the chunk's rows sit at positions c0.. after c0 cached keys; keys [0, nk) are visible
+  const int c0 = ctx ? ctx[s] : 0, nk = c0 + n;
 
   auto swz = [](int row, int ch) { return row * D + ((ch ^ (row & 7)) * 8); };
 
@@ -53,7 +56,7 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     for (int c = tid; c < ABKV * CH; c += ATHREADS) {
       int r = c / CH, ch = c % CH;
       int key = kb * ABKV + r;
-      int page = key < n ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
+      int page = key < nk ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
       bool ok = page >= 0 && page < num_pages;
       size_t off = ok ? (((size_t)page * n_kv + kvh) * kPageSize + (key & 15)) * D + ch * 8 : 0;
       cp_async16(smem_u32(sK + buf * ABKV * D + swz(r, ch)), kpool + off, ok ? 16 : 0);
@@ -61,7 +64,7 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     }
   };
 
-  const int kv_end = min(n, q0 + ABQ);  // keys needed: [0, kv_end)
+  const int kv_end = min(nk, c0 + q0 + ABQ);  // keys needed: [0, kv_end)
   const int nkv = (kv_end + ABKV - 1) / ABKV;
   load_kv(0, 0);
   cp_async_commit();
@@ -74,7 +77,8 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     for (int j = 0; j < 4; ++j) o[i][j] = 0.f;
   float m_a = -FLT_MAX, m_b = -FLT_MAX, l_a = 0.f, l_b = 0.f;
   const int ra = warp * 16 + (lane >> 2);
-  const int qa = q0 + ra, qb = qa + 8;
+  const int qa = q0 + ra, qb = qa + 8;            // rows within the chunk
+  const int pa_ = c0 + qa, pb_ = c0 + qb;          // their positions
 
   for (int kb = 0; kb < nkv; ++kb) {
     if (kb + 1 < nkv) load_kv((kb + 1) & 1, kb + 1);
@@ -133,8 +137,8 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         int k = key + e;
-        float va = (k <= qa && k < n) ? sc[nb][e] * scale_log2 : -INFINITY;
-        float vb = (k <= qb && k < n) ? sc[nb][2 + e] * scale_log2 : -INFINITY;
+        float va = (k <= pa_ && k < nk) ? sc[nb][e] * scale_log2 : -INFINITY;
+        float vb = (k <= pb_ && k < nk) ? sc[nb][2 + e] * scale_log2 : -INFINITY;
         sc[nb][e] = va;
         sc[nb][2 + e] = vb;
         mx_a = fmaxf(mx_a, va);
@@ -357,8 +361,8 @@ __global__ void __launch_bounds__(DTHREADS) attn_decode_kernel(
 
 template <int D>
 cudaError_t prefill_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool, const int* bt,
-                      int max_pages, int num_pages, const int* cu, const int* tiles, int num_tiles,
-                      int n_q, int n_kv, bf16* out, int ldo, cudaStream_t stream) {
+                      int max_pages, int num_pages, const int* cu, const int* ctx, const int* tiles,
+                      int num_tiles, int n_q, int n_kv, bf16* out, int ldo, cudaStream_t stream) {
   constexpr int smem = (ABQ + 4 * ABKV) * D * 2;
   static bool attr = false;
   if (!attr) {
@@ -369,7 +373,7 @@ cudaError_t prefill_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   dim3 grid(num_tiles, n_q);
   attn_prefill_kernel<D><<<grid, ATHREADS, smem, stream>>>(q, ldq, k_pool, v_pool, bt, max_pages, num_pages,
-                                                          cu, tiles, n_q, n_kv, out, ldo, scale_log2);
+                                                          cu, ctx, tiles, n_q, n_kv, out, ldo, scale_log2);
   return cudaGetLastError();
 }
 
@@ -377,14 +381,14 @@ cudaError_t prefill_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_
 
 cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                      const int* block_table, int max_pages, int num_pages,
-                                     const int* cu, const int* tiles, int num_tiles, int n_q,
+                                     const int* cu, const int* ctx, const int* tiles, int num_tiles, int n_q,
                                      int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream) {
   if (num_tiles <= 0) return cudaSuccess;
   if (d_head == 128)
-    return prefill_d<128>(q, ldq, k_pool, v_pool, block_table, max_pages, num_pages, cu, tiles,
+    return prefill_d<128>(q, ldq, k_pool, v_pool, block_table, max_pages, num_pages, cu, ctx, tiles,
                           num_tiles, n_q, n_kv, out, ldo, stream);
   if (d_head == 64)
-    return prefill_d<64>(q, ldq, k_pool, v_pool, block_table, max_pages, num_pages, cu, tiles,
+    return prefill_d<64>(q, ldq, k_pool, v_pool, block_table, max_pages, num_pages, cu, ctx, tiles,
                          num_tiles, n_q, n_kv, out, ldo, stream);
   return cudaErrorNotSupported;
 }

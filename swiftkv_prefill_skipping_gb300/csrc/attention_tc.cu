@@ -1,7 +1,9 @@
 // Varlen causal GQA flash attention on tcgen05 (sm_103a), d_head = 128, reading K/V
 // straight out of the paged cache with TMA.
 //
-// One CTA = 128 query rows of one prompt x one query head, 8 warps:
+// One CTA = 128 query rows of one prompt chunk x one query head. A chunk may follow ctx
+// tokens already in the cache (chunked prefill, decode rows): its rows then sit at
+// positions ctx.. and see keys [0, ctx + row]. 8 warps:
 //   warp 0     TMA producer: the Q tile once (two 64-column halves, 128B swizzle), then
 //              per 64-key block the K and V rows of its four 16-token pages (each page
 //              row block is contiguous in the pool) into a 3-stage ring
@@ -101,8 +103,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
 __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmV, const int* __restrict__ bt, int max_pages, int num_pages,
-    const int* __restrict__ cu, const int* __restrict__ tiles, int n_q, int n_kv, bf16* __restrict__ out,
-    int ldo, float scale_log2, int* status) {
+    const int* __restrict__ cu, const int* __restrict__ ctx, const int* __restrict__ tiles, int n_q, int n_kv,
+    bf16* __restrict__ out, int ldo, float scale_log2, int* status) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -119,7 +121,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
   const int h = blockIdx.y, kvh = h / (n_q / n_kv);
   const int seq0 = cu[s], n = cu[s + 1] - seq0;
   const int q0 = qt * BQ;
-  const int kv_end = min(n, q0 + BQ);
+  // the chunk's rows sit at positions c0.. after c0 cached keys; keys [0, nk) are visible
+  const int c0 = ctx ? ctx[s] : 0, nk = c0 + n;
+  const int kv_end = min(nk, c0 + q0 + BQ);
   const int nblk = (kv_end + BKV - 1) / BKV;
   const int pool_rows = num_pages * n_kv * kPageSize;
 
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
 #pragma unroll
         for (int pg = 0; pg < BKV / kPageSize; ++pg) {
           const int key = j * BKV + pg * kPageSize;
-          int page = key < n ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
+          int page = key < nk ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
           // a page outside the pool reads rows past the tensor's end: TMA fills zeros
           const int row = (page >= 0 && page < num_pages) ? (page * n_kv + kvh) * kPageSize : pool_rows;
 #pragma unroll
@@ -260,7 +264,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
     // by the warp, in TMEM, after the previous block's P V has landed.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
-    const int qpos = q0 + r;
+    const int qrow = q0 + r;     // row within the chunk
+    const int qpos = c0 + qrow;  // its position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -280,12 +285,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
       tmem_ld32(tmem + lane_off + S_COL + sb * BKV + 32, sc + 32);
       tc_fence_before();
       mbar_arrive(bar(ctl->s_empty[sb]));
-      const bool interior = (j + 1) * BKV - 1 <= q0 && (j + 1) * BKV <= n;  // no key masked in any row
+      const bool interior = (j + 1) * BKV - 1 <= c0 + q0 && (j + 1) * BKV <= nk;  // no key masked in any row
       if (!interior) {
 #pragma unroll
         for (int i = 0; i < BKV; ++i) {
           const int key = j * BKV + i;
-          if (key > qpos || key >= n) sc[i] = -INFINITY;
+          if (key > qpos || key >= nk) sc[i] = -INFINITY;
         }
       }
       float mx = -INFINITY;
@@ -345,12 +350,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
     if (ok) {
       tc_fence_after();
       const float inv = 1.f / l;
-      bf16* dst = out + (size_t)(seq0 + min(qpos, n - 1)) * ldo + h * D;
+      bf16* dst = out + (size_t)(seq0 + min(qrow, n - 1)) * ldo + h * D;
 #pragma unroll
       for (int c = 0; c < D; c += 32) {
         float t[32];
         tmem_ld32(tmem + lane_off + O_COL + c, t);
-        if (qpos < n) {
+        if (qrow < n) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 u;
@@ -395,8 +400,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
 
 cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
                                         const int* block_table, int max_pages, int num_pages, const int* cu,
-                                        const int* tiles, int num_tiles, int n_q, int n_kv, int d_head, bf16* out,
-                                        int ldo, int* status, cudaStream_t stream) {
+                                        const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
+                                        int d_head, bf16* out, int ldo, int* status, cudaStream_t stream) {
   if (num_tiles <= 0) return cudaSuccess;
   if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
@@ -413,8 +418,8 @@ cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf1
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   dim3 grid(num_tiles, n_q);
-  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, block_table, max_pages, num_pages, cu, tiles,
-                                                        n_q, n_kv, out, ldo, scale_log2, status);
+  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, block_table, max_pages, num_pages, cu, ctx,
+                                                        tiles, n_q, n_kv, out, ldo, scale_log2, status);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,9 @@ cudaError_t launch_upload(int* dst, const IntBlob& blob, cudaStream_t stream);
 cudaError_t upload_ints(int* dst, const int* src, int n, cudaStream_t stream);
 
 // positions / slots / last index of a packed prefill batch; validates tokens and pages.
-cudaError_t launch_plan_prefill(const int* cu, int P, int T, const int* tokens, int vocab,
+// ctx (device, nullable = all zero): tokens already cached per sequence; chunk row i of
+// sequence s sits at position ctx[s] + i.
+cudaError_t launch_plan_prefill(const int* cu, const int* ctx, int P, int T, const int* tokens, int vocab,
                                 const int* block_table, int max_pages, int num_pages, int* positions,
                                 int* slots, int* last_idx, int* last_pos, int* status,
                                 cudaStream_t stream);
@@ -62,18 +64,20 @@ cudaError_t launch_argmax(const float* logits, int rows, int V, int* out, cudaSt
 cudaError_t launch_scale_columns(bf16* W, int rows, int K, const float* gamma, cudaStream_t stream);
 
 // ---- attention ---------------------------------------------------------------------------
-// Varlen causal GQA attention of packed prompts against their own paged K/V.
-// tiles: [num_tiles] (seq << 16 | q_tile) 64-row query tiles; cu: [P+1] device.
+// Varlen causal GQA attention of packed prompt chunks against their own paged K/V.
+// tiles: [num_tiles] (seq << 16 | q_tile) 64-row query tiles; cu: [P+1] device; ctx: [P]
+// device or nullptr: cached tokens before each chunk (row i at position ctx[s] + i sees
+// keys [0, ctx[s] + i]).
 cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                      const int* block_table, int max_pages, int num_pages,
-                                     const int* cu, const int* tiles, int num_tiles, int n_q,
+                                     const int* cu, const int* ctx, const int* tiles, int num_tiles, int n_q,
                                      int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream);
 // Same on tcgen05 (d_head 128 only; cudaErrorNotSupported otherwise). tiles are 128-row tiles;
 // T = rows of q. status receives kStatusTimeout if a bounded wait expires.
 cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
                                         const int* block_table, int max_pages, int num_pages, const int* cu,
-                                        const int* tiles, int num_tiles, int n_q, int n_kv, int d_head, bf16* out,
-                                        int ldo, int* status, cudaStream_t stream);
+                                        const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
+                                        int d_head, bf16* out, int ldo, int* status, cudaStream_t stream);
 // One query row per sequence b at position qpos[b] attending to keys 0..qpos[b] of its paged cache.
 cudaError_t launch_attention_decode(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                     const int* block_table, int max_pages, int num_pages,

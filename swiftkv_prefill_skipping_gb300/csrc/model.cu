@@ -55,7 +55,7 @@ struct LayerW {
 };
 
 struct Workspace {
-  int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens;
+  int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens, *ctx;
   float *x, *xt, *part, *logits;
   bf16 *u, *q, *attn, *h, *ut, *qt, *at, *ht;
 };
@@ -177,6 +177,7 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
       (size_t)P * m->Nq * 2,         // qt
       (size_t)P * m->Nq * 2,         // at
       (size_t)P * m->Fp * 2,         // ht
+      (size_t)P * 4,                 // cached tokens before each chunk
   };
   const int n = sizeof(sizes) / sizeof(sizes[0]);
   size_t off[32], total = 0;
@@ -219,6 +220,7 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
   w->qt = (bf16*)(b + off[17]);
   w->at = (bf16*)(b + off[18]);
   w->ht = (bf16*)(b + off[19]);
+  w->ctx = (int*)(b + off[20]);
   return SWIFTKV_OK;
 }
 
@@ -242,6 +244,7 @@ struct Ctx {
   bf16* const* k_dev;  // device arrays of pool pointers
   bf16* const* v_dev;
   bool tc_attn = false;  // prefill attention on tcgen05 (128-row query tiles)
+  const int* ctx = nullptr;  // device [P]: cached tokens before each chunk (nullptr: none)
 };
 
 cudaEvent_t prof_event(swiftkv_model* m) {
@@ -328,11 +331,11 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode", 1, attn_flops, 0.0);
   if (prefill && x.tc_attn)
     e = launch_attention_prefill_tc(qb, m->Nq, M, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
-                                    x.kv->num_pages, x.w.cu, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq,
-                                    m->status, x.s);
+                                    x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
+                                    m->Nq, m->status, x.s);
   else if (prefill)
     e = launch_attention_prefill(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
-                                 x.w.cu, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
+                                 x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
   else
     e = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
                                 qpos, M, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
@@ -709,8 +712,10 @@ int swiftkv_profile_end(swiftkv_model* m, swiftkv_profile_entry* out, int max_en
   return (int)agg.size();
 }
 
-static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* cu, int P, int l, int g,
-                        const swiftkv_kv_pages* kv, float* logits, cudaStream_t s, bool host_io) {
+// Prefill of packed prompt chunks; ctx (host, nullable) = tokens each sequence already has
+// in the cache (0 for a fresh prompt, its length for a decode token).
+static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* cu, const int32_t* ctx, int P,
+                        int l, int g, const swiftkv_kv_pages* kv, float* logits, cudaStream_t s, bool host_io) {
   RET(check_ready(m));
   if (l != m->l) return fail(SWIFTKV_EINVAL_L, "l=%d but the model was packed for l=%d", l, m->l);
   if (g != m->g) return fail(SWIFTKV_EINVAL_GROUP, "g=%d but the model was packed for g=%d", g, m->g);
@@ -719,14 +724,14 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   if (!cu || !tokens || !logits) return fail(SWIFTKV_EINVAL, "null tokens / cu_seqlens / logits");
   RET(check_kv(m, kv));
   if (cu[0] != 0) return fail(SWIFTKV_EINVAL_SEQLENS, "cu_seqlens[0] != 0");
-  int maxn = 0;
   for (int i = 0; i < P; ++i) {
-    int n = cu[i + 1] - cu[i];
+    const int n = cu[i + 1] - cu[i];
+    const int c0 = ctx ? ctx[i] : 0;
     if (n < 1) return fail(SWIFTKV_EINVAL_SEQLENS, "prompt %d has %d tokens", i, n);
-    if (n > kv->max_pages_per_seq * kPageSize)
-      return fail(SWIFTKV_ENO_PAGES, "prompt %d needs %d pages, block table holds %d", i, (n + 15) / 16,
-                  kv->max_pages_per_seq);
-    maxn = std::max(maxn, n);
+    if (c0 < 0) return fail(SWIFTKV_EINVAL_SEQLENS, "ctx_lens[%d] = %d < 0", i, c0);
+    if ((long long)c0 + n > (long long)kv->max_pages_per_seq * kPageSize)
+      return fail(SWIFTKV_ENO_PAGES, "sequence %d needs %lld pages, block table holds %d", i,
+                  ((long long)c0 + n + 15) / 16, kv->max_pages_per_seq);
   }
   const int T = cu[P];
   if ((long long)T * std::max(m->Fp, m->cfg.d) >= (1LL << 31)) return fail(SWIFTKV_EUNSUPPORTED, "batch too large");
@@ -734,12 +739,14 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
 
   const bool tc_attn = m->attn_impl == 0 && m->cfg.d_head == 128;
   const int tile_rows = tc_attn ? 128 : 64;
+  // query tiles, heaviest first (a tile's keys grow with its last row's position)
   std::vector<int> tiles;
   for (int i = 0; i < P; ++i) {
     int nt = (cu[i + 1] - cu[i] + tile_rows - 1) / tile_rows;
     for (int t = 0; t < nt; ++t) tiles.push_back((i << 16) | t);
   }
-  std::stable_sort(tiles.begin(), tiles.end(), [](int a, int b) { return (a & 0xffff) > (b & 0xffff); });
+  auto keys_of = [&](int tl) { return (ctx ? ctx[tl >> 16] : 0) + (tl & 0xffff) * tile_rows; };
+  std::stable_sort(tiles.begin(), tiles.end(), [&](int a, int b) { return keys_of(a) > keys_of(b); });
 
   Ctx x;
   x.m = m;
@@ -753,18 +760,23 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
     CK(cudaMemcpyAsync(x.w.tokens, tokens, (size_t)T * 4, cudaMemcpyHostToDevice, s));
     tok = x.w.tokens;
   }
-  double attn_flops = 0;
+  double attn_flops = 0, tail_keys = 0;  // causal score/PV flops; keys seen by the last rows
   for (int i = 0; i < P; ++i) {
-    double n = cu[i + 1] - cu[i];
-    attn_flops += 4.0 * m->cfg.n_q * m->cfg.d_head * n * (n + 1) / 2;
+    const double n = cu[i + 1] - cu[i], c0 = ctx ? ctx[i] : 0;
+    attn_flops += 4.0 * m->cfg.n_q * m->cfg.d_head * (n * c0 + n * (n + 1) / 2);
+    tail_keys += c0 + n;
   }
   {
   Prof pr(m, s, "plan", 1 + (P + 1 + kBlobInts - 1) / kBlobInts + ((int)tiles.size() + kBlobInts - 1) / kBlobInts +
-          (4 * m->C + kBlobInts - 1) / kBlobInts, 0.0, 0.0);
+          (4 * m->C + kBlobInts - 1) / kBlobInts + (ctx ? (P + kBlobInts - 1) / kBlobInts : 0), 0.0, 0.0);
   CK(upload_ints(x.w.cu, cu, P + 1, s));
   CK(upload_ints(x.w.tiles, tiles.data(), (int)tiles.size(), s));
+  if (ctx) {
+    CK(upload_ints(x.w.ctx, ctx, P, s));
+    x.ctx = x.w.ctx;
+  }
   RET(upload_pools(x));
-  CK(launch_plan_prefill(x.w.cu, P, T, tok, m->cfg.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
+  CK(launch_plan_prefill(x.w.cu, x.ctx, P, T, tok, m->cfg.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
                          x.w.positions, x.w.slots, x.w.last_idx, x.w.last_pos, m->status, s));
   }
   const auto& c = m->cfg;
@@ -786,7 +798,7 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   for (int j = m->l; j < c.L; ++j) {
     RET(qkv(x, j, P, x.w.ut, x.w.qt, x.w.last_pos, nullptr, "gemm_tail"));
     RET(layer_rest(x, j, P, x.w.xt, x.w.qt, x.w.at, x.w.ut, x.w.ht, false, x.w.last_pos, 0, "gemm_tail",
-                   4.0 * c.n_q * c.d_head * (double)T));
+                   4.0 * c.n_q * c.d_head * tail_keys));
     RET(norm(x, x.w.xt, nullptr, P, j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final, x.w.ut, nullptr));
   }
   EpiParams el = epi_base(x, EPI_STORE_F32, P, c.vocab);
@@ -803,12 +815,18 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
 
 int swiftkv_prefill(swiftkv_model* m, const int32_t* tokens, const int32_t* cu_seqlens, int num_seqs, int l,
                     int g, const swiftkv_kv_pages* kv, float* logits, swiftkv_stream stream) {
-  return prefill_impl(m, tokens, cu_seqlens, num_seqs, l, g, kv, logits, (cudaStream_t)stream, false);
+  return prefill_impl(m, tokens, cu_seqlens, nullptr, num_seqs, l, g, kv, logits, (cudaStream_t)stream, false);
 }
 
 int swiftkv_prefill_host(swiftkv_model* m, const int32_t* tokens_host, const int32_t* cu_seqlens, int num_seqs,
                          int l, int g, const swiftkv_kv_pages* kv, float* logits_host, swiftkv_stream stream) {
-  return prefill_impl(m, tokens_host, cu_seqlens, num_seqs, l, g, kv, logits_host, (cudaStream_t)stream, true);
+  return prefill_impl(m, tokens_host, cu_seqlens, nullptr, num_seqs, l, g, kv, logits_host, (cudaStream_t)stream,
+                      true);
+}
+
+int swiftkv_forward(swiftkv_model* m, const int32_t* tokens, const int32_t* cu_seqlens, const int32_t* ctx_lens,
+                    int num_seqs, int l, int g, const swiftkv_kv_pages* kv, float* logits, swiftkv_stream stream) {
+  return prefill_impl(m, tokens, cu_seqlens, ctx_lens, num_seqs, l, g, kv, logits, (cudaStream_t)stream, false);
 }
 
 int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* seq_lens, int B,

@@ -19,7 +19,8 @@ __global__ void upload_kernel(int* dst, IntBlob blob) {
     dst[i] = blob.v[i];
 }
 
-__global__ void plan_prefill_kernel(const int* __restrict__ cu, int P, int T, const int* __restrict__ tokens,
+__global__ void plan_prefill_kernel(const int* __restrict__ cu, const int* __restrict__ ctx, int P, int T,
+                                    const int* __restrict__ tokens,
                                     int vocab, const int* __restrict__ bt, int max_pages, int num_pages,
                                     int* positions, int* slots, int* last_idx, int* last_pos, int* status) {
   for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < T; t += blockDim.x * gridDim.x) {
@@ -30,8 +31,9 @@ __global__ void plan_prefill_kernel(const int* __restrict__ cu, int P, int T, co
       else hi = mid - 1;
     }
     const int s = lo;
-    const int pos = t - cu[s];
-    const int n = cu[s + 1] - cu[s];
+    const int c0 = ctx ? ctx[s] : 0;
+    const int pos = c0 + t - cu[s];
+    const int n = c0 + cu[s + 1] - cu[s];  // the sequence's length after this chunk
     const int page = bt[(size_t)s * max_pages + (pos >> 4)];
     const bool ok = page >= 0 && page < num_pages;
     if (!ok) atomicOr(status, kStatusBadPage);
@@ -232,13 +234,13 @@ cudaError_t upload_ints(int* dst, const int* src, int n, cudaStream_t stream) {
   return cudaSuccess;
 }
 
-cudaError_t launch_plan_prefill(const int* cu, int P, int T, const int* tokens, int vocab,
+cudaError_t launch_plan_prefill(const int* cu, const int* ctx, int P, int T, const int* tokens, int vocab,
                                 const int* block_table, int max_pages, int num_pages, int* positions,
                                 int* slots, int* last_idx, int* last_pos, int* status,
                                 cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   int blocks = (T + 255) / 256;
-  plan_prefill_kernel<<<blocks, 256, 0, stream>>>(cu, P, T, tokens, vocab, block_table, max_pages,
+  plan_prefill_kernel<<<blocks, 256, 0, stream>>>(cu, ctx, P, T, tokens, vocab, block_table, max_pages,
                                                    num_pages, positions, slots, last_idx, last_pos,
                                                    status);
   return cudaGetLastError();

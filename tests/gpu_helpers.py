@@ -11,6 +11,13 @@ from oracle import model as OM
 KV_REL_TOL = 1e-2      # per cache and K/V tensor: ||gpu - ref||_2 / ||ref||_2
 LOGIT_ABS_TOL = 5e-2   # last-token logits, max |gpu - ref|
 
+# d_head = 128 shape with several 128-row GEMM tiles and attention tiles (tcgen05 attention)
+SMALL128 = synth.ModelShape("small-d128", L=6, d=512, n_q=4, n_kv=2, d_h=128, ffn=1000, vocab=2048,
+                            rope_theta=500000.0)
+# Q/K/V bias (Qwen-style), single KV head
+SMALL_BIAS = synth.ModelShape("small-bias", L=4, d=640, n_q=5, n_kv=1, d_h=128, ffn=704, vocab=1024,
+                              rope_theta=1000000.0, qkv_bias=True)
+
 
 def rel_l2(a, b) -> float:
     a = np.asarray(a, np.float64)

@@ -5,16 +5,10 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_helpers import (KV_REL_TOL, LOGIT_ABS_TOL, compare_prefill, oracle_prefill, rel_l2,
-                         run_gpu_prefill, untouched_rows_are_zero)
+from gpu_helpers import (KV_REL_TOL, LOGIT_ABS_TOL, SMALL128, SMALL_BIAS, compare_prefill, oracle_prefill,
+                         rel_l2, run_gpu_prefill, untouched_rows_are_zero)
 
 pytestmark = pytest.mark.gpu
-
-# d_head = 128 shape with several 128-row GEMM tiles and 64-row attention tiles
-SMALL128 = synth.ModelShape("small-d128", L=6, d=512, n_q=4, n_kv=2, d_h=128, ffn=1000, vocab=2048,
-                            rope_theta=500000.0)
-SMALL_BIAS = synth.ModelShape("small-bias", L=4, d=640, n_q=5, n_kv=1, d_h=128, ffn=704, vocab=1024,
-                              rope_theta=1000000.0, qkv_bias=True)
 
 
 def _case(shape, l, g, lens, gain_std=0.0, spare_pages=3):
