@@ -106,6 +106,9 @@ class ClockSampler:
 
 def workload_batch(w, rank: int, reserve_tokens: int = 0):
     """Each replica prefills its own prompts (weak scaling): the input seed depends on the rank."""
+    if w.mixed:
+        return synth.mixed_batch(w.shape.vocab, w.mix_chunks, w.mix_decode, w.mix_decode_ctx[0],
+                                 w.mix_decode_ctx[1], w.page_size, seed=synth.SEED_INPUTS + 1000 * rank)
     return synth.prompt_batch(w.shape.vocab, w.num_prompts, w.len_lo, w.len_hi, w.page_size,
                               reserve_tokens=reserve_tokens, seed=synth.SEED_INPUTS + 1000 * rank)
 
@@ -196,6 +199,19 @@ def oracle_sample_time(w, weights, tokens):
 
 
 def workload_config(w, batch):
+    if w.mixed:
+        chunks = ", ".join(f"{n}@{c}" for c, n in w.mix_chunks)
+        return {
+            "workload": f"{w.name}: {w.shape.name} shape bf16 random-init N(0,0.02), SwiftKV l={w.l}, "
+                        f"AcrossKV g={w.g}, one serving step: prompt chunks (tokens@cached) {chunks} + "
+                        f"{w.mix_decode} decode tokens with cached context U[{w.mix_decode_ctx[0]},"
+                        f"{w.mix_decode_ctx[1]}], 16-token pages",
+            "chunks": len(w.mix_chunks), "decode_tokens": int(w.mix_decode),
+            "tokens_per_step": int(batch.cu_seqlens[-1]), "cached_tokens": int(batch.extra["ctx"].sum()),
+            "l": w.l, "g": w.g, "L": w.shape.L,
+            "l2": "inputs larger than L2 (all weights, >=14 GB, stream from HBM every step)",
+            "parallelism": "replicas (one independent serving step per GPU)",
+        }
     return {
         "workload": f"{w.name}: {w.shape.name} shape bf16 random-init N(0,0.02), SwiftKV l={w.l}, "
                     f"AcrossKV g={w.g}, {w.num_prompts} prompts U[{w.len_lo},{w.len_hi}] packed varlen, "
@@ -260,7 +276,7 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     peaks, peak_src = load_peaks()
-    n_dec_req = args.decode_steps if args.decode_steps is not None else w.decode_steps
+    n_dec_req = 0 if w.mixed else (args.decode_steps if args.decode_steps is not None else w.decode_steps)
     batch = workload_batch(w, rank, reserve_tokens=n_dec_req + 1 if n_dec_req > 0 else 0)
     T, P = int(batch.cu_seqlens[-1]), int(len(batch.lens))
     want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
@@ -283,9 +299,21 @@ def run_ours(args, w, rank, world, local_rank):
     tokens = torch.as_tensor(batch.tokens, device=dev)
     logits = torch.empty((P, w.shape.vocab), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
+    ctx_lens = None
+    if w.mixed:
+        # the cached prefixes of the step's sequences, filled once before timing; every
+        # timed step then rewrites the same cache rows with the same values
+        ctx_lens = [int(c) for c in batch.extra["ctx"]]
+        t0 = time.time()
+        fill_prefixes(model, kv, batch, stream, dev)
+        torch.cuda.synchronize()
+        log(f"[ours] rank {rank}: {sum(ctx_lens)} cached prefix tokens prefilled in {time.time() - t0:.1f}s")
 
     def step():
-        api.prefill(model, tokens, batch.cu_seqlens, kv, logits=logits, stream=stream)
+        if ctx_lens is not None:
+            api.forward(model, tokens, batch.cu_seqlens, ctx_lens, kv, logits=logits, stream=stream)
+        else:
+            api.prefill(model, tokens, batch.cu_seqlens, kv, logits=logits, stream=stream)
 
     def barrier():
         replica_barrier(world)
@@ -326,7 +354,7 @@ def run_ours(args, w, rank, world, local_rank):
                                  "bytes": e.bytes}
     launches = sum(v["kernels"] for v in prof.values())
 
-    fl = FL.prefill_flops(w.shape, batch.lens, w.l, w.g)
+    fl = FL.prefill_flops(w.shape, batch.lens, w.l, w.g, ctx=ctx_lens)
     dense_tflops = sum_over_ranks(fl["dense_equiv"], world, dev) * args.steps / (ms / 1e3) / 1e12
     exec_tflops = sum_over_ranks(fl["executed"], world, dev) * args.steps / (ms / 1e3) / 1e12
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
@@ -354,7 +382,29 @@ def run_ours(args, w, rank, world, local_rank):
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and ctx_lens is not None:
+        # public Python API with pinned host buffers: token copy in, forward, logits copy out
+        h_tok = torch.empty(T, dtype=torch.int32, pin_memory=True)
+        h_tok.copy_(torch.as_tensor(batch.tokens))
+        h_log = torch.empty((P, w.shape.vocab), dtype=torch.float32, pin_memory=True)
+        d_tok = torch.empty(T, dtype=torch.int32, device=dev)
+
+        def e2e_step():
+            d_tok.copy_(h_tok, non_blocking=True)
+            api.forward(model, d_tok, batch.cu_seqlens, ctx_lens, kv, logits=logits, stream=stream)
+            h_log.copy_(logits, non_blocking=True)
+            stream.synchronize()
+
+        e2e_step()
+        barrier()
+        t1 = time.perf_counter()
+        for _ in range(args.steps):
+            e2e_step()
+        el = max_over_ranks(time.perf_counter() - t1, world, dev)
+        e2e = {"value": whole_job_throughput(T_all, args.steps, el), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * 4 + (2 * P + 1) * 4, "d2h_bytes_per_step": P * w.shape.vocab * 4,
+               "ms_per_step": 1e3 * el / args.steps}
+    elif not args.no_e2e:
         h_tok = torch.empty(T, dtype=torch.int32, pin_memory=True)
         h_tok.copy_(torch.as_tensor(batch.tokens))
         h_log = torch.empty((P, w.shape.vocab), dtype=torch.float32, pin_memory=True)
@@ -371,7 +421,7 @@ def run_ours(args, w, rank, world, local_rank):
 
     # decode from the filled caches (greedy, every sequence one token per step): TPOT
     decode = None
-    n_dec = args.decode_steps if args.decode_steps is not None else w.decode_steps
+    n_dec = n_dec_req
     if n_dec > 0:
         if batch.block_table.shape[1] * 16 < int(batch.lens.max()) + n_dec:
             raise RuntimeError("block table too small for the decode steps")
@@ -427,6 +477,30 @@ def run_ours(args, w, rank, world, local_rank):
         print(json.dumps(line), flush=True)
     model.free()
     return 0
+
+
+def fill_prefixes(model, kv, batch, stream, dev, max_tokens: int = 16384) -> None:
+    """Prefills the cached prefix of every sequence of a serving-step batch (ctx > 0) in
+    groups of at most max_tokens tokens (a longer prefix gets a group of its own)."""
+    import torch
+    from swiftkv_prefill_skipping_gb300 import api
+    ctx, pcu, ptok = batch.extra["ctx"], batch.extra["prefix_cu"], batch.extra["prefix_tokens"]
+    rows = [s for s in range(len(ctx)) if ctx[s] > 0]
+    group, n = [], 0
+
+    def run(group):
+        toks = np.concatenate([ptok[pcu[s]:pcu[s + 1]] for s in group])
+        cu = np.concatenate([[0], np.cumsum([int(ctx[s]) for s in group])]).astype(np.int32)
+        api.prefill(model, torch.as_tensor(toks, device=dev), cu, kv.view(group), stream=stream)
+
+    for s in rows:
+        if group and n + int(ctx[s]) > max_tokens:
+            run(group)
+            group, n = [], 0
+        group.append(s)
+        n += int(ctx[s])
+    if group:
+        run(group)
 
 
 def traffic_per_launch(kernel: str):

@@ -223,13 +223,17 @@ constexpr int DTHREADS = 256, DWARPS = DTHREADS / 32, DMAXG = 8;
 template <int D>
 __global__ void __launch_bounds__(DTHREADS) attn_decode_kernel(
     const bf16* __restrict__ q, int ldq, const bf16* __restrict__ kpool, const bf16* __restrict__ vpool,
-    const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ qpos, int n_q,
-    int n_kv, bf16* __restrict__ out, int ldo, float scale_log2) {
+    const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ qpos,
+    const int* __restrict__ rows, const int* __restrict__ seqs, int n_q, int n_kv, bf16* __restrict__ out, int ldo,
+    float scale_log2) {
   constexpr int DPL = D / 32;  // dims per lane in the PV sweep
   __shared__ float s_q[DMAXG][D];
   __shared__ float s_m[DWARPS][DMAXG], s_l[DWARPS][DMAXG];
   __shared__ float s_o[DWARPS][DMAXG][D];
-  const int b = blockIdx.x, kvh = blockIdx.y;
+  const int kvh = blockIdx.y;
+  // item -> its row of q / out / qpos and its block table row (identity without maps)
+  const int b = rows ? rows[blockIdx.x] : blockIdx.x;
+  const int sq = seqs ? seqs[blockIdx.x] : blockIdx.x;
   const int G = n_q / n_kv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nkeys = qpos[b] + 1;
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(DTHREADS) attn_decode_kernel(
 #pragma unroll
     for (int i = 0; i < DPL; ++i) o[g][i] = 0.f;
   }
-  const int* btrow = bt + (size_t)b * max_pages;
+  const int* btrow = bt + (size_t)sq * max_pages;
   for (int k0 = warp * 32; k0 < nkeys; k0 += DWARPS * 32) {
     const int k = k0 + lane;
     int page = k < nkeys ? btrow[k >> 4] : -1;
@@ -396,17 +400,17 @@ cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool,
 cudaError_t launch_attention_decode(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                     const int* block_table, int max_pages, int num_pages,
                                     const int* qpos, int B, int n_q, int n_kv, int d_head, bf16* out,
-                                    int ldo, cudaStream_t stream) {
+                                    int ldo, cudaStream_t stream, const int* rows, const int* seqs) {
   if (B <= 0) return cudaSuccess;
   if (n_q / n_kv > DMAXG) return cudaErrorNotSupported;
   dim3 grid(B, n_kv);
   if (d_head == 128) {
     attn_decode_kernel<128><<<grid, DTHREADS, 0, stream>>>(q, ldq, k_pool, v_pool, block_table, max_pages,
-                                                           num_pages, qpos, n_q, n_kv, out, ldo,
+                                                           num_pages, qpos, rows, seqs, n_q, n_kv, out, ldo,
                                                            1.4426950408889634f / sqrtf(128.f));
   } else if (d_head == 64) {
     attn_decode_kernel<64><<<grid, DTHREADS, 0, stream>>>(q, ldq, k_pool, v_pool, block_table, max_pages,
-                                                          num_pages, qpos, n_q, n_kv, out, ldo,
+                                                          num_pages, qpos, rows, seqs, n_q, n_kv, out, ldo,
                                                           1.4426950408889634f / sqrtf(64.f));
   } else {
     return cudaErrorNotSupported;

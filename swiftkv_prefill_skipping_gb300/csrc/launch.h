@@ -78,10 +78,12 @@ cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf1
                                         const int* block_table, int max_pages, int num_pages, const int* cu,
                                         const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
                                         int d_head, bf16* out, int ldo, int* status, cudaStream_t stream);
-// One query row per sequence b at position qpos[b] attending to keys 0..qpos[b] of its paged cache.
+// B single query rows: item b is row r = rows[b] of q / out (r = b if rows is null) at
+// position qpos[r], attending to keys 0..qpos[r] of block table row seqs[b] (b if null).
 cudaError_t launch_attention_decode(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                     const int* block_table, int max_pages, int num_pages,
                                     const int* qpos, int B, int n_q, int n_kv, int d_head, bf16* out,
-                                    int ldo, cudaStream_t stream);
+                                    int ldo, cudaStream_t stream, const int* rows = nullptr,
+                                    const int* seqs = nullptr);
 
 }  // namespace skv

@@ -55,10 +55,12 @@ struct LayerW {
 };
 
 struct Workspace {
-  int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens, *ctx;
+  int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens, *ctx, *srow, *sseq;
   float *x, *xt, *part, *logits;
   bf16 *u, *q, *attn, *h, *ut, *qt, *at, *ht;
 };
+
+constexpr int kShortChunk = 4;  // chunks up to this many rows take the single-row attention kernel
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -178,6 +180,7 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
       (size_t)P * m->Nq * 2,         // at
       (size_t)P * m->Fp * 2,         // ht
       (size_t)P * 4,                 // cached tokens before each chunk
+      (size_t)T * 4, (size_t)T * 4,  // rows of short chunks and their sequences
   };
   const int n = sizeof(sizes) / sizeof(sizes[0]);
   size_t off[32], total = 0;
@@ -221,6 +224,8 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
   w->at = (bf16*)(b + off[18]);
   w->ht = (bf16*)(b + off[19]);
   w->ctx = (int*)(b + off[20]);
+  w->srow = (int*)(b + off[21]);
+  w->sseq = (int*)(b + off[22]);
   return SWIFTKV_OK;
 }
 
@@ -245,6 +250,7 @@ struct Ctx {
   bf16* const* v_dev;
   bool tc_attn = false;  // prefill attention on tcgen05 (128-row query tiles)
   const int* ctx = nullptr;  // device [P]: cached tokens before each chunk (nullptr: none)
+  int nshort = 0;            // rows of short chunks, attended one row at a time (w.srow / w.sseq)
 };
 
 cudaEvent_t prof_event(swiftkv_model* m) {
@@ -328,7 +334,8 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   const bf16* vp = static_cast<const bf16*>(x.kv->v_pool[cidx]);
   cudaError_t e;
   {
-  Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode", 1, attn_flops, 0.0);
+  Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode", prefill ? (ntiles > 0) + (x.nshort > 0) : 1,
+          attn_flops, 0.0);
   if (prefill && x.tc_attn)
     e = launch_attention_prefill_tc(qb, m->Nq, M, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
@@ -339,6 +346,10 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   else
     e = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
                                 qpos, M, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
+  if (e == cudaSuccess && prefill && x.nshort > 0)
+    e = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
+                                x.w.positions, x.nshort, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s, x.w.srow,
+                                x.w.sseq);
   }
   if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "attention layer %d: %s", j, cudaGetErrorString(e));
   EpiParams eo = epi_base(x, EPI_RESID, M, c.d);
@@ -739,10 +750,22 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
 
   const bool tc_attn = m->attn_impl == 0 && m->cfg.d_head == 128;
   const int tile_rows = tc_attn ? 128 : 64;
-  // query tiles, heaviest first (a tile's keys grow with its last row's position)
-  std::vector<int> tiles;
+  // Chunks of at most kShortChunk rows (decode tokens) are attended one row at a time by
+  // the GQA-grouped single-row kernel: a 128-row query tile would be nearly empty and its CTA
+  // per query head would read the sequence's keys once per head. The rest go in query
+  // tiles, heaviest first (a tile's keys grow with its last row's position).
+  const int short_max = m->cfg.n_q / m->cfg.n_kv <= 8 ? kShortChunk : 0;
+  std::vector<int> tiles, srow, sseq;
   for (int i = 0; i < P; ++i) {
-    int nt = (cu[i + 1] - cu[i] + tile_rows - 1) / tile_rows;
+    const int n = cu[i + 1] - cu[i];
+    if (n <= short_max) {
+      for (int r = 0; r < n; ++r) {
+        srow.push_back(cu[i] + r);
+        sseq.push_back(i);
+      }
+      continue;
+    }
+    int nt = (n + tile_rows - 1) / tile_rows;
     for (int t = 0; t < nt; ++t) tiles.push_back((i << 16) | t);
   }
   auto keys_of = [&](int tl) { return (ctx ? ctx[tl >> 16] : 0) + (tl & 0xffff) * tile_rows; };
@@ -768,12 +791,18 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   }
   {
   Prof pr(m, s, "plan", 1 + (P + 1 + kBlobInts - 1) / kBlobInts + ((int)tiles.size() + kBlobInts - 1) / kBlobInts +
-          (4 * m->C + kBlobInts - 1) / kBlobInts + (ctx ? (P + kBlobInts - 1) / kBlobInts : 0), 0.0, 0.0);
+          (4 * m->C + kBlobInts - 1) / kBlobInts + (ctx ? (P + kBlobInts - 1) / kBlobInts : 0) +
+          2 * (((int)srow.size() + kBlobInts - 1) / kBlobInts), 0.0, 0.0);
   CK(upload_ints(x.w.cu, cu, P + 1, s));
   CK(upload_ints(x.w.tiles, tiles.data(), (int)tiles.size(), s));
   if (ctx) {
     CK(upload_ints(x.w.ctx, ctx, P, s));
     x.ctx = x.w.ctx;
+  }
+  if (!srow.empty()) {
+    CK(upload_ints(x.w.srow, srow.data(), (int)srow.size(), s));
+    CK(upload_ints(x.w.sseq, sseq.data(), (int)sseq.size(), s));
+    x.nshort = (int)srow.size();
   }
   RET(upload_pools(x));
   CK(launch_plan_prefill(x.w.cu, x.ctx, P, T, tok, m->cfg.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,

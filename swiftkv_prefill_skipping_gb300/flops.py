@@ -21,25 +21,29 @@ def _linear_per_token(d, n_q, n_kv, d_h, ffn):
     return qkv, q, kv, o, mlp
 
 
-def _attn_pairs(lens: Sequence[int]) -> int:
-    """Sum over prompts of the causal (query, key) pairs n(n+1)/2."""
-    return sum(int(n) * (int(n) + 1) // 2 for n in lens)
+def _attn_pairs(lens: Sequence[int], ctx: Sequence[int] = None) -> int:
+    """Sum over chunks of the causal (query, key) pairs: n(n+1)/2, plus n * ctx for a
+    chunk that follows ctx cached tokens."""
+    ctx = ctx if ctx is not None else [0] * len(lens)
+    return sum(int(n) * (int(n) + 1) // 2 + int(n) * int(c) for n, c in zip(lens, ctx))
 
 
-def prefill_flops(shape, lens: Sequence[int], l: int, g: int = 1) -> Dict[str, float]:
+def prefill_flops(shape, lens: Sequence[int], l: int, g: int = 1, ctx: Sequence[int] = None) -> Dict[str, float]:
     """FLOPs of one SwiftKV prefill of prompts `lens` (executed) and of the ordinary
-    model (dense-equivalent), by component."""
+    model (dense-equivalent), by component. With ctx, chunk s follows ctx[s] cached
+    tokens (serving forward)."""
     L, d, n_q, n_kv, d_h, F, V = shape.L, shape.d, shape.n_q, shape.n_kv, shape.d_h, shape.ffn, shape.vocab
     T, P = int(sum(lens)), len(lens)
+    ctx = ctx if ctx is not None else [0] * P
     qkv, q, kv, o, mlp = _linear_per_token(d, n_q, n_kv, d_h, F)
-    pairs = _attn_pairs(lens)
+    pairs = _attn_pairs(lens, ctx)
     attn_layer = 4 * n_q * d_h * pairs           # QK^T and PV over causal pairs
     G = (L - l) // g
     full_gemm = l * T * (qkv + o + mlp)
     wide_kv = T * G * kv
     # tail: last token of each prompt through layers l+1..L (Q, attention, O, MLP)
     tail_gemm = (L - l) * P * (q + o + mlp)
-    tail_attn = (L - l) * 4 * n_q * d_h * sum(int(n) for n in lens)
+    tail_attn = (L - l) * 4 * n_q * d_h * sum(int(n) + int(c) for n, c in zip(lens, ctx))
     lm = P * 2 * d * V
     executed = full_gemm + wide_kv + l * attn_layer + tail_gemm + tail_attn + lm
     dense = L * T * (qkv + o + mlp) + L * attn_layer + lm

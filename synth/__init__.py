@@ -147,7 +147,23 @@ class Workload:
     len_hi: int
     decode_steps: int = 0
     page_size: int = 16
+    # serving-step mix (chunked prefill with decode tokens): mix_decode sequences with a
+    # cached context U[mix_decode_ctx] contribute one decode token each; mix_chunks holds
+    # (cached tokens, chunk tokens) of prompt chunks. Empty: a plain prompt batch.
+    mix_decode: int = 0
+    mix_decode_ctx: tuple = (0, 0)
+    mix_chunks: tuple = ()
 
+    @property
+    def mixed(self) -> bool:
+        return self.mix_decode > 0 or len(self.mix_chunks) > 0
+
+
+# an 8192-token serving step: four 2016-token chunks of 8064-token prompts (at each of the
+# four chunk offsets) and 128 decode tokens of requests with 2000-token prompts and up to
+# 250 generated tokens
+_MIX_8K = dict(mix_decode=128, mix_decode_ctx=(2000, 2250),
+               mix_chunks=((0, 2016), (2016, 2016), (4032, 2016), (6048, 2016)))
 
 WORKLOADS = {
     w.name: w for w in [
@@ -161,6 +177,9 @@ WORKLOADS = {
         Workload("llama70b_l40", LLAMA70B, l=40, g=1, num_prompts=8, len_lo=500, len_hi=1000),
         Workload("qwen14b_l24_g4", QWEN14B, l=24, g=4, num_prompts=24, len_lo=1000, len_hi=1000,
                  decode_steps=100),
+        Workload("llama8b_l16_mixed", LLAMA8B, l=16, g=1, num_prompts=0, len_lo=0, len_hi=0, **_MIX_8K),
+        # the same serving step through the ordinary model (l = L)
+        Workload("llama8b_full_mixed", LLAMA8B, l=32, g=1, num_prompts=0, len_lo=0, len_hi=0, **_MIX_8K),
     ]
 }
 
@@ -272,6 +291,34 @@ def prompt_batch(vocab: int, num_prompts: int, len_lo: int, len_hi: int, page_si
         k += m
     return Batch(lens=lens, cu_seqlens=cu, tokens=tokens, block_table=bt, num_pages=num_pages,
                  page_size=page_size)
+
+
+def mixed_batch(vocab: int, chunks, num_decode: int, decode_ctx_lo: int, decode_ctx_hi: int,
+                page_size: int = 16, seed: int = SEED_INPUTS, page_seed: int = SEED_PAGES) -> Batch:
+    """A serving step: prompt chunks [(ctx, n)] followed by num_decode one-token chunks
+    whose contexts are U[decode_ctx_lo, decode_ctx_hi]. lens / cu_seqlens / tokens describe
+    the step's chunks; extra["ctx"] holds each sequence's cached length and
+    extra["prefix_tokens"] / extra["prefix_cu"] the token ids of those cached prefixes
+    (to fill the cache before the step). The block table covers ctx + n per sequence."""
+    ctx = [int(c) for c, _ in chunks] + list(uniform_int(seed, 21, num_decode, decode_ctx_lo, decode_ctx_hi))
+    lens = np.asarray([int(n) for _, n in chunks] + [1] * num_decode, dtype=np.int32)
+    ctx = np.asarray(ctx, dtype=np.int32)
+    cu = np.zeros(len(lens) + 1, dtype=np.int32)
+    cu[1:] = np.cumsum(lens)
+    tokens = uniform_int(seed, 22, int(cu[-1]), 0, vocab - 1)
+    pcu = np.zeros(len(lens) + 1, dtype=np.int32)
+    pcu[1:] = np.cumsum(ctx)
+    prefix = uniform_int(seed, 23, int(pcu[-1]), 0, vocab - 1)
+    pages_per = [(int(c) + int(n) + page_size - 1) // page_size for c, n in zip(ctx, lens)]
+    num_pages = sum(pages_per)
+    perm = permutation(page_seed, 24, num_pages)
+    bt = np.full((len(lens), max(pages_per)), -1, dtype=np.int32)
+    k = 0
+    for s, m in enumerate(pages_per):
+        bt[s, :m] = perm[k:k + m]
+        k += m
+    return Batch(lens=lens, cu_seqlens=cu, tokens=tokens, block_table=bt, num_pages=num_pages,
+                 page_size=page_size, extra={"ctx": ctx, "prefix_tokens": prefix, "prefix_cu": pcu})
 
 
 def workload_batch(w: Workload, reserve_tokens: int = 0) -> Batch:

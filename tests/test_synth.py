@@ -56,3 +56,35 @@ def test_prompt_batch_block_table():
     for s, n in enumerate(b.lens):
         assert (b.block_table[s] >= 0).sum() == (n + 3 + 15) // 16
     assert b.tokens.min() >= 0 and b.tokens.max() < 1024
+
+
+def test_mixed_batch_layout():
+    """Serving-step batch: chunks then decode tokens, prefixes and block table sized to
+    ctx + n, every page used once."""
+    b = synth.mixed_batch(1000, ((0, 40), (33, 17)), 5, 10, 30)
+    ctx = b.extra["ctx"]
+    assert list(b.lens) == [40, 17, 1, 1, 1, 1, 1]
+    assert list(ctx[:2]) == [0, 33] and all(10 <= c <= 30 for c in ctx[2:])
+    assert b.cu_seqlens[-1] == len(b.tokens) == 62
+    assert b.extra["prefix_cu"][-1] == len(b.extra["prefix_tokens"]) == ctx.sum()
+    used = []
+    for s in range(7):
+        need = (int(ctx[s]) + int(b.lens[s]) + 15) // 16
+        row = b.block_table[s]
+        assert (row[:need] >= 0).all() and (row[need:] == -1).all()
+        used += list(row[:need])
+    assert sorted(used) == list(range(b.num_pages))
+    assert (b.tokens >= 0).all() and (b.tokens < 1000).all()
+
+
+def test_serving_flops_count_cached_pairs():
+    """Causal pairs of a chunk after a cached prefix: brute-force count of (query, key)
+    with key <= query position; a prefix-free batch keeps the prefill count."""
+    from swiftkv_prefill_skipping_gb300 import flops as FL
+    lens, ctx = [5, 1, 7], [0, 9, 3]
+    brute = sum(1 for n, c in zip(lens, ctx) for i in range(n) for k in range(c + n) if k <= c + i)
+    assert FL._attn_pairs(lens, ctx) == brute
+    assert FL._attn_pairs(lens) == sum(n * (n + 1) // 2 for n in lens)
+    a = FL.prefill_flops(synth.TINY, lens, 2, 1, ctx=ctx)
+    b = FL.prefill_flops(synth.TINY, lens, 2, 1)
+    assert a["executed"] > b["executed"] and a["wide_kv_gemm"] == b["wide_kv_gemm"]
