@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <vector>
+
 #include "common.cuh"
 
 namespace skv {
@@ -85,5 +87,25 @@ cudaError_t launch_attention_decode(const bf16* q, int ldq, const bf16* k_pool, 
                                     const int* qpos, int B, int n_q, int n_kv, int d_head, bf16* out,
                                     int ldo, cudaStream_t stream, const int* rows = nullptr,
                                     const int* seqs = nullptr);
+
+// Key-split single-row attention (decode tokens, SwiftKV tail rows, rows of short chunks).
+// Items b = 0..num_items-1 are mapped as in launch_attention_decode (rows / seqs / qpos);
+// units [2 * num_units] = (item, split) pairs, item-major with splits ascending; ubeg
+// [num_items + 1] = first unit of each item; part = split_part_floats(num_units, ...) floats.
+struct SplitPlan {
+  const int* units;
+  const int* ubeg;
+  int num_units, num_items, split_keys;
+  bool any_split;  // some item has more than one unit (the combine pass runs)
+  float* part;
+};
+// Host: splits items with nkeys[b] keys into units of kSplitKeys keys; returns the split.
+constexpr int kSplitKeys = 256;
+int split_plan_host(const int* nkeys, int items, std::vector<int>* units, std::vector<int>* ubeg);
+size_t split_part_floats(int num_units, int n_q, int d_head);
+cudaError_t launch_attention_decode_split(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
+                                          const int* block_table, int max_pages, int num_pages, const int* qpos,
+                                          const int* rows, const int* seqs, const SplitPlan& plan, int n_q,
+                                          int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream);
 
 }  // namespace skv

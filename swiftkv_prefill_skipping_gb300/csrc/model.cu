@@ -55,8 +55,8 @@ struct LayerW {
 };
 
 struct Workspace {
-  int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens, *ctx, *srow, *sseq;
-  float *x, *xt, *part, *logits;
+  int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens, *ctx, *srow, *sseq, *dint;
+  float *x, *xt, *part, *logits, *dpart;
   bf16 *u, *q, *attn, *h, *ut, *qt, *at, *ht;
 };
 
@@ -157,7 +157,10 @@ int cache_of_layer(const swiftkv_model* m, int j) { return j < m->l ? j : m->l +
 // ---------------------------------------------------------------------------- workspace
 
 
-int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t part_bytes, Workspace* w) {
+// dec_ints / dec_floats: key-split plans of the single-row attention (units + ubeg) and
+// their partial results.
+int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t part_bytes, Workspace* w,
+                     size_t dec_ints = 0, size_t dec_floats = 0) {
   const auto& c = m->cfg;
   const size_t A = 256;
   size_t sizes[] = {
@@ -181,6 +184,8 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
       (size_t)P * m->Fp * 2,         // ht
       (size_t)P * 4,                 // cached tokens before each chunk
       (size_t)T * 4, (size_t)T * 4,  // rows of short chunks and their sequences
+      dec_ints * 4,                  // key-split plans
+      dec_floats * 4,                // key-split partials
   };
   const int n = sizeof(sizes) / sizeof(sizes[0]);
   size_t off[32], total = 0;
@@ -226,6 +231,8 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
   w->ctx = (int*)(b + off[20]);
   w->srow = (int*)(b + off[21]);
   w->sseq = (int*)(b + off[22]);
+  w->dint = (int*)(b + off[23]);
+  w->dpart = (float*)(b + off[24]);
   return SWIFTKV_OK;
 }
 
@@ -251,7 +258,39 @@ struct Ctx {
   bool tc_attn = false;  // prefill attention on tcgen05 (128-row query tiles)
   const int* ctx = nullptr;  // device [P]: cached tokens before each chunk (nullptr: none)
   int nshort = 0;            // rows of short chunks, attended one row at a time (w.srow / w.sseq)
+  SplitPlan sp_short{};      // key-split plan of those rows
+  SplitPlan sp_rows{};       // key-split plan of the single-row attention (tail / decode rows)
 };
+
+// Host side of a key-split plan: units then ubeg in one vector (one upload).
+struct HostSplit {
+  std::vector<int> units, ubeg;
+  int split = 0;
+  size_t ints() const { return units.size() + ubeg.size(); }
+  int num_units() const { return (int)(units.size() / 2); }
+};
+
+HostSplit make_split(const std::vector<int>& nkeys) {
+  HostSplit h;
+  if (!nkeys.empty()) h.split = split_plan_host(nkeys.data(), (int)nkeys.size(), &h.units, &h.ubeg);
+  return h;
+}
+
+// Uploads h into dst and describes it (partials in the shared key-split buffer).
+int upload_split(Ctx& x, const HostSplit& h, int* dst, SplitPlan* p) {
+  if (h.units.empty()) return SWIFTKV_OK;
+  std::vector<int> blob(h.units);
+  blob.insert(blob.end(), h.ubeg.begin(), h.ubeg.end());
+  CK(upload_ints(dst, blob.data(), (int)blob.size(), x.s));
+  p->units = dst;
+  p->ubeg = dst + h.units.size();
+  p->num_units = h.num_units();
+  p->num_items = (int)h.ubeg.size() - 1;
+  p->split_keys = h.split;
+  p->any_split = p->num_units > p->num_items;
+  p->part = x.w.dpart;
+  return SWIFTKV_OK;
+}
 
 cudaEvent_t prof_event(swiftkv_model* m) {
   if (m->ev_used == m->ev_pool.size()) {
@@ -333,9 +372,23 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   const bf16* kp = static_cast<const bf16*>(x.kv->k_pool[cidx]);
   const bf16* vp = static_cast<const bf16*>(x.kv->v_pool[cidx]);
   cudaError_t e;
+  // single-row attention: key-split kernel (default), else / if unsupported the one-CTA-per-row kernel
+  auto rows_attn = [&](const int* pos, int items, const int* rows, const int* seqs, const SplitPlan& sp) {
+    cudaError_t r = cudaErrorNotSupported;
+    if (m->attn_impl == 0 && sp.num_units > 0)
+      r = launch_attention_decode_split(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
+                                        x.kv->num_pages, pos, rows, seqs, sp, c.n_q, c.n_kv, c.d_head, ab, m->Nq,
+                                        x.s);
+    if (r == cudaErrorNotSupported)
+      r = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
+                                  pos, items, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s, rows, seqs);
+    return r;
+  };
+  auto launches = [&](const SplitPlan& sp) { return m->attn_impl == 0 ? 1 + (int)sp.any_split : 1; };
   {
-  Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode", prefill ? (ntiles > 0) + (x.nshort > 0) : 1,
-          attn_flops, 0.0);
+  Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode",
+          prefill ? (ntiles > 0) + (x.nshort > 0 ? launches(x.sp_short) : 0) : launches(x.sp_rows), attn_flops,
+          0.0);
   if (prefill && x.tc_attn)
     e = launch_attention_prefill_tc(qb, m->Nq, M, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
@@ -344,12 +397,8 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
     e = launch_attention_prefill(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
                                  x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
   else
-    e = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
-                                qpos, M, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
-  if (e == cudaSuccess && prefill && x.nshort > 0)
-    e = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
-                                x.w.positions, x.nshort, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s, x.w.srow,
-                                x.w.sseq);
+    e = rows_attn(qpos, M, nullptr, nullptr, x.sp_rows);
+  if (e == cudaSuccess && prefill && x.nshort > 0) e = rows_attn(x.w.positions, x.nshort, x.w.srow, x.w.sseq, x.sp_short);
   }
   if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "attention layer %d: %s", j, cudaGetErrorString(e));
   EpiParams eo = epi_base(x, EPI_RESID, M, c.d);
@@ -777,7 +826,16 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   x.kv = kv;
   x.tc_attn = tc_attn;
   size_t part = std::max(skinny_part_bytes(m, P), skinny_part_bytes(m, T));
-  RET(ensure_workspace(m, T, P, m->C, (int)tiles.size(), part, &x.w));
+  std::vector<int> nk_short, nk_tail(P);
+  for (size_t i = 0; i < srow.size(); ++i) {
+    const int sq = sseq[i];
+    nk_short.push_back((ctx ? ctx[sq] : 0) + srow[i] - cu[sq] + 1);
+  }
+  for (int i = 0; i < P; ++i) nk_tail[i] = (ctx ? ctx[i] : 0) + cu[i + 1] - cu[i];
+  const HostSplit hs_short = make_split(nk_short), hs_tail = make_split(nk_tail);
+  RET(ensure_workspace(m, T, P, m->C, (int)tiles.size(), part, &x.w, hs_short.ints() + hs_tail.ints(),
+                       std::max(split_part_floats(hs_short.num_units(), m->cfg.n_q, m->cfg.d_head),
+                                split_part_floats(hs_tail.num_units(), m->cfg.n_q, m->cfg.d_head))));
   const int* tok = tokens;
   if (host_io) {
     CK(cudaMemcpyAsync(x.w.tokens, tokens, (size_t)T * 4, cudaMemcpyHostToDevice, s));
@@ -792,7 +850,9 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   {
   Prof pr(m, s, "plan", 1 + (P + 1 + kBlobInts - 1) / kBlobInts + ((int)tiles.size() + kBlobInts - 1) / kBlobInts +
           (4 * m->C + kBlobInts - 1) / kBlobInts + (ctx ? (P + kBlobInts - 1) / kBlobInts : 0) +
-          2 * (((int)srow.size() + kBlobInts - 1) / kBlobInts), 0.0, 0.0);
+          2 * (((int)srow.size() + kBlobInts - 1) / kBlobInts) +
+          ((int)hs_short.ints() + kBlobInts - 1) / kBlobInts + ((int)hs_tail.ints() + kBlobInts - 1) / kBlobInts,
+          0.0, 0.0);
   CK(upload_ints(x.w.cu, cu, P + 1, s));
   CK(upload_ints(x.w.tiles, tiles.data(), (int)tiles.size(), s));
   if (ctx) {
@@ -804,6 +864,8 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
     CK(upload_ints(x.w.sseq, sseq.data(), (int)sseq.size(), s));
     x.nshort = (int)srow.size();
   }
+  RET(upload_split(x, hs_short, x.w.dint, &x.sp_short));
+  RET(upload_split(x, hs_tail, x.w.dint + hs_short.ints(), &x.sp_rows));
   RET(upload_pools(x));
   CK(launch_plan_prefill(x.w.cu, x.ctx, P, T, tok, m->cfg.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
                          x.w.positions, x.w.slots, x.w.last_idx, x.w.last_pos, m->status, s));
@@ -876,9 +938,14 @@ int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   x.m = m;
   x.s = s;
   x.kv = kv;
-  RET(ensure_workspace(m, B, B, m->C, 1, skinny_part_bytes(m, B), &x.w));
+  std::vector<int> nk(B);
+  for (int b = 0; b < B; ++b) nk[b] = seq_lens[b] + 1;
+  const HostSplit hs = make_split(nk);
+  RET(ensure_workspace(m, B, B, m->C, 1, skinny_part_bytes(m, B), &x.w, hs.ints(),
+                       split_part_floats(hs.num_units(), m->cfg.n_q, m->cfg.d_head)));
   CK(upload_ints(x.w.cu, seq_lens, B, s));
   RET(upload_pools(x));
+  RET(upload_split(x, hs, x.w.dint, &x.sp_rows));
   const auto& c = m->cfg;
   CK(launch_plan_decode(x.w.cu, B, tokens, c.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
                         x.w.positions, x.w.slots, m->status, s));
