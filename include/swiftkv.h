@@ -213,8 +213,9 @@ int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspa
 /* Kernel family for GEMMs with more than 64 rows: 0 = tcgen05 on CTA pairs (cta_group::2,
  * 256 x 256 tiles, default), 1 = warp-level mma.sync tiles, 2 = tcgen05 on single CTAs
  * (128 x 256 tiles); 1 and 2 are kept as cross-checks. All are fed by TMA where tcgen05 is
- * used. GEMMs with at most 64 rows always use the skinny kernel (one CTA per pair of
- * 16-column strips streaming its weights over the whole K). */
+ * used. GEMMs with at most 64 rows use the persistent TMA-fed skinny kernel (impl 6 of
+ * swiftkv_gemm_bf16) when the weight has at least SMs / 2 tiles of 64 rows, else the
+ * cp.async one (impl 5). */
 int swiftkv_set_gemm_impl(swiftkv_model* m, int impl);
 
 /* Kernel family for the prompt tokens' attention: 0 = tcgen05 with TMA-staged paged K/V
@@ -226,7 +227,9 @@ int swiftkv_set_attention_impl(swiftkv_model* m, int impl);
  *   impl 0 = tcgen05 single CTA, 1 = mma.sync tiles, 2 = skinny split-K (M <= 64; allocates
  *   and frees its own scratch and synchronises the device), 3 = tcgen05 with CTA pairs
  *   sharing the weight tile by TMA multicast, 4 = tcgen05 CTA pairs (cta_group::2),
- *   5 = skinny without split-K (M <= 64; what the model uses for its M <= 64 GEMMs)
+ *   5 = skinny, one CTA per pair of 16-column strips over the whole K (M <= 64),
+ *   6 = skinny, persistent, TMA-fed, 64-row weight tiles over the whole K (M <= 64 and
+ *       N / 64 >= SMs / 2, else SWIFTKV_EUNSUPPORTED)
  *   status  device int or NULL: receives SWIFTKV_STATUS_TIMEOUT if a bounded wait expired
  * Requires K % 64 == 0 and N % 128 == 0. */
 int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,

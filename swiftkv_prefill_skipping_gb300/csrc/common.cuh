@@ -50,7 +50,7 @@ struct EpiParams {
   int cache_base;            // EPI_QKV: the layer's cache; EPI_WIDE_KV: first skipped cache
 };
 
-__device__ __forceinline__ int pair_half(const EpiParams& p) {
+__host__ __device__ __forceinline__ int pair_half(const EpiParams& p) {
   return (p.kind == EPI_QKV || p.kind == EPI_WIDE_KV) ? (p.d_head >> 1) : 64;
 }
 

@@ -23,6 +23,10 @@ cudaError_t launch_gemm_skinny(const bf16* A, int lda, const bf16* B, int K, con
                                float* scratch, int num_sms, cudaStream_t stream);
 // M <= 64 without split-K: each CTA streams 32 weight rows over the full K (no scratch).
 cudaError_t launch_gemv(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep, cudaStream_t stream);
+// Persistent TMA-fed skinny GEMM for M <= 64 over 64-row weight tiles; cudaErrorNotSupported
+// outside its shapes, including matrices with fewer than num_sms / 2 tiles (launch_gemv then).
+cudaError_t launch_gemv_tma(const bf16* A, int lda, const bf16* W, int K, const EpiParams& ep, int num_sms,
+                            int* status, cudaStream_t stream);
 // tcgen05 (TMEM accumulator, TMA-fed) GEMM; returns cudaErrorNotSupported if the shape is not
 // handled, so the caller can fall back to launch_gemm_tiled.
 // mode 0: one CTA per 128 x 256 tile; 1: CTA pairs share the weight tile through TMA

@@ -242,7 +242,9 @@ size_t skinny_part_bytes(const swiftkv_model* m, int M) {
   size_t mx = 16;
   int shapes[][2] = {{m->Nq + 2 * m->Nkv, c.d}, {m->Nq, c.d}, {c.d, m->Nq}, {2 * m->Fp, c.d},
                      {c.d, m->Fp}, {c.vocab, c.d}, {std::max(m->Nwide, 64), c.d}};
-  for (auto& s : shapes) mx = std::max(mx, skinny_scratch_bytes(M, s[0], s[1], m->num_sms));
+  for (auto& s : shapes) {
+    mx = std::max(mx, skinny_scratch_bytes(M, s[0], s[1], m->num_sms));
+  }
   return mx;
 }
 
@@ -327,7 +329,8 @@ int gemm(Ctx& x, const char* name, const bf16* A, int lda, const bf16* B, int K,
   Prof pr(x.m, x.s, name, 1, flops, bytes);
   cudaError_t e;
   if (skinny) {
-    e = launch_gemv(A, lda, B, K, ep, x.s);
+    e = launch_gemv_tma(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s);
+    if (e == cudaErrorNotSupported) e = launch_gemv(A, lda, B, K, ep, x.s);
     if (e == cudaErrorNotSupported) e = launch_gemm_skinny(A, lda, B, K, ep, x.w.part, x.m->num_sms, x.s);
   } else {
     e = cudaErrorNotSupported;
@@ -715,6 +718,8 @@ int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int 
     e = launch_gemm_tiled(a, K, b, K, ep, s);
   } else if (impl == 5) {
     e = M > 64 ? cudaErrorNotSupported : launch_gemv(a, K, b, K, ep, s);
+  } else if (impl == 6) {
+    e = M > 64 ? cudaErrorNotSupported : launch_gemv_tma(a, K, b, K, ep, sms, st, s);
   } else if (impl == 2) {
     if (M > 64) e = cudaErrorNotSupported;
     else {

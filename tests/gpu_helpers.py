@@ -14,6 +14,10 @@ LOGIT_ABS_TOL = 5e-2   # last-token logits, max |gpu - ref|
 # d_head = 128 shape with several 128-row GEMM tiles and attention tiles (tcgen05 attention)
 SMALL128 = synth.ModelShape("small-d128", L=6, d=512, n_q=4, n_kv=2, d_h=128, ffn=1000, vocab=2048,
                             rope_theta=500000.0)
+# wide enough that the Q/K/V (6144), gate/up (9728), skipped-layer KV at l = 1 (6144) and LM
+# head (5120) GEMMs of the tail and of decode take the TMA-fed skinny kernel (>= 76 tiles)
+MEDIUM = synth.ModelShape("medium-wide", L=4, d=1024, n_q=32, n_kv=8, d_h=128, ffn=4864, vocab=5120,
+                          rope_theta=500000.0)
 # Q/K/V bias (Qwen-style), single KV head
 SMALL_BIAS = synth.ModelShape("small-bias", L=4, d=640, n_q=5, n_kv=1, d_h=128, ffn=704, vocab=1024,
                               rope_theta=1000000.0, qkv_bias=True)

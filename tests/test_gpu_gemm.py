@@ -67,3 +67,43 @@ def test_gemv_matches_torch_fp32(M, N, K):
     assert not torch.isnan(Cm).any()
     err = (Cm - ref).abs().max().item() / ref.abs().max().item()
     assert err < 2e-5, (M, N, K, err)
+
+
+# N / 64 >= 76 tiles (the TMA kernel's range on 152 SMs); K = 704 and 320 end inside a
+# 256-deep stage (the boxes past K read zeros)
+@pytest.mark.parametrize("M,N,K", [(1, 5120, 4096), (16, 9728, 512), (64, 5120, 14336), (37, 10240, 704),
+                                   (48, 128256, 256), (24, 7168, 5120), (5, 4864, 320)])
+def test_tma_gemv_matches_torch_fp32(M, N, K):
+    import torch
+    Cm, ref = _run(6, M, N, K)
+    assert not torch.isnan(Cm).any()
+    err = (Cm - ref).abs().max().item() / ref.abs().max().item()
+    assert err < 2e-5, (M, N, K, err)
+
+
+def test_tma_gemv_rejects_narrow_weights():
+    import torch
+    from swiftkv_prefill_skipping_gb300 import binding as B
+    with pytest.raises(B.SwiftKVError) as e:
+        _run(6, 16, 4096, 4096)
+    assert e.value.code == -9
+
+
+@pytest.mark.parametrize("N,K", [(5120, 4096), (9728, 704), (7168, 5120)])
+def test_tma_gemv_rows_do_not_depend_on_batch_size(N, K):
+    """A row's result is the same bits whatever M is."""
+    import torch
+    from swiftkv_prefill_skipping_gb300 import binding as B
+    g = torch.Generator(device="cuda").manual_seed(7)
+    A = (torch.randn(64, K, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    W = (torch.randn(N, K, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    outs = []
+    for M in (1, 17, 33, 64):
+        Cm = torch.empty((M, N), device="cuda")
+        B.check(B.lib().swiftkv_gemm_bf16(A.data_ptr(), W.data_ptr(), Cm.data_ptr(), M, N, K, 6, st.data_ptr(),
+                                          C.c_void_p(torch.cuda.current_stream().cuda_stream)))
+        outs.append(Cm[0].clone())
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert all(torch.equal(outs[0], o) for o in outs[1:])
