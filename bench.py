@@ -277,7 +277,8 @@ def run_ours(args, w, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     peaks, peak_src = load_peaks()
     n_dec_req = 0 if w.mixed else (args.decode_steps if args.decode_steps is not None else w.decode_steps)
-    batch = workload_batch(w, rank, reserve_tokens=n_dec_req + 1 if n_dec_req > 0 else 0)
+    # decode steps: one warm-up, the timed ones, and up to five profiled ones
+    batch = workload_batch(w, rank, reserve_tokens=n_dec_req + 6 if n_dec_req > 0 else 0)
     T, P = int(batch.cu_seqlens[-1]), int(len(batch.lens))
     want_cpu = (rank == 0 and world == 1 and not args.no_cpu_baseline)
 
@@ -439,8 +440,22 @@ def run_ours(args, w, rank, world, local_rank):
         d1.record(stream)
         torch.cuda.synchronize()
         tpot = max_over_ranks(d0.elapsed_time(d1) / n_dec, world, dev)
+        # one more profiled pass of a few steps: where a decode step's time goes
+        n_prof = min(n_dec, 5)
+        binding.check(binding.lib().swiftkv_profile_begin(model.handle))
+        for _ in range(n_prof):
+            _, nxt = api.decode_step(model, nxt, lens, kv, stream=stream)
+            lens = [x + 1 for x in lens]
+        torch.cuda.synchronize()
+        n_ent = binding.check(binding.lib().swiftkv_profile_end(model.handle, entries, 64))
+        dk = {}
+        for i in range(n_ent):
+            e = entries[i]
+            dk[e.name.decode()] = {"ms_per_step": e.ms / n_prof, "calls_per_step": e.calls / n_prof,
+                                   "gbs": (e.bytes / (e.ms / 1e3) / 1e9) if e.bytes else None}
         decode = {"steps": n_dec, "batch": P, "tpot_ms": tpot, "ttft_ms": ms_per_step,
-                  "decode_tokens_per_s": P * 1e3 / tpot}
+                  "decode_tokens_per_s": P * 1e3 / tpot,
+                  "kernels_profiled": dict(sorted(dk.items(), key=lambda kv_: -kv_[1]["ms_per_step"]))}
 
     cpu = None
     if want_cpu:

@@ -94,22 +94,25 @@ cudaError_t launch_attention_decode(const bf16* q, int ldq, const bf16* k_pool, 
 
 // Key-split single-row attention (decode tokens, SwiftKV tail rows, rows of short chunks).
 // Items b = 0..num_items-1 are mapped as in launch_attention_decode (rows / seqs / qpos);
-// units [2 * num_units] = (item, split) pairs, item-major with splits ascending; ubeg
+// units [3 * num_units] = (item, first key, keys), item-major with keys ascending; ubeg
 // [num_items + 1] = first unit of each item; part = split_part_floats(num_units, ...) floats.
 struct SplitPlan {
   const int* units;
   const int* ubeg;
-  int num_units, num_items, split_keys;
+  int num_units, num_items;
   bool any_split;  // some item has more than one unit (the combine pass runs)
   float* part;
 };
-// Host: splits items with nkeys[b] keys into units of kSplitKeys keys; returns the split.
+// Host: splits item b's nkeys[b] keys into units of split_keys_for(nkeys[b]) keys (a
+// multiple of 64 that depends on nothing but the row's own length).
 constexpr int kSplitKeys = 256;
-int split_plan_host(const int* nkeys, int items, std::vector<int>* units, std::vector<int>* ubeg);
+int split_keys_for(int nkeys);
+void split_plan_host(const int* nkeys, int items, std::vector<int>* units, std::vector<int>* ubeg);
 size_t split_part_floats(int num_units, int n_q, int d_head);
 cudaError_t launch_attention_decode_split(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                           const int* block_table, int max_pages, int num_pages, const int* qpos,
                                           const int* rows, const int* seqs, const SplitPlan& plan, int n_q,
-                                          int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream);
+                                          int n_kv, int d_head, bf16* out, int ldo, int num_sms,
+                                          cudaStream_t stream);
 
 }  // namespace skv

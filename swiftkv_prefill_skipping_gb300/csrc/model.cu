@@ -267,14 +267,13 @@ struct Ctx {
 // Host side of a key-split plan: units then ubeg in one vector (one upload).
 struct HostSplit {
   std::vector<int> units, ubeg;
-  int split = 0;
   size_t ints() const { return units.size() + ubeg.size(); }
-  int num_units() const { return (int)(units.size() / 2); }
+  int num_units() const { return (int)(units.size() / 3); }
 };
 
 HostSplit make_split(const std::vector<int>& nkeys) {
   HostSplit h;
-  if (!nkeys.empty()) h.split = split_plan_host(nkeys.data(), (int)nkeys.size(), &h.units, &h.ubeg);
+  if (!nkeys.empty()) split_plan_host(nkeys.data(), (int)nkeys.size(), &h.units, &h.ubeg);
   return h;
 }
 
@@ -288,7 +287,6 @@ int upload_split(Ctx& x, const HostSplit& h, int* dst, SplitPlan* p) {
   p->ubeg = dst + h.units.size();
   p->num_units = h.num_units();
   p->num_items = (int)h.ubeg.size() - 1;
-  p->split_keys = h.split;
   p->any_split = p->num_units > p->num_items;
   p->part = x.w.dpart;
   return SWIFTKV_OK;
@@ -381,7 +379,7 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
     if (m->attn_impl == 0 && sp.num_units > 0)
       r = launch_attention_decode_split(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
                                         x.kv->num_pages, pos, rows, seqs, sp, c.n_q, c.n_kv, c.d_head, ab, m->Nq,
-                                        x.s);
+                                        m->num_sms, x.s);
     if (r == cudaErrorNotSupported)
       r = launch_attention_decode(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
                                   pos, items, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s, rows, seqs);
