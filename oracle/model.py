@@ -194,7 +194,68 @@ class Weights:
         return np.asarray(self._embed_fn(np.asarray(tokens)), dtype=F64)
 
 
-KV = Tuple[np.ndarray, np.ndarray]   # (K, V), each [tokens, n_kv, d_h], bfloat16 values
+# ----------------------------------------------------------------------------- FP8 KV cache
+#
+# Per-token FP8 KV-cache quantization ([S] 3.4 AcrossKV "Complementarity with KV
+# quantization", Appendix B.1 / Table B.1; [S] Table 3): post-training, no retraining.
+# Reading: each token's K (after RoPE) and V vector of one KV head -- the bfloat16 values a
+# bf16 cache would hold -- gets one float32 scale, amax / 448, and float8 e4m3 codes of
+# value / scale (448 is the largest finite e4m3 value); the attention uses code * scale.
+
+E4M3_MAX = 448.0
+
+
+def e4m3(x) -> np.ndarray:
+    """Round to the nearest float8 e4m3 ("fn": no infinities, largest finite 448) value,
+    ties to even: 4 significant bits for |x| >= 2^-6, steps of 2^-9 below (subnormals);
+    magnitudes past 448 saturate to 448."""
+    x = np.asarray(x, dtype=F64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                  # a = m * 2^e, m in [0.5, 1): floor(log2 a) = e - 1
+    quantum = np.exp2(np.maximum(e - 1.0, -6.0) - 3.0)
+    r = np.rint(a / quantum) * quantum
+    return np.sign(x) * np.minimum(r, E4M3_MAX)
+
+
+def fp8_quantize(v: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Codes (as their e4m3 values) and float32 scales of bfloat16 vectors v[..., d_h]:
+    scale = float32(amax) / 448 in float32, code = e4m3(float32(v) / scale) with a
+    float32 division (a zero vector has scale 0 and codes 0)."""
+    v32 = np.asarray(v, dtype=np.float32)
+    amax = np.max(np.abs(v32), axis=-1, keepdims=True)
+    scale = (amax / np.float32(E4M3_MAX)).astype(np.float32)
+    safe = np.where(scale > 0, scale, np.float32(1.0))
+    q = (v32 / safe).astype(np.float32)
+    codes = np.where(scale > 0, e4m3(q), 0.0)
+    return codes, scale[..., 0]
+
+
+def fp8_dequantize(codes: np.ndarray, scale: np.ndarray) -> np.ndarray:
+    return np.asarray(codes, F64) * np.asarray(scale, F64)[..., None]
+
+
+_KV_FP8 = [False]
+
+
+class kv_cache_fp8:
+    """Context manager: the KV cache stores per-token FP8 (every cache write goes through
+    fp8_quantize / fp8_dequantize), as with a float8 KV cache."""
+
+    def __enter__(self):
+        _KV_FP8.append(True)
+        return self
+
+    def __exit__(self, *exc):
+        _KV_FP8.pop()
+        return False
+
+
+def _cache_values(t: np.ndarray) -> np.ndarray:
+    """What the cache holds for the bfloat16 K or V rows t[tokens, n_kv, d_h]."""
+    return fp8_dequantize(*fp8_quantize(t)) if _KV_FP8[-1] else t
+
+
+KV = Tuple[np.ndarray, np.ndarray]   # (K, V), each [tokens, n_kv, d_h], values the cache holds
 
 
 def _heads(x: np.ndarray, h: int, d_h: int) -> np.ndarray:
@@ -207,7 +268,7 @@ def qkv_proj(cfg: Config, lw: Layer, x: np.ndarray, pos: np.ndarray) -> Tuple[np
     q = rope(_heads(linear(u, lw.wq, lw.bq), cfg.n_q, cfg.d_h), pos, cfg.rope_theta)
     k = rope(_heads(linear(u, lw.wk, lw.bk), cfg.n_kv, cfg.d_h), pos, cfg.rope_theta)
     v = _heads(linear(u, lw.wv, lw.bv), cfg.n_kv, cfg.d_h)
-    return bf16(q), (bf16(k), bf16(v))
+    return bf16(q), (_cache_values(bf16(k)), _cache_values(bf16(v)))
 
 
 def q_proj(cfg: Config, lw: Layer, x: np.ndarray, pos: np.ndarray) -> np.ndarray:
@@ -224,7 +285,7 @@ def swiftkv_kv(cfg: Config, rep: Layer, x_l: np.ndarray, pos: np.ndarray) -> KV:
     u = bf16(rms_norm(x_l, rep.gamma_attn, cfg.rms_eps))
     k = rope(_heads(linear(u, rep.wk, rep.bk), cfg.n_kv, cfg.d_h), pos, cfg.rope_theta)
     v = _heads(linear(u, rep.wv, rep.bv), cfg.n_kv, cfg.d_h)
-    return bf16(k), bf16(v)
+    return _cache_values(bf16(k)), _cache_values(bf16(v))
 
 
 def attn_out(cfg: Config, lw: Layer, x: np.ndarray, q: np.ndarray, kv: KV, q_pos: np.ndarray,

@@ -253,3 +253,24 @@ def test_forward_chunks_equal_whole_prompt_and_decode(w_gain, tokens):
         np.testing.assert_allclose(a[0], b[0], **TOL)
     with pytest.raises(ValueError):
         M.swiftkv_forward_one(CFG, w_gain, c_all, [], l, g)
+
+
+def test_fp8_cache_mode_quantizes_every_cache_write(w_gain, tokens):
+    """Under kv_cache_fp8 every cache (full layers and skipped groups) holds per-token
+    code * scale values of its bf16 rows; the logits move by a small nonzero amount."""
+    l, g = 2, 2
+    c_bf, lg_bf = M.swiftkv_prefill_one(CFG, w_gain, tokens, l, g)
+    with M.kv_cache_fp8():
+        c_f8, lg_f8 = M.swiftkv_prefill_one(CFG, w_gain, tokens, l, g)
+        c_dec, _ = M.swiftkv_decode_step(CFG, w_gain, c_f8, 7, l, g)
+    for c in range(len(c_f8)):
+        for t in range(2):
+            got = c_f8[c][t]
+            codes, scale = M.fp8_quantize(got)
+            np.testing.assert_array_equal(M.fp8_dequantize(codes, scale), got)   # already on the grid
+            assert np.abs(got - c_bf[c][t]).max() > 0
+            rel = np.linalg.norm(got - c_bf[c][t]) / np.linalg.norm(c_bf[c][t])
+            assert rel < 0.05, (c, t, rel)
+        assert c_dec[c][0].shape[0] == len(tokens) + 1
+    d = np.abs(lg_f8 - lg_bf).max()
+    assert 0 < d < 0.5, d

@@ -85,3 +85,32 @@ def w_gain():
 def tokens():
     import synth
     return synth.uniform_int(synth.SEED_INPUTS, 12, 48, 0, synth.TINY.vocab - 1)
+
+
+def test_fp8_scale_off_by_range_is_caught(monkeypatch):
+    """Scales computed for the wrong e4m3 range (amax / 240) leave the codes off +-448."""
+    good = M.fp8_quantize
+
+    def bad(v):
+        codes, scale = good(v)
+        return M.e4m3(codes * 240.0 / 448.0), (scale * np.float32(448.0 / 240.0)).astype(np.float32)
+    monkeypatch.setattr(M, "fp8_quantize", bad)
+    assert _fails(TN.test_fp8_quantize_per_token_and_head)
+
+
+def test_fp8_e4m3_with_bf16_precision_is_caught(monkeypatch):
+    """Rounding codes to 8 significant bits (a bf16 'fp8') is not e4m3."""
+    monkeypatch.setattr(M, "e4m3", lambda x: np.minimum(np.abs(M.bf16(x)), 448.0) * np.sign(x))
+    assert _fails(TN.test_e4m3_matches_torch_float8_cast)
+
+
+def test_fp8_mode_skipping_v_is_caught(monkeypatch, w_gain, tokens):
+    """A cache mode that quantizes K but stores V unquantized is caught by the model pin."""
+    good = M._cache_values
+    calls = {"n": 0}
+
+    def k_only(t):
+        calls["n"] += 1
+        return good(t) if calls["n"] % 2 == 1 else t   # K then V at every write
+    monkeypatch.setattr(M, "_cache_values", k_only)
+    assert _fails(TM.test_fp8_cache_mode_quantizes_every_cache_write, w_gain, tokens)

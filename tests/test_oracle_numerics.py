@@ -157,3 +157,47 @@ def test_precision_mode_rounds_softmax_weights_before_v():
     assert not np.array_equal(got, exact)
     np.testing.assert_allclose(got, exact, rtol=2e-3, atol=2e-3)
     assert M.fp16(1 + 2 ** -11) == 1.0 and M.fp16(1 + 3 * 2 ** -11) == 1 + 2 ** -9   # ties to even
+
+
+def test_e4m3_matches_torch_float8_cast():
+    """float8 e4m3 rounding against torch's float8_e4m3fn cast (round to nearest even)
+    over normals, subnormals, exact ties and values just below powers of two."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    x = np.concatenate([
+        rng.uniform(-448, 448, 4000), rng.uniform(-1, 1, 4000) * 2.0 ** rng.integers(-12, 0, 4000),
+        np.array([0.0, 1.0625, 1.1875, -1.1875, 2 ** -10, 3 * 2 ** -10, 5 * 2 ** -11, 2 ** -6, 255.99, 447.9,
+                  np.nextafter(256.0, 0.0), np.nextafter(2.0 ** -6, 0.0)])]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(M.e4m3(x.astype(np.float64)), ref)
+
+
+def test_e4m3_grid_by_hand():
+    # 4 significant bits: 1, 1.125, ..., 1.875 between 1 and 2; 2^-9 steps below 2^-6
+    assert M.e4m3(1.0625) == 1.0 and M.e4m3(1.1875) == 1.25 and M.e4m3(1.2) == 1.25
+    assert M.e4m3(17.0) == 16.0 and M.e4m3(17.5) == 18.0
+    assert M.e4m3(2 ** -10) == 0.0 and M.e4m3(3 * 2 ** -10) == 2 ** -8
+    assert M.e4m3(500.0) == 448.0 and M.e4m3(-1e9) == -448.0
+
+
+def test_fp8_quantize_per_token_and_head():
+    """One scale per (token, head) vector: the largest magnitude maps to +-448 exactly,
+    every code is an e4m3 value, dequantized values are within half an e4m3 step, a zero
+    vector stays zero, and quantization is per vector (scaling one vector changes only its
+    own scale)."""
+    rng = np.random.default_rng(9)
+    v = M.bf16(rng.normal(0, 1, (5, 3, 64)) * np.array([1e-3, 1.0, 50.0])[None, :, None])
+    v[2, 1] = 0.0
+    codes, scale = M.fp8_quantize(v)
+    assert scale.shape == (5, 3) and scale.dtype == np.float32
+    np.testing.assert_array_equal(M.e4m3(codes), codes)
+    amax = np.abs(codes).max(axis=-1)
+    assert np.all(amax[scale > 0] == 448.0) and scale[2, 1] == 0 and np.all(codes[2, 1] == 0)
+    deq = M.fp8_dequantize(codes, scale)
+    step = np.exp2(np.floor(np.log2(np.maximum(np.abs(codes), 2 ** -6))) - 3) * scale[..., None]
+    assert np.all(np.abs(deq - v) <= 0.5 * step * (1 + 1e-6) + 1e-12)
+    v2 = v.copy()
+    v2[0, 0] *= 4.0
+    c2, s2 = M.fp8_quantize(v2)
+    assert s2[0, 0] == np.float32(scale[0, 0] * 4) and np.array_equal(s2[1:], scale[1:])
+    np.testing.assert_array_equal(c2[1:], codes[1:])
