@@ -208,7 +208,7 @@ def workload_config(w, batch):
                         f"{w.mix_decode_ctx[1]}], 16-token pages",
             "chunks": len(w.mix_chunks), "decode_tokens": int(w.mix_decode),
             "tokens_per_step": int(batch.cu_seqlens[-1]), "cached_tokens": int(batch.extra["ctx"].sum()),
-            "l": w.l, "g": w.g, "L": w.shape.L,
+            "l": w.l, "g": w.g, "L": w.shape.L, "kv_cache": w.kv_dtype,
             "l2": "inputs larger than L2 (all weights, >=14 GB, stream from HBM every step)",
             "parallelism": "replicas (one independent serving step per GPU)",
         }
@@ -217,7 +217,7 @@ def workload_config(w, batch):
                     f"AcrossKV g={w.g}, {w.num_prompts} prompts U[{w.len_lo},{w.len_hi}] packed varlen, "
                     f"16-token pages",
         "prompts": int(w.num_prompts), "tokens_per_step": int(batch.cu_seqlens[-1]),
-        "l": w.l, "g": w.g, "L": w.shape.L,
+        "l": w.l, "g": w.g, "L": w.shape.L, "kv_cache": w.kv_dtype,
         "l2": "inputs larger than L2 (all weights, >=14 GB, stream from HBM every step)",
         "parallelism": "replicas (one independent prefill per GPU)",
     }
@@ -296,7 +296,7 @@ def run_ours(args, w, rank, world, local_rank):
                 raw_globals = wts
     log(f"[ours] rank {rank}: weights generated + loaded in {time.time() - t0:.1f}s "
         f"({model.memory()[0] / 2**30:.1f} GiB on device)")
-    kv = api.KVCache(model, batch.num_pages, batch.block_table, device=dev)
+    kv = api.KVCache(model, batch.num_pages, batch.block_table, device=dev, dtype=w.kv_dtype)
     tokens = torch.as_tensor(batch.tokens, device=dev)
     logits = torch.empty((P, w.shape.vocab), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream()
@@ -482,6 +482,7 @@ def run_ours(args, w, rank, world, local_rank):
             "executed_tflops": exec_tflops,
             "executed_frac_of_peak": {"burst": exec_tflops / peak_burst, "sustained": exec_tflops / peak_sus},
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "kv_cache": kv_cache_info(model, w),
             "decode": decode,
             "clocks": clocks,
             "kernels": {k: {"ms_per_step": v["ms"] / args.steps, "calls_per_step": v["calls"] / args.steps,
@@ -492,6 +493,17 @@ def run_ours(args, w, rank, world, local_rank):
         print(json.dumps(line), flush=True)
     model.free()
     return 0
+
+
+def kv_cache_info(model, w) -> dict:
+    """KV-cache bytes per token (all caches, K and V, scales included) and the reduction
+    against an ordinary model's bf16 cache (L caches)."""
+    sh = w.shape
+    per_head = sh.d_h * (1 if w.kv_dtype == "fp8" else 2) + (4 if w.kv_dtype == "fp8" else 0)
+    per_token = model.num_caches * 2 * sh.n_kv * per_head
+    ordinary = sh.L * 2 * sh.n_kv * sh.d_h * 2
+    return {"dtype": w.kv_dtype, "caches": model.num_caches, "bytes_per_token": per_token,
+            "reduction_vs_ordinary_bf16": 1.0 - per_token / ordinary}
 
 
 def fill_prefixes(model, kv, batch, stream, dev, max_tokens: int = 16384) -> None:

@@ -106,10 +106,15 @@ typedef struct {
 /* Paged KV cache, owned by the caller (device memory).
  * There are num_caches = swiftkv_cache_count(L, l, g) caches: caches 0..l-1
  * belong to the full layers, cache l + i to the i-th group of skipped layers.
- * Each cache has a K pool and a V pool, bf16 [num_pages][n_kv][page_size][d_head]:
- * one (page, head) block of page_size * d_head elements is contiguous.
+ * Each cache has a K pool and a V pool of [num_pages][n_kv][page_size][d_head]
+ * elements: one (page, head) block of page_size * d_head elements is contiguous.
  * Token at position p of sequence s lives in page block_table[s][p / page_size],
- * row p % page_size. */
+ * row p % page_size.
+ * kv_dtype 0: bf16 elements. kv_dtype 1: per-token FP8 ("SwiftKV" summary, AcrossKV,
+ * complementarity with KV quantization, Appendix B.1 / Table B.1): uint8 float8-e4m3
+ * codes, and for every (page, head, row) one float32 scale in k_scale / v_scale pools of
+ * [num_pages][n_kv][page_size]; the value is code * scale, scale = max|v| / 448 over the
+ * token's d_head values of that head (K after RoPE). */
 typedef struct {
   void* const* k_pool;        /* host array [num_caches] of device pointers */
   void* const* v_pool;        /* host array [num_caches] of device pointers */
@@ -118,6 +123,9 @@ typedef struct {
   int page_size;              /* must be 16 */
   const int32_t* block_table; /* device int32 [num_seqs][max_pages_per_seq] */
   int max_pages_per_seq;
+  int kv_dtype;               /* 0 bf16, 1 fp8 e4m3 + per-token scales */
+  void* const* k_scale;       /* kv_dtype 1: host array [num_caches] of device float pools; else NULL */
+  void* const* v_scale;
 } swiftkv_kv_pages;
 
 typedef struct swiftkv_model swiftkv_model; /* opaque; owns device weights + workspace */

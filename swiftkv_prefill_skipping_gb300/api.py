@@ -108,42 +108,73 @@ def load_synthetic(shape, l: int, g: int = 1, seed: int = 0, gain_std: float = 0
 
 
 class KVCache:
-    """Caller-owned paged KV cache: num_caches x (K, V) pools of
-    bf16 [num_pages][n_kv][16][d_h], plus a device block table."""
+    """Caller-owned paged KV cache: num_caches x (K, V) pools of [num_pages][n_kv][16][d_h]
+    elements plus a device block table. dtype "bf16": bfloat16 elements; dtype "fp8":
+    uint8 float8-e4m3 codes with float32 scales [num_pages][n_kv][16] per pool (per-token
+    FP8)."""
 
-    def __init__(self, model: Model, num_pages: int, block_table: np.ndarray, device=None):
+    def __init__(self, model: Model, num_pages: int, block_table: np.ndarray, device=None, dtype: str = "bf16"):
+        if dtype not in ("bf16", "fp8"):
+            raise ValueError(f"KV cache dtype {dtype!r}")
         s = model.shape
         dev = device or torch.device("cuda", torch.cuda.current_device())
-        self.num_pages = num_pages
+        self.num_pages, self.dtype = num_pages, dtype
         shape = (model.num_caches, num_pages, s.n_kv, 16, s.d_h)
-        self.k = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
-        self.v = torch.zeros(shape, dtype=torch.bfloat16, device=dev)
+        elem = torch.bfloat16 if dtype == "bf16" else torch.uint8
+        self.k = torch.zeros(shape, dtype=elem, device=dev)
+        self.v = torch.zeros(shape, dtype=elem, device=dev)
+        self.k_scale = self.v_scale = None
+        if dtype == "fp8":
+            self.k_scale = torch.zeros(shape[:-1], dtype=torch.float32, device=dev)
+            self.v_scale = torch.zeros(shape[:-1], dtype=torch.float32, device=dev)
         self.block_table = torch.as_tensor(np.ascontiguousarray(block_table, dtype=np.int32), device=dev)
-        self._kp = (C.c_void_p * model.num_caches)(*[self.k[c].data_ptr() for c in range(model.num_caches)])
-        self._vp = (C.c_void_p * model.num_caches)(*[self.v[c].data_ptr() for c in range(model.num_caches)])
-        self.pages = B.KVPages(C.cast(self._kp, C.POINTER(C.c_void_p)), C.cast(self._vp, C.POINTER(C.c_void_p)),
-                               model.num_caches, num_pages, 16, self.block_table.data_ptr(),
-                               self.block_table.shape[1])
+        n = model.num_caches
+        self._kp = (C.c_void_p * n)(*[self.k[c].data_ptr() for c in range(n)])
+        self._vp = (C.c_void_p * n)(*[self.v[c].data_ptr() for c in range(n)])
+        self._ks = self._vs = None
+        if dtype == "fp8":
+            self._ks = (C.c_void_p * n)(*[self.k_scale[c].data_ptr() for c in range(n)])
+            self._vs = (C.c_void_p * n)(*[self.v_scale[c].data_ptr() for c in range(n)])
+        self.num_caches = n
+        self.pages = self._pages(self.block_table)
+
+    def _pages(self, block_table: torch.Tensor) -> B.KVPages:
+        ptr = lambda a: C.cast(a, C.POINTER(C.c_void_p)) if a is not None else None  # noqa: E731
+        return B.KVPages(ptr(self._kp), ptr(self._vp), self.num_caches, self.num_pages, 16, block_table.data_ptr(),
+                         block_table.shape[1], 1 if self.dtype == "fp8" else 0, ptr(self._ks), ptr(self._vs))
 
     def view(self, rows: Sequence[int]) -> "KVCache":
         """The same pools with block table rows `rows` (in that order): a batch that holds
         only some of the sequences, or holds them in another order."""
         out = object.__new__(KVCache)
-        out.num_pages, out.k, out.v, out._kp, out._vp = self.num_pages, self.k, self.v, self._kp, self._vp
+        out.__dict__.update(self.__dict__)
         out.block_table = self.block_table[torch.as_tensor(list(rows), dtype=torch.long,
                                                            device=self.block_table.device)].contiguous()
-        out.pages = B.KVPages(C.cast(self._kp, C.POINTER(C.c_void_p)), C.cast(self._vp, C.POINTER(C.c_void_p)),
-                              self.pages.num_caches, self.num_pages, 16, out.block_table.data_ptr(),
-                              out.block_table.shape[1])
+        out.pages = out._pages(out.block_table)
         return out
 
-    def gather(self, c: int, s: int, n: int, which: str = "k") -> torch.Tensor:
-        """Cache c's first n rows of sequence s, [n, n_kv, d_h] (test/inspection helper)."""
-        pool = self.k[c] if which == "k" else self.v[c]
+    def _rows(self, pool: torch.Tensor, s: int, n: int) -> torch.Tensor:
         bt = self.block_table[s]
         pos = torch.arange(n, device=pool.device)
-        pages = bt[pos // 16].long()
-        return pool[pages, :, pos % 16, :]
+        return pool[bt[pos // 16].long(), :, pos % 16]
+
+    def gather(self, c: int, s: int, n: int, which: str = "k") -> torch.Tensor:
+        """Cache c's first n rows of sequence s, [n, n_kv, d_h] (test/inspection helper);
+        for an fp8 cache the values code * scale in float32."""
+        pool = self.k[c] if which == "k" else self.v[c]
+        if self.dtype == "bf16":
+            return self._rows(pool, s, n)
+        return self.codes(c, s, n, which) * self.scales(c, s, n, which)[..., None]
+
+    def codes(self, c: int, s: int, n: int, which: str = "k") -> torch.Tensor:
+        """fp8 cache: the e4m3 codes of cache c's first n rows of sequence s, as float32."""
+        pool = self.k[c] if which == "k" else self.v[c]
+        return self._rows(pool, s, n).view(torch.float8_e4m3fn).float()
+
+    def scales(self, c: int, s: int, n: int, which: str = "k") -> torch.Tensor:
+        """fp8 cache: the float32 scales [n, n_kv] of cache c's first n rows of sequence s."""
+        pool = self.k_scale[c] if which == "k" else self.v_scale[c]
+        return self._rows(pool, s, n)
 
 
 def prefill(model: Model, tokens: torch.Tensor, cu_seqlens: Sequence[int], kv: KVCache,

@@ -60,7 +60,8 @@ class HostWeights(C.Structure):
 class KVPages(C.Structure):
     _fields_ = [("k_pool", C.POINTER(C.c_void_p)), ("v_pool", C.POINTER(C.c_void_p)),
                 ("num_caches", C.c_int), ("num_pages", C.c_int), ("page_size", C.c_int),
-                ("block_table", C.c_void_p), ("max_pages_per_seq", C.c_int)]
+                ("block_table", C.c_void_p), ("max_pages_per_seq", C.c_int), ("kv_dtype", C.c_int),
+                ("k_scale", C.POINTER(C.c_void_p)), ("v_scale", C.POINTER(C.c_void_p))]
 
 
 class ProfileEntry(C.Structure):

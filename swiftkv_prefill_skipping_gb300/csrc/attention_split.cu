@@ -261,6 +261,277 @@ __global__ void __launch_bounds__(SW * 32, 1) attn_split_kernel(
   cp_async_wait<0>();
 }
 
+// FP8 cache variant of attn_split_kernel: pages hold e4m3 codes (16*d_head bytes per
+// (page, head) block) and one float32 scale per key row. The ring stages K codes, V codes,
+// both scale rows and the unit's Q. S: the K codes go to the tensor core without a
+// shared-memory pass -- ldmatrix reads a 16-dim slice of 8 keys as 8 two-code elements, so a
+// thread receives 4 consecutive dims of one key, converted (exactly) to f16; Q's fragments
+// are built with the same dim order, so the dot products are unchanged -- with f16 Q,
+// fp32 accumulate, then each score times its key's scale. P V: ldmatrix.trans on the V
+// codes gives a thread two keys x two adjacent dims; byte permutes split them into an
+// even-dim and an odd-dim fragment (exact f16). V's per-key scale rides on P: P' = p *
+// s_v / S_ref in f16, S_ref the largest V scale seen so far in the unit (O is rescaled
+// when it grows, like the softmax max), and O * S_ref is the unnormalised output.
+constexpr int SSTAGES8 = 3;
+
+template <int D>
+struct Sp8 {
+  static constexpr int CODES = kPageSize * D;        // bytes of one (page, head) K or V block
+  static constexpr int QB = SMAXG * D * 2;            // bytes of the unit's query rows (bf16)
+  static constexpr int STAGE = 2 * CODES + 2 * kPageSize * 4 + QB;
+  static constexpr int SMEM = SW * SSTAGES8 * STAGE;
+  static constexpr int CHB = D / 16;                  // 16-byte chunks per code row
+};
+
+template <int D>
+__global__ void __launch_bounds__(SW * 32, 1) attn_split_fp8_kernel(
+    const bf16* __restrict__ q, int ldq, const uint8_t* __restrict__ kpool, const uint8_t* __restrict__ vpool,
+    const float* __restrict__ kscale, const float* __restrict__ vscale, const int* __restrict__ bt, int max_pages,
+    int num_pages, const int* __restrict__ qpos, const int* __restrict__ rows, const int* __restrict__ seqs,
+    const int* __restrict__ units, int num_units, int n_q, int n_kv, bf16* __restrict__ out, int ldo,
+    float* __restrict__ part, float scale_log2) {
+  using S = Sp8<D>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  unsigned char* ring = smem + (size_t)warp * SSTAGES8 * S::STAGE;
+  const int G = n_q / n_kv;
+  const int total = num_units * n_kv;
+  const int gw = blockIdx.x * SW + warp, nw = gridDim.x * SW;
+
+  // code rows of D bytes, 16-byte chunks XOR-swizzled so 8 rows of one chunk hit 8 bank groups
+  auto swzb = [](int row, int ch) {
+    const int sel = D == 128 ? (row & 7) : ((row >> 1) & 3);
+    return row * D + ((ch ^ sel) << 4);
+  };
+  auto swzq = [](int row, int ch) { return row * D + ((ch ^ (row & 7)) * 8); };  // bf16 elements
+  struct Geo {
+    int r, kvh, k_begin, k_end, p_begin, npages, nkeys;
+    const int* btrow;
+  };
+  auto geo = [&](int v) {
+    Geo g;
+    const int u = v / n_kv;
+    g.kvh = v - u * n_kv;
+    const int b = units[3 * u];
+    g.r = rows ? rows[b] : b;
+    const int sq = seqs ? seqs[b] : b;
+    g.nkeys = qpos[g.r] + 1;
+    g.k_begin = units[3 * u + 1];
+    g.k_end = min(g.nkeys, g.k_begin + units[3 * u + 2]);
+    g.p_begin = g.k_begin / kPageSize;
+    g.npages = (g.k_end + kPageSize - 1) / kPageSize - g.p_begin;
+    g.btrow = bt + (size_t)sq * max_pages;
+    return g;
+  };
+
+  int lv = gw, lp = 0, lslot = 0;
+  Geo lg;
+  if (lv < total) lg = geo(lv);
+  auto issue = [&]() {
+    if (lv < total) {
+      unsigned char* st = ring + lslot * S::STAGE;
+      const int page = lg.btrow[lg.p_begin + lp];
+      const bool ok = page >= 0 && page < num_pages;
+      const size_t blk = ok ? (size_t)page * n_kv + lg.kvh : 0;
+#pragma unroll
+      for (int c = lane; c < kPageSize * S::CHB; c += 32) {
+        const int row = c / S::CHB, ch = c % S::CHB;
+        cp_async16(smem_u32(st + swzb(row, ch)), kpool + blk * S::CODES + row * D + ch * 16, ok ? 16 : 0);
+        cp_async16(smem_u32(st + S::CODES + swzb(row, ch)), vpool + blk * S::CODES + row * D + ch * 16, ok ? 16 : 0);
+      }
+      if (lane < 8) {  // 16 K scales, then 16 V scales
+        const float* sp = (lane < 4 ? kscale : vscale) + blk * kPageSize + (lane & 3) * 4;
+        cp_async16(smem_u32(st + 2 * S::CODES + lane * 16), sp, ok ? 16 : 0);
+      }
+      if (lp == 0) {
+        const bf16* qsrc = q + (size_t)lg.r * ldq + (size_t)lg.kvh * G * D;
+        bf16* qs = reinterpret_cast<bf16*>(st + 2 * S::CODES + 2 * kPageSize * 4);
+        for (int c = lane; c < G * (D / 8); c += 32) {
+          const int row = c / (D / 8), ch = c % (D / 8);
+          cp_async16(smem_u32(qs + swzq(row, ch)), qsrc + row * D + ch * 8, 16);
+        }
+      }
+      if (++lslot == SSTAGES8) lslot = 0;
+      if (++lp == lg.npages) {
+        lp = 0;
+        lv += nw;
+        if (lv < total) lg = geo(lv);
+      }
+    }
+    cp_async_commit();
+  };
+
+  const int g0 = lane >> 2, qd = lane & 3;
+  uint32_t qf[D / 16][4];
+  float o[D / 8][4];
+  float m0 = -FLT_MAX, l0 = 0.f, sref = 0.f;
+
+#pragma unroll
+  for (int i = 0; i < SSTAGES8 - 1; ++i) issue();
+  int cv = gw, cp = 0, cslot = 0;
+  Geo cg;
+  if (cv < total) cg = geo(cv);
+  while (cv < total) {
+    issue();
+    cp_async_wait<SSTAGES8 - 1>();
+    __syncwarp();
+    const unsigned char* st = ring + cslot * S::STAGE;
+    const float* sk = reinterpret_cast<const float*>(st + 2 * S::CODES);
+    const float* sv = sk + kPageSize;
+    if (cp == 0) {  // Q in f16, dims 16ks + 4qd .. +3 of head g0 (the order the K codes arrive in)
+      const bf16* qs = reinterpret_cast<const bf16*>(st + 2 * S::CODES + 2 * kPageSize * 4);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        uint32_t lo = 0u, hi = 0u;
+        if (g0 < G) {
+          const uint2 w = *reinterpret_cast<const uint2*>(qs + swzq(g0, 2 * ks + (qd >> 1)) + 4 * (qd & 1));
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w.y));
+          lo = pack_f16(a.x, a.y);
+          hi = pack_f16(b.x, b.y);
+        }
+        qf[ks][0] = lo;
+        qf[ks][1] = 0u;
+        qf[ks][2] = hi;
+        qf[ks][3] = 0u;
+      }
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+      m0 = -FLT_MAX;
+      l0 = 0.f;
+      sref = 0.f;
+    }
+
+    // S = Q K^T straight from the codes
+    float sc[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sc[t][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ks += 2) {
+      uint32_t r[4];
+      const int row = (lane & 7) + ((lane >> 4) << 3);
+      const int ch = ks + ((lane >> 3) & 1);
+      ldmatrix_x4(smem_u32(st + swzb(row, ch)), r[0], r[1], r[2], r[3]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // k-steps ks, ks + 1
+        uint32_t b0[2], b1[2];
+        b0[0] = f16x2_from_e4m3x2(r[h] & 0xffffu);
+        b0[1] = f16x2_from_e4m3x2(r[h] >> 16);
+        b1[0] = f16x2_from_e4m3x2(r[2 + h] & 0xffffu);
+        b1[1] = f16x2_from_e4m3x2(r[2 + h] >> 16);
+        mma_f16_16816(sc[0], qf[ks + h], b0);
+        mma_f16_16816(sc[1], qf[ks + h], b1);
+      }
+    }
+    const int pg = cg.btrow[cg.p_begin + cp];
+    const bool page_ok = pg >= 0 && pg < num_pages;
+    const int key0 = (cg.p_begin + cp) * kPageSize;
+    float mx0 = -FLT_MAX, vmax = 0.f;
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int kk = 8 * t + 2 * qd + e;
+        const int key = key0 + kk;
+        const bool valid = page_ok && key >= cg.k_begin && key < cg.k_end;
+        sc[t][e] = valid ? sc[t][e] * sk[kk] * scale_log2 : -INFINITY;
+        mx0 = fmaxf(mx0, sc[t][e]);
+        if (valid) vmax = fmaxf(vmax, sv[kk]);
+      }
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      vmax = fmaxf(vmax, __shfl_xor_sync(0xffffffffu, vmax, off));
+    }
+    // one rescale for both moving references: the softmax max (O and l) and S_ref (O)
+    if (__any_sync(0xffffffffu, mx0 > m0 || vmax > sref)) {
+      const float mn0 = fmaxf(m0, mx0), sn = fmaxf(sref, vmax);
+      const float al0 = exp2f(m0 - mn0);
+      const float fo = al0 * (sn > 0.f ? sref / sn : 1.f);
+      m0 = mn0;
+      l0 *= al0;
+      sref = sn;
+#pragma unroll
+      for (int n = 0; n < D / 8; ++n) {
+        o[n][0] *= fo;
+        o[n][1] *= fo;
+      }
+    }
+    const float isref = sref > 0.f ? 1.f / sref : 0.f;
+    float ps0 = 0.f, pv[2][2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p = exp2f(sc[t][e] - m0);
+        ps0 += p;
+        pv[t][e] = p * (sv[8 * t + 2 * qd + e] * isref);
+      }
+    l0 += ps0;
+    uint32_t pa[4];
+    pa[0] = pack_f16(pv[0][0], pv[0][1]);
+    pa[1] = 0u;
+    pa[2] = pack_f16(pv[1][0], pv[1][1]);
+    pa[3] = 0u;
+    // O += P' V: per 16-dim chunk c, an even-dim and an odd-dim n-tile (O column order:
+    // chunk c holds dims 16c + 4qd + {0, 2} in n-tile 2c and 16c + 4qd + {1, 3} in 2c + 1)
+#pragma unroll
+    for (int c = 0; c < D / 16; c += 2) {
+      uint32_t r[4];
+      ldmatrix_x4_trans(smem_u32(st + S::CODES + swzb(lane & 15, c + (lane >> 4))), r[0], r[1], r[2], r[3]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {  // chunks c, c + 1: keys 0-7 in r[2h], keys 8-15 in r[2h+1]
+        uint32_t be[2], bo[2];
+        be[0] = f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x0020));
+        bo[0] = f16x2_from_e4m3x2(__byte_perm(r[2 * h], 0, 0x0031));
+        be[1] = f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x0020));
+        bo[1] = f16x2_from_e4m3x2(__byte_perm(r[2 * h + 1], 0, 0x0031));
+        mma_f16_16816(o[2 * (c + h)], pa, be);
+        mma_f16_16816(o[2 * (c + h) + 1], pa, bo);
+      }
+    }
+    __syncwarp();
+    if (++cslot == SSTAGES8) cslot = 0;
+
+    if (++cp == cg.npages) {
+      float s0 = l0;
+#pragma unroll
+      for (int off = 1; off <= 2; off <<= 1) s0 += __shfl_xor_sync(0xffffffffu, s0, off);
+      const bool whole = cg.k_begin == 0 && cg.k_end == cg.nkeys;
+      const int u = cv / n_kv;
+      if (g0 < G) {
+        if (whole) {
+          const float f = s0 > 0.f ? sref / s0 : 0.f;
+          bf16* orow = out + (size_t)cg.r * ldo + (size_t)(cg.kvh * G + g0) * D;
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            uint2 w;
+            w.x = pack_bf16(o[2 * c][0] * f, o[2 * c + 1][0] * f);
+            w.y = pack_bf16(o[2 * c][1] * f, o[2 * c + 1][1] * f);
+            *reinterpret_cast<uint2*>(orow + 16 * c + 4 * qd) = w;
+          }
+        } else {
+          float* pp = part + (((size_t)u * n_kv + cg.kvh) * G + g0) * (D + 2);
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {  // (D + 2)-float records: 8-byte alignment only
+            *reinterpret_cast<float2*>(pp + 2 + 16 * c + 4 * qd) = make_float2(o[2 * c][0] * sref, o[2 * c + 1][0] * sref);
+            *reinterpret_cast<float2*>(pp + 4 + 16 * c + 4 * qd) = make_float2(o[2 * c][1] * sref, o[2 * c + 1][1] * sref);
+          }
+          if (qd == 0) *reinterpret_cast<float2*>(pp) = make_float2(m0, s0);
+        }
+      }
+      cp = 0;
+      cv += nw;
+      if (cv < total) cg = geo(cv);
+    }
+  }
+  cp_async_wait<0>();
+}
+
 // Merges the splits of every item that has more than one, per head in split order: the
 // split weights 2^(m_u - max) are computed once into shared memory, then each output
 // element sums its splits' unnormalised O four loads at a time.
@@ -353,7 +624,51 @@ cudaError_t split_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_po
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t split_fp8_d(const bf16* q, int ldq, const uint8_t* k8, const uint8_t* v8, const float* ks,
+                        const float* vs, const int* bt, int max_pages, int num_pages, const int* qpos,
+                        const int* rows, const int* seqs, const SplitPlan& plan, int n_q, int n_kv, bf16* out,
+                        int ldo, int num_sms, cudaStream_t stream) {
+  constexpr int smem = Sp8<D>::SMEM;
+  static_assert(smem <= 227 * 1024, "rings must fit in shared memory");
+  static_assert(Sp8<D>::STAGE % 16 == 0, "ring slots must keep 16-byte alignment");
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(attn_split_fp8_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
+  const int total = plan.num_units * n_kv;
+  const int ctas = std::min((total + SW - 1) / SW, num_sms);
+  attn_split_fp8_kernel<D><<<ctas, SW * 32, smem, stream>>>(q, ldq, k8, v8, ks, vs, bt, max_pages, num_pages, qpos,
+                                                            rows, seqs, plan.units, plan.num_units, n_q, n_kv, out,
+                                                            ldo, plan.part, scale_log2);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !plan.any_split) return e;
+  attn_split_combine<D><<<dim3(plan.num_items, n_kv), CMB_THREADS, 0, stream>>>(rows, plan.ubeg, n_q, n_kv,
+                                                                                plan.part, out, ldo);
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_attention_decode_split_fp8(const bf16* q, int ldq, const uint8_t* k8, const uint8_t* v8,
+                                              const float* k_scale, const float* v_scale, const int* block_table,
+                                              int max_pages, int num_pages, const int* qpos, const int* rows,
+                                              const int* seqs, const SplitPlan& plan, int n_q, int n_kv, int d_head,
+                                              bf16* out, int ldo, int num_sms, cudaStream_t stream) {
+  if (plan.num_units <= 0) return cudaSuccess;
+  if (n_q % n_kv || n_q / n_kv > SMAXG) return cudaErrorNotSupported;
+  if (d_head == 128)
+    return split_fp8_d<128>(q, ldq, k8, v8, k_scale, v_scale, block_table, max_pages, num_pages, qpos, rows, seqs,
+                            plan, n_q, n_kv, out, ldo, num_sms, stream);
+  if (d_head == 64)
+    return split_fp8_d<64>(q, ldq, k8, v8, k_scale, v_scale, block_table, max_pages, num_pages, qpos, rows, seqs,
+                           plan, n_q, n_kv, out, ldo, num_sms, stream);
+  return cudaErrorNotSupported;
+}
 
 int split_keys_for(int nkeys) {
   (void)nkeys;

@@ -7,6 +7,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -48,6 +49,8 @@ struct EpiParams {
   bf16* const* k_pools;      // device array [num_caches] of K pools
   bf16* const* v_pools;      // device array [num_caches] of V pools
   int cache_base;            // EPI_QKV: the layer's cache; EPI_WIDE_KV: first skipped cache
+  bf16* kv_stage;            // non-null (FP8 cache): K (after RoPE) and V rows go here instead,
+  int kv_stage_ld;           //   [M][kv_stage_ld] at their K/V column, for the quantize pass
 };
 
 __host__ __device__ __forceinline__ int pair_half(const EpiParams& p) {
@@ -125,12 +128,19 @@ __device__ __forceinline__ void apply_pair(const EpiParams& p, int m, int n_lo, 
         if (slot < 0) break;
         int c = n_lo - p.q_cols;
         const int kvc = p.n_kv * dh;
+        const int cs = c;
         bool is_k = c < kvc;
         if (!is_k) c -= kvc;
         int head = c / dh, i = c % dh;
         if (is_k) rope_rotate(p, p.positions[m], i, a, b);
-        paged_store_pair(is_k ? p.k_pools[p.cache_base] : p.v_pools[p.cache_base], slot, p.n_kv, head,
-                         dh, i, a, b);
+        if (p.kv_stage) {
+          bf16* o = p.kv_stage + (size_t)m * p.kv_stage_ld + cs;
+          o[0] = __float2bfloat16_rn(a);
+          o[dh >> 1] = __float2bfloat16_rn(b);
+        } else {
+          paged_store_pair(is_k ? p.k_pools[p.cache_base] : p.v_pools[p.cache_base], slot, p.n_kv, head,
+                           dh, i, a, b);
+        }
       }
       break;
     }
@@ -149,6 +159,12 @@ __device__ __forceinline__ void apply_pair(const EpiParams& p, int m, int n_lo, 
       if (!is_k) c -= kvc;
       int head = c / dh, i = c % dh;
       if (is_k) rope_rotate(p, p.positions[m], i, a, b);
+      if (p.kv_stage) {
+        bf16* o = p.kv_stage + (size_t)m * p.kv_stage_ld;
+        o[n_lo] = __float2bfloat16_rn(a);
+        o[n_hi] = __float2bfloat16_rn(b);
+        break;
+      }
       int cache = p.cache_base + grp;
       paged_store_pair(is_k ? p.k_pools[cache] : p.v_pools[cache], slot, p.n_kv, head, dh, i, a, b);
       break;
@@ -249,6 +265,7 @@ __device__ __forceinline__ void apply_chunk32(const EpiParams& p, int m, int n_l
         c = n_lo - grp * 2 * kvc;
         cache = p.cache_base + grp;
       }
+      const int cs = p.kind == EPI_QKV ? n_lo - p.q_cols : n_lo;  // K/V column of the stage
       const bool is_k = c < kvc;
       if (!is_k) c -= kvc;
       const int head = c / dh, i0 = c % dh;
@@ -256,6 +273,12 @@ __device__ __forceinline__ void apply_chunk32(const EpiParams& p, int m, int n_l
         const int pos = p.positions[m];
 #pragma unroll
         for (int i = 0; i < 32; ++i) rope_rotate(p, pos, i0 + i, a[i], b[i]);
+      }
+      if (p.kv_stage) {
+        bf16* o = p.kv_stage + (size_t)m * p.kv_stage_ld + cs;
+        store_bf16x32(o, a);
+        store_bf16x32(o + (dh >> 1), b);
+        break;
       }
       bf16* pool = is_k ? p.k_pools[cache] : p.v_pools[cache];
       bf16* row = pool + ((size_t)(slot >> 4) * p.n_kv + head) * kPageSize * dh + (size_t)(slot & 15) * dh;
@@ -266,6 +289,18 @@ __device__ __forceinline__ void apply_chunk32(const EpiParams& p, int m, int n_l
     default:
       break;
   }
+}
+
+// ---------------------------------------------------------------------------- float8 e4m3
+
+// Two floats to e4m3 codes (round to nearest even, saturating at +-448); lo in bits 0..7.
+__device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+// Two e4m3 codes (bits 0..7 and 8..15) to an f16x2 (exact), the low code in the low half.
+__device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t codes16) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)codes16, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
 // ---------------------------------------------------------------------------- PTX helpers

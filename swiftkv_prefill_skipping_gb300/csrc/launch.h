@@ -56,6 +56,20 @@ cudaError_t launch_plan_decode(const int* seq_lens, int B, const int* tokens, in
                                const int* block_table, int max_pages, int num_pages, int* positions,
                                int* slots, int* status, cudaStream_t stream);
 
+// ---- FP8 KV cache -------------------------------------------------------------------------
+// Quantizes staged K/V rows (stage [M][ld]: per group [K heads | V heads] of d_head bf16
+// values) per (row, group, K/V, head) into uint8 e4m3 pools (device arrays of pool pointers,
+// cache cache_base + group) with float32 scales [num_pages][n_kv][16]; rows with slot < 0
+// are skipped. sk/sv (groups == 1, may be null): bf16 expansion pools written as well.
+cudaError_t launch_kv_quantize(const bf16* stage, int ld, int M, const int* slots, int groups, int n_kv, int d_head,
+                               int cache_base, uint8_t* const* k8, uint8_t* const* v8, float* const* ks,
+                               float* const* vs, bf16* sk, bf16* sv, cudaStream_t stream);
+// Expands the (page, all heads) blocks named by items [2 * num_items] = (sequence, page index
+// in its block-table row) of one cache into bf16 pools sk/sv of the same layout.
+cudaError_t launch_kv_dequant_pages(const int* items, int num_items, const int* block_table, int max_pages,
+                                    int num_pages, int n_kv, int d_head, const uint8_t* k8, const uint8_t* v8,
+                                    const float* ks, const float* vs, bf16* sk, bf16* sv, cudaStream_t stream);
+
 // ---- row kernels -------------------------------------------------------------------------
 // x[t] = embed[tok[t]] (fp32); u[t] = bf16(rmsnorm(x[t]) * gamma)
 cudaError_t launch_embed_rmsnorm(const int* tokens, int T, const bf16* embed, int vocab, int d,
@@ -109,6 +123,12 @@ constexpr int kSplitKeys = 256;
 int split_keys_for(int nkeys);
 void split_plan_host(const int* nkeys, int items, std::vector<int>* units, std::vector<int>* ubeg);
 size_t split_part_floats(int num_units, int n_q, int d_head);
+// The same over an FP8 cache: uint8 e4m3 pools and float32 scales [num_pages][n_kv][16].
+cudaError_t launch_attention_decode_split_fp8(const bf16* q, int ldq, const uint8_t* k8, const uint8_t* v8,
+                                              const float* k_scale, const float* v_scale, const int* block_table,
+                                              int max_pages, int num_pages, const int* qpos, const int* rows,
+                                              const int* seqs, const SplitPlan& plan, int n_q, int n_kv, int d_head,
+                                              bf16* out, int ldo, int num_sms, cudaStream_t stream);
 cudaError_t launch_attention_decode_split(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
                                           const int* block_table, int max_pages, int num_pages, const int* qpos,
                                           const int* rows, const int* seqs, const SplitPlan& plan, int n_q,

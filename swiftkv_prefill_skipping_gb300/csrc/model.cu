@@ -58,6 +58,9 @@ struct Workspace {
   int *cu, *tiles, *pools, *positions, *slots, *last_idx, *last_pos, *tokens, *ctx, *srow, *sseq, *dint;
   float *x, *xt, *part, *logits, *dpart;
   bf16 *u, *q, *attn, *h, *ut, *qt, *at, *ht;
+  bf16 *kv_stage;         // FP8 cache: staged K/V rows before quantization
+  bf16 *exp_k, *exp_v;    // FP8 cache: bf16 expansion of one cache for the prompt-tile attention
+  int* deq_items;         // FP8 cache: (sequence, page) pairs of cached prefixes to expand
 };
 
 constexpr int kShortChunk = 4;  // chunks up to this many rows take the single-row attention kernel
@@ -160,13 +163,14 @@ int cache_of_layer(const swiftkv_model* m, int j) { return j < m->l ? j : m->l +
 // dec_ints / dec_floats: key-split plans of the single-row attention (units + ubeg) and
 // their partial results.
 int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t part_bytes, Workspace* w,
-                     size_t dec_ints = 0, size_t dec_floats = 0) {
+                     size_t dec_ints = 0, size_t dec_floats = 0, size_t stage_elems = 0, size_t exp_elems = 0,
+                     size_t deq_ints = 0) {
   const auto& c = m->cfg;
   const size_t A = 256;
   size_t sizes[] = {
       (size_t)(P + 1) * 4,           // cu / seq lens
       (size_t)std::max(ntiles, 1) * 4,  // tiles
-      (size_t)4 * C * 4,             // pool pointers (2C x 8 bytes)
+      (size_t)8 * C * 4,             // pool pointers: K, V, K scale, V scale (4C x 8 bytes)
       (size_t)T * 4, (size_t)T * 4,  // positions, slots
       (size_t)P * 4, (size_t)P * 4,  // last idx / pos
       (size_t)T * 4,                 // tokens (host-buffer entry)
@@ -186,6 +190,9 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
       (size_t)T * 4, (size_t)T * 4,  // rows of short chunks and their sequences
       dec_ints * 4,                  // key-split plans
       dec_floats * 4,                // key-split partials
+      stage_elems * 2,               // staged K/V rows (FP8 cache)
+      exp_elems * 2, exp_elems * 2,  // bf16 expansion of one cache (FP8 cache)
+      deq_ints * 4,                  // prefix pages to expand
   };
   const int n = sizeof(sizes) / sizeof(sizes[0]);
   size_t off[32], total = 0;
@@ -233,6 +240,10 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
   w->sseq = (int*)(b + off[22]);
   w->dint = (int*)(b + off[23]);
   w->dpart = (float*)(b + off[24]);
+  w->kv_stage = (bf16*)(b + off[25]);
+  w->exp_k = (bf16*)(b + off[26]);
+  w->exp_v = (bf16*)(b + off[27]);
+  w->deq_items = (int*)(b + off[28]);
   return SWIFTKV_OK;
 }
 
@@ -262,6 +273,11 @@ struct Ctx {
   int nshort = 0;            // rows of short chunks, attended one row at a time (w.srow / w.sseq)
   SplitPlan sp_short{};      // key-split plan of those rows
   SplitPlan sp_rows{};       // key-split plan of the single-row attention (tail / decode rows)
+  bool fp8 = false;          // the caches hold e4m3 codes + per-token scales
+  float* const* ks_dev = nullptr;  // device arrays of scale pools
+  float* const* vs_dev = nullptr;
+  bool expand = false;       // FP8: prompt tiles read a bf16 expansion of the layer's cache
+  int n_deq = 0;             // FP8: prefix pages to expand per full layer (w.deq_items)
 };
 
 // Host side of a key-split plan: units then ubeg in one vector (one upload).
@@ -375,6 +391,12 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   cudaError_t e;
   // single-row attention: key-split kernel (default), else / if unsupported the one-CTA-per-row kernel
   auto rows_attn = [&](const int* pos, int items, const int* rows, const int* seqs, const SplitPlan& sp) {
+    if (x.fp8)  // no fallback: only the key-split kernel reads e4m3 pages
+      return launch_attention_decode_split_fp8(
+          qb, m->Nq, static_cast<const uint8_t*>(x.kv->k_pool[cidx]), static_cast<const uint8_t*>(x.kv->v_pool[cidx]),
+          static_cast<const float*>(x.kv->k_scale[cidx]), static_cast<const float*>(x.kv->v_scale[cidx]),
+          x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages, pos, rows, seqs, sp, c.n_q, c.n_kv, c.d_head,
+          ab, m->Nq, m->num_sms, x.s);
     cudaError_t r = cudaErrorNotSupported;
     if (m->attn_impl == 0 && sp.num_units > 0)
       r = launch_attention_decode_split(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
@@ -385,17 +407,20 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
                                   pos, items, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s, rows, seqs);
     return r;
   };
-  auto launches = [&](const SplitPlan& sp) { return m->attn_impl == 0 ? 1 + (int)sp.any_split : 1; };
+  auto launches = [&](const SplitPlan& sp) { return m->attn_impl == 0 || x.fp8 ? 1 + (int)sp.any_split : 1; };
+  // prompt tiles read the bf16 expansion of the layer's cache when the cache is FP8
+  const bf16* tkp = x.fp8 ? x.w.exp_k : kp;
+  const bf16* tvp = x.fp8 ? x.w.exp_v : vp;
   {
   Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode",
           prefill ? (ntiles > 0) + (x.nshort > 0 ? launches(x.sp_short) : 0) : launches(x.sp_rows), attn_flops,
           0.0);
   if (prefill && x.tc_attn)
-    e = launch_attention_prefill_tc(qb, m->Nq, M, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq,
+    e = launch_attention_prefill_tc(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
                                     m->Nq, m->status, x.s);
   else if (prefill)
-    e = launch_attention_prefill(qb, m->Nq, kp, vp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
+    e = launch_attention_prefill(qb, m->Nq, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
                                  x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
   else
     e = rows_attn(qpos, M, nullptr, nullptr, x.sp_rows);
@@ -418,6 +443,18 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   return SWIFTKV_OK;
 }
 
+// FP8 cache: staged K/V rows of `groups` consecutive caches from cache_base -> e4m3 codes
+// and scales; with `expand`, the bf16 expansion pools get the dequantized rows too.
+int quantize(Ctx& x, int M, const int* slots, int groups, int cache_base, int ld, bool expand) {
+  swiftkv_model* m = x.m;
+  Prof pr(m, x.s, "kv_quantize", 1, 0.0, (double)M * ld * (2 + 1) + (double)M * groups * 2 * m->cfg.n_kv * 4);
+  CK(launch_kv_quantize(x.w.kv_stage, ld, M, slots, groups, m->cfg.n_kv, m->cfg.d_head, cache_base,
+                        reinterpret_cast<uint8_t* const*>(x.k_dev), reinterpret_cast<uint8_t* const*>(x.v_dev),
+                        const_cast<float* const*>(x.ks_dev), const_cast<float* const*>(x.vs_dev),
+                        expand ? x.w.exp_k : nullptr, expand ? x.w.exp_v : nullptr, x.s));
+  return SWIFTKV_OK;
+}
+
 // Q/K/V (full layer: cache_base = j) or Q only (skipped layer) projection with RoPE.
 int qkv(Ctx& x, int j, int M, const bf16* ub, bf16* qb, const int* pos, const int* slots, const char* gname) {
   swiftkv_model* m = x.m;
@@ -431,7 +468,13 @@ int qkv(Ctx& x, int j, int M, const bf16* ub, bf16* qb, const int* pos, const in
   e.positions = pos;
   e.slots = slots;
   e.cache_base = j;
-  return gemm(x, gname, ub, m->cfg.d, L.wqkv, m->cfg.d, e, 2.0 * M * e.N * m->cfg.d);
+  if (full && x.fp8) {
+    e.kv_stage = x.w.kv_stage;
+    e.kv_stage_ld = 2 * m->Nkv;
+  }
+  RET(gemm(x, gname, ub, m->cfg.d, L.wqkv, m->cfg.d, e, 2.0 * M * e.N * m->cfg.d));
+  if (full && x.fp8) RET(quantize(x, M, slots, 1, j, 2 * m->Nkv, x.expand));
+  return SWIFTKV_OK;
 }
 
 // Boundary: one row-RMS of x_l (gains folded into W_KV) and the wide KV GEMM into the
@@ -444,7 +487,13 @@ int wide_kv(Ctx& x, int M, const float* xres, bf16* ub, const int* pos, const in
   e.positions = pos;
   e.slots = slots;
   e.cache_base = m->l;
-  return gemm(x, "gemm_wide_kv", ub, m->cfg.d, m->w_wide, m->cfg.d, e, 2.0 * M * m->Nwide * m->cfg.d);
+  if (x.fp8) {
+    e.kv_stage = x.w.kv_stage;
+    e.kv_stage_ld = m->Nwide;
+  }
+  RET(gemm(x, "gemm_wide_kv", ub, m->cfg.d, m->w_wide, m->cfg.d, e, 2.0 * M * m->Nwide * m->cfg.d));
+  if (x.fp8) RET(quantize(x, M, slots, m->G, m->l, m->Nwide, false));
+  return SWIFTKV_OK;
 }
 
 int check_ready(const swiftkv_model* m) {
@@ -462,19 +511,36 @@ int check_kv(const swiftkv_model* m, const swiftkv_kv_pages* kv) {
   if (kv->num_pages < 1 || kv->max_pages_per_seq < 1) return fail(SWIFTKV_EINVAL, "empty page pool");
   for (int c = 0; c < m->C; ++c)
     if (!kv->k_pool[c] || !kv->v_pool[c]) return fail(SWIFTKV_EINVAL, "null pool pointer for cache %d", c);
+  if (kv->kv_dtype != 0 && kv->kv_dtype != 1) return fail(SWIFTKV_EINVAL, "kv_dtype %d", kv->kv_dtype);
+  if (kv->kv_dtype == 1) {
+    if (!kv->k_scale || !kv->v_scale) return fail(SWIFTKV_EINVAL, "fp8 cache without scale pools");
+    for (int c = 0; c < m->C; ++c)
+      if (!kv->k_scale[c] || !kv->v_scale[c]) return fail(SWIFTKV_EINVAL, "null scale pool for cache %d", c);
+    if (m->cfg.n_q / m->cfg.n_kv > 8)
+      return fail(SWIFTKV_EUNSUPPORTED, "fp8 cache needs at most 8 query heads per KV head");
+  }
   return SWIFTKV_OK;
 }
 
 int upload_pools(Ctx& x) {
   const int C = x.m->C;
-  std::vector<void*> ptrs(2 * C);
+  const int n = x.fp8 ? 4 * C : 2 * C;
+  std::vector<void*> ptrs(n);
   for (int c = 0; c < C; ++c) {
     ptrs[c] = x.kv->k_pool[c];
     ptrs[C + c] = x.kv->v_pool[c];
+    if (x.fp8) {
+      ptrs[2 * C + c] = x.kv->k_scale[c];
+      ptrs[3 * C + c] = x.kv->v_scale[c];
+    }
   }
-  CK(upload_ints(x.w.pools, reinterpret_cast<const int*>(ptrs.data()), 4 * C, x.s));
+  CK(upload_ints(x.w.pools, reinterpret_cast<const int*>(ptrs.data()), 2 * n, x.s));
   x.k_dev = reinterpret_cast<bf16* const*>(x.w.pools);
   x.v_dev = reinterpret_cast<bf16* const*>(x.w.pools) + C;
+  if (x.fp8) {
+    x.ks_dev = reinterpret_cast<float* const*>(x.w.pools) + 2 * C;
+    x.vs_dev = reinterpret_cast<float* const*>(x.w.pools) + 3 * C;
+  }
   return SWIFTKV_OK;
 }
 
@@ -828,6 +894,23 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   x.s = s;
   x.kv = kv;
   x.tc_attn = tc_attn;
+  // FP8 cache: prompt tiles attend over a bf16 expansion of the layer's cache (chunk rows
+  // written by the quantize pass, cached prefixes expanded page by page before each layer)
+  x.fp8 = kv->kv_dtype == 1;
+  x.expand = x.fp8 && !tiles.empty();
+  std::vector<int> deq;
+  if (x.expand)
+    for (int i = 0; i < P; ++i) {
+      const int n = cu[i + 1] - cu[i], c0 = ctx ? ctx[i] : 0;
+      if (n <= short_max) continue;
+      for (int pidx = 0; pidx < (c0 + kPageSize - 1) / kPageSize; ++pidx) {
+        deq.push_back(i);
+        deq.push_back(pidx);
+      }
+    }
+  x.n_deq = (int)deq.size() / 2;
+  const size_t stage_elems = x.fp8 ? (size_t)T * std::max(2 * m->Nkv, m->Nwide) : 0;
+  const size_t exp_elems = x.expand ? (size_t)kv->num_pages * m->cfg.n_kv * kPageSize * m->cfg.d_head : 0;
   size_t part = std::max(skinny_part_bytes(m, P), skinny_part_bytes(m, T));
   std::vector<int> nk_short, nk_tail(P);
   for (size_t i = 0; i < srow.size(); ++i) {
@@ -838,7 +921,8 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   const HostSplit hs_short = make_split(nk_short), hs_tail = make_split(nk_tail);
   RET(ensure_workspace(m, T, P, m->C, (int)tiles.size(), part, &x.w, hs_short.ints() + hs_tail.ints(),
                        std::max(split_part_floats(hs_short.num_units(), m->cfg.n_q, m->cfg.d_head),
-                                split_part_floats(hs_tail.num_units(), m->cfg.n_q, m->cfg.d_head))));
+                                split_part_floats(hs_tail.num_units(), m->cfg.n_q, m->cfg.d_head)),
+                       stage_elems, exp_elems, deq.size()));
   const int* tok = tokens;
   if (host_io) {
     CK(cudaMemcpyAsync(x.w.tokens, tokens, (size_t)T * 4, cudaMemcpyHostToDevice, s));
@@ -854,8 +938,10 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   Prof pr(m, s, "plan", 1 + (P + 1 + kBlobInts - 1) / kBlobInts + ((int)tiles.size() + kBlobInts - 1) / kBlobInts +
           (4 * m->C + kBlobInts - 1) / kBlobInts + (ctx ? (P + kBlobInts - 1) / kBlobInts : 0) +
           2 * (((int)srow.size() + kBlobInts - 1) / kBlobInts) +
-          ((int)hs_short.ints() + kBlobInts - 1) / kBlobInts + ((int)hs_tail.ints() + kBlobInts - 1) / kBlobInts,
+          ((int)hs_short.ints() + kBlobInts - 1) / kBlobInts + ((int)hs_tail.ints() + kBlobInts - 1) / kBlobInts +
+          ((int)deq.size() + kBlobInts - 1) / kBlobInts,
           0.0, 0.0);
+  if (!deq.empty()) CK(upload_ints(x.w.deq_items, deq.data(), (int)deq.size(), s));
   CK(upload_ints(x.w.cu, cu, P + 1, s));
   CK(upload_ints(x.w.tiles, tiles.data(), (int)tiles.size(), s));
   if (ctx) {
@@ -881,6 +967,14 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   // layers 1..l in full for every prompt token
   for (int j = 0; j < m->l; ++j) {
     if (j > 0) RET(norm(x, x.w.x, nullptr, T, m->layers[j].g_attn, x.w.u, nullptr));
+    if (x.n_deq > 0) {
+      Prof pr(m, s, "kv_dequant", 1, 0.0,
+              (double)x.n_deq * 2 * c.n_kv * kPageSize * (c.d_head * 3.0 + 4.0));
+      CK(launch_kv_dequant_pages(x.w.deq_items, x.n_deq, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
+                                 c.n_kv, c.d_head, static_cast<const uint8_t*>(kv->k_pool[j]),
+                                 static_cast<const uint8_t*>(kv->v_pool[j]), static_cast<const float*>(kv->k_scale[j]),
+                                 static_cast<const float*>(kv->v_scale[j]), x.w.exp_k, x.w.exp_v, s));
+    }
     RET(qkv(x, j, T, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_layers"));
     RET(layer_rest(x, j, T, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, true, nullptr, (int)tiles.size(),
                    "gemm_layers", attn_flops));
@@ -944,8 +1038,10 @@ int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   std::vector<int> nk(B);
   for (int b = 0; b < B; ++b) nk[b] = seq_lens[b] + 1;
   const HostSplit hs = make_split(nk);
+  x.fp8 = kv->kv_dtype == 1;
   RET(ensure_workspace(m, B, B, m->C, 1, skinny_part_bytes(m, B), &x.w, hs.ints(),
-                       split_part_floats(hs.num_units(), m->cfg.n_q, m->cfg.d_head)));
+                       split_part_floats(hs.num_units(), m->cfg.n_q, m->cfg.d_head),
+                       x.fp8 ? (size_t)B * std::max(2 * m->Nkv, m->Nwide) : 0));
   CK(upload_ints(x.w.cu, seq_lens, B, s));
   RET(upload_pools(x));
   RET(upload_split(x, hs, x.w.dint, &x.sp_rows));

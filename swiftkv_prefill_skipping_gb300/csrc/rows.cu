@@ -234,6 +234,133 @@ cudaError_t upload_ints(int* dst, const int* src, int n, cudaStream_t stream) {
   return cudaSuccess;
 }
 
+namespace {
+
+// ---------------------------------------------------------------------------- FP8 KV cache
+
+// One warp per staged (row m, group, K/V, head) vector of d_head bf16 values: per-vector
+// scale amax / 448, e4m3 codes of value / scale (float32 division, round to nearest even)
+// into the paged uint8 pool at the row's slot, the scale into the scale pool; with `sk`/`sv`
+// (groups == 1) the dequantized values also go, as bf16, into bf16 expansion pools of the
+// same layout for the prompt-tile attention.
+template <int E>
+__global__ void kv_quantize_kernel(const bf16* __restrict__ stage, int ld, int M, const int* __restrict__ slots,
+                                   int groups, int n_kv, int cache_base, uint8_t* const* k8, uint8_t* const* v8,
+                                   float* const* ks, float* const* vs, bf16* sk, bf16* sv) {
+  constexpr int DH = E * 32;
+  const int lane = threadIdx.x & 31;
+  const long long vid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int per_row = groups * 2 * n_kv;
+  if (vid >= (long long)M * per_row) return;
+  const int m = (int)(vid / per_row);
+  int r = (int)(vid - (long long)m * per_row);
+  const int grp = r / (2 * n_kv);
+  r -= grp * 2 * n_kv;
+  const int kvsel = r / n_kv, head = r - kvsel * n_kv;
+  const int slot = slots[m];
+  if (slot < 0) return;
+  const int kvc = n_kv * DH;
+  const bf16* src = stage + (size_t)m * ld + (size_t)grp * 2 * kvc + kvsel * kvc + head * DH + lane * E;
+  float v[E];
+#pragma unroll
+  for (int i = 0; i < E; i += 2) {
+    float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(src + i));
+    v[i] = f.x;
+    v[i + 1] = f.y;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const float scale = amax / 448.f;
+  uint16_t c2[E / 2];
+#pragma unroll
+  for (int i = 0; i < E; i += 2)
+    c2[i / 2] = scale > 0.f ? e4m3x2_from_f32(v[i] / scale, v[i + 1] / scale) : (uint16_t)0;
+  const int cache = cache_base + grp;
+  const size_t rowoff = ((size_t)(slot >> 4) * n_kv + head) * kPageSize + (slot & 15);
+  uint8_t* dst = (kvsel ? v8[cache] : k8[cache]) + rowoff * DH + lane * E;
+  if constexpr (E == 4) {
+    *reinterpret_cast<uint32_t*>(dst) = (uint32_t)c2[0] | ((uint32_t)c2[1] << 16);
+  } else {
+    *reinterpret_cast<uint16_t*>(dst) = c2[0];
+  }
+  if (lane == 0) (kvsel ? vs[cache] : ks[cache])[rowoff] = scale;
+  bf16* ex = kvsel ? sv : sk;
+  if (ex) {
+#pragma unroll
+    for (int i = 0; i < E; i += 2) {
+      const uint32_t h = f16x2_from_e4m3x2(c2[i / 2]);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+      *reinterpret_cast<__nv_bfloat162*>(ex + rowoff * DH + lane * E + i) =
+          __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    }
+  }
+}
+
+// Expands whole (page, all heads) blocks of one cache's uint8 pools into bf16 pools of the
+// same layout: item i = (sequence, page index) pairs; 16 codes per thread-step.
+__global__ void kv_dequant_pages_kernel(const int* __restrict__ items, const int* __restrict__ bt, int max_pages,
+                                        int num_pages, int n_kv, int dh, const uint8_t* __restrict__ k8,
+                                        const uint8_t* __restrict__ v8, const float* __restrict__ ks,
+                                        const float* __restrict__ vs, bf16* sk, bf16* sv) {
+  const int s = items[2 * blockIdx.x], pidx = items[2 * blockIdx.x + 1];
+  const int page = bt[(size_t)s * max_pages + pidx];
+  if (page < 0 || page >= num_pages) return;
+  const int per_page = n_kv * kPageSize * dh;  // codes of one page, all heads
+  const size_t base = (size_t)page * per_page;
+  for (int c = threadIdx.x; c < 2 * per_page / 16; c += blockDim.x) {
+    const int kvsel = c >= per_page / 16;
+    const int e = (c - kvsel * (per_page / 16)) * 16;  // element within the page
+    const float scale = (kvsel ? vs : ks)[(size_t)page * n_kv * kPageSize + e / dh];
+    const uint4 raw = *reinterpret_cast<const uint4*>((kvsel ? v8 : k8) + base + e);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t h = f16x2_from_e4m3x2((w[i] >> (16 * hh)) & 0xffffu);
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+        o[2 * i + hh] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+    }
+    bf16* dst = (kvsel ? sv : sk) + base + e;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4*>(dst + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_quantize(const bf16* stage, int ld, int M, const int* slots, int groups, int n_kv, int d_head,
+                               int cache_base, uint8_t* const* k8, uint8_t* const* v8, float* const* ks,
+                               float* const* vs, bf16* sk, bf16* sv, cudaStream_t stream) {
+  const long long vecs = (long long)M * groups * 2 * n_kv;
+  if (vecs <= 0) return cudaSuccess;
+  const int blocks = (int)((vecs * 32 + 255) / 256);
+  if (d_head == 128)
+    kv_quantize_kernel<4><<<blocks, 256, 0, stream>>>(stage, ld, M, slots, groups, n_kv, cache_base, k8, v8, ks, vs,
+                                                      sk, sv);
+  else if (d_head == 64)
+    kv_quantize_kernel<2><<<blocks, 256, 0, stream>>>(stage, ld, M, slots, groups, n_kv, cache_base, k8, v8, ks, vs,
+                                                      sk, sv);
+  else
+    return cudaErrorNotSupported;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_dequant_pages(const int* items, int num_items, const int* block_table, int max_pages,
+                                    int num_pages, int n_kv, int d_head, const uint8_t* k8, const uint8_t* v8,
+                                    const float* ks, const float* vs, bf16* sk, bf16* sv, cudaStream_t stream) {
+  if (num_items <= 0) return cudaSuccess;
+  kv_dequant_pages_kernel<<<num_items, 256, 0, stream>>>(items, block_table, max_pages, num_pages, n_kv, d_head, k8,
+                                                          v8, ks, vs, sk, sv);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_plan_prefill(const int* cu, const int* ctx, int P, int T, const int* tokens, int vocab,
                                 const int* block_table, int max_pages, int num_pages, int* positions,
                                 int* slots, int* last_idx, int* last_pos, int* status,

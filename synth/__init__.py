@@ -153,6 +153,7 @@ class Workload:
     mix_decode: int = 0
     mix_decode_ctx: tuple = (0, 0)
     mix_chunks: tuple = ()
+    kv_dtype: str = "bf16"  # "fp8": per-token float8 e4m3 KV cache
 
     @property
     def mixed(self) -> bool:
@@ -177,6 +178,15 @@ WORKLOADS = {
         Workload("llama70b_l40", LLAMA70B, l=40, g=1, num_prompts=8, len_lo=500, len_hi=1000),
         Workload("qwen14b_l24_g4", QWEN14B, l=24, g=4, num_prompts=24, len_lo=1000, len_hi=1000,
                  decode_steps=100),
+        # 50 % SwiftKV + 4-way AcrossKV + per-token FP8 KV cache (the pages' Table B.1 / Table 3
+        # configuration), bf16 and fp8 caches
+        Workload("llama8b_l16_g4", LLAMA8B, l=16, g=4, num_prompts=16, len_lo=500, len_hi=1000),
+        Workload("llama8b_l16_g4_fp8", LLAMA8B, l=16, g=4, num_prompts=16, len_lo=500, len_hi=1000,
+                 kv_dtype="fp8"),
+        Workload("qwen14b_l24_g4_fp8", QWEN14B, l=24, g=4, num_prompts=24, len_lo=1000, len_hi=1000,
+                 decode_steps=100, kv_dtype="fp8"),
+        Workload("llama8b_l16_mixed_fp8", LLAMA8B, l=16, g=1, num_prompts=0, len_lo=0, len_hi=0, kv_dtype="fp8",
+                 **_MIX_8K),
         Workload("llama8b_l16_mixed", LLAMA8B, l=16, g=1, num_prompts=0, len_lo=0, len_hi=0, **_MIX_8K),
         # the same serving step through the ordinary model (l = L)
         Workload("llama8b_full_mixed", LLAMA8B, l=32, g=1, num_prompts=0, len_lo=0, len_hi=0, **_MIX_8K),
