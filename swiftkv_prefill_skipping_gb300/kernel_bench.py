@@ -2,13 +2,17 @@
 
   python -m swiftkv_prefill_skipping_gb300.kernel_bench gemm --impl 0 --M 11703 --N 6144 --K 4096
   python -m swiftkv_prefill_skipping_gb300.kernel_bench prefill --layers 2 --l 1 --prompts 16
+  python -m swiftkv_prefill_skipping_gb300.kernel_bench decode --batch 24 --ctx 1000 --kv fp8
 
 `gemm` runs the C-ABI GEMM self-test entry (impl 0 tcgen05, 1 mma.sync tiles; impl 2 is
 the skinny split-K kernel through swiftkv_gemm_skinny_noalloc, so no allocation is timed)
 on seeded bf16 operands and reports TFLOP/s and GB/s of operand traffic. `prefill` runs a SwiftKV prefill of a
 reduced-depth model with the Llama-3.1-8B layer shape (same per-layer kernels as the
 full model, a few GB on the device) and prints the per-kernel-class breakdown; it is
-the small case for profiling the attention and norm kernels.
+the small case for profiling the attention and norm kernels. `decode` prefills `batch`
+sequences of `ctx` tokens through a reduced-depth model with the Qwen2.5-14B layer shape
+(40 query heads, 8 KV heads, d_head 128) and times greedy decode steps from its bf16 or
+FP8 cache: the small case for the single-row attention and the skinny GEMMs.
 """
 from __future__ import annotations
 
@@ -90,6 +94,41 @@ def prefill(args):
     assert m.status() == 0
 
 
+def decode(args):
+    import dataclasses
+
+    import torch
+
+    import synth
+    from swiftkv_prefill_skipping_gb300 import api, binding
+    shape = dataclasses.replace(synth.QWEN14B, L=args.layers, name=f"qwen2.5-14b-width-{args.layers}layers")
+    batch = synth.prompt_batch(shape.vocab, args.batch, args.ctx, args.ctx, reserve_tokens=args.warmup + args.iters)
+    m = api.load_synthetic(shape, args.l, args.g)
+    kv = api.KVCache(m, batch.num_pages, batch.block_table, dtype=args.kv)
+    lg = api.prefill(m, torch.as_tensor(batch.tokens, device="cuda"), batch.cu_seqlens, kv)
+    nxt = torch.argmax(lg, dim=-1).to(torch.int32)
+    lens = [int(x) for x in batch.lens]
+    for _ in range(args.warmup):
+        _, nxt = api.decode_step(m, nxt, lens, kv)
+        lens = [x + 1 for x in lens]
+    torch.cuda.synchronize()
+    binding.check(binding.lib().swiftkv_profile_begin(m.handle))
+    for _ in range(args.iters):
+        _, nxt = api.decode_step(m, nxt, lens, kv)
+        lens = [x + 1 for x in lens]
+    torch.cuda.synchronize()
+    ents = (binding.ProfileEntry * 64)()
+    n = binding.check(binding.lib().swiftkv_profile_end(m.handle, ents, 64))
+    res = {}
+    for i in range(n):
+        e = ents[i]
+        res[e.name.decode()] = {"ms_per_step": e.ms / args.iters, "calls": e.calls // args.iters,
+                                "gbs": e.bytes / (e.ms / 1e3) / 1e9 if e.bytes else None}
+    print(json.dumps({"kernel": "decode", "batch": args.batch, "ctx": args.ctx, "kv": args.kv,
+                      "layers": args.layers, "classes": res}))
+    assert m.status() == 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="cmd", required=True)
@@ -109,8 +148,17 @@ def main():
     p.add_argument("--len-hi", type=int, default=1000)
     p.add_argument("--iters", type=int, default=5)
     p.add_argument("--warmup", type=int, default=2)
+    d = sub.add_parser("decode")
+    d.add_argument("--layers", type=int, default=2)
+    d.add_argument("--l", type=int, default=1)
+    d.add_argument("--g", type=int, default=1)
+    d.add_argument("--batch", type=int, default=24)
+    d.add_argument("--ctx", type=int, default=1000)
+    d.add_argument("--kv", choices=("bf16", "fp8"), default="bf16")
+    d.add_argument("--iters", type=int, default=3)
+    d.add_argument("--warmup", type=int, default=2)
     args = ap.parse_args()
-    {"gemm": gemm, "prefill": prefill}[args.cmd](args)
+    {"gemm": gemm, "prefill": prefill, "decode": decode}[args.cmd](args)
 
 
 if __name__ == "__main__":
