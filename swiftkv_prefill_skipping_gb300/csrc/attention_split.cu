@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(SW * 32, 1) attn_split_kernel(
   using S = Sp<D>;
   constexpr int CH = D / 8;  // 16-byte chunks per row
   extern __shared__ __align__(128) unsigned char smem[];
+  griddep_launch_dependents();  // a programmatic dependent may start as these blocks leave
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bf16* ring = reinterpret_cast<bf16*>(smem) + (size_t)warp * SSTAGES * S::STAGE;
   const int G = n_q / n_kv;
@@ -292,6 +293,7 @@ __global__ void __launch_bounds__(SW * 32, 1) attn_split_fp8_kernel(
     float* __restrict__ part, float scale_log2) {
   using S = Sp8<D>;
   extern __shared__ __align__(128) unsigned char smem[];
+  griddep_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* ring = smem + (size_t)warp * SSTAGES8 * S::STAGE;
   const int G = n_q / n_kv;
@@ -545,6 +547,7 @@ __global__ void __launch_bounds__(CMB_THREADS) attn_split_combine(const int* __r
                                                                   bf16* __restrict__ out, int ldo) {
   __shared__ float s_w[CMB_MAX_W];
   __shared__ float s_mx[SMAXG], s_den[SMAXG];
+  griddep_launch_dependents();
   const int b = blockIdx.x, kvh = blockIdx.y;
   const int u0 = ubeg[b], ns = ubeg[b + 1] - u0;
   if (ns <= 1) return;  // written directly by its only unit

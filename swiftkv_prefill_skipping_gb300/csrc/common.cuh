@@ -303,6 +303,18 @@ __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t codes16) {
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// ---------------------------------------------------------------------------- programmatic launch
+
+// Lets the next kernel on the stream, if it was launched as a programmatic dependent, start
+// (its blocks are then scheduled as this kernel's blocks leave; it must griddep_wait()
+// before reading anything this kernel writes). Harmless for ordinary successors.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the kernels this one depends on have completed and their writes are visible;
+// returns at once for a kernel launched without a programmatic dependency.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------- PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(128) gemv_kernel(const bf16* __restrict__ A, i
                                                    const bf16* __restrict__ B, int K, EpiParams ep) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int WROWS = 32, AROWS = MB * 16;
+  griddep_launch_dependents();  // a programmatic dependent may start as these blocks leave
   constexpr int STAGE = (WROWS + AROWS) * GV_LD;  // bf16 elements per stage per warp
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int M = ep.M;

@@ -87,24 +87,50 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   }
   __syncthreads();
 
+  // Launched as a programmatic dependent of the previous kernel on the stream: the first
+  // stages' weight boxes (which no earlier kernel writes) are requested before waiting for
+  // that kernel; everything that reads its output (A, and the epilogue's residual rows)
+  // comes after griddepcontrol.wait.
+  griddep_launch_dependents();
   if (warp == GT_CONSUMERS) {
     // producer
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      auto load_w = [&](int st, int kt, int col_lo) {
+        const uint32_t sw = ring + st * G::STAGE;
+#pragma unroll
+        for (int q = 0; q < GT_KSUB; ++q) {
+          const int x = (kt * GT_KSUB + q) * GT_BK;
+          tma_load_2d(sw + q * G::WBOX, &tmW, x, col_lo, full(st));
+          tma_load_2d(sw + (GT_KSUB + q) * G::WBOX, &tmW, x, col_lo + half, full(st));
+        }
+      };
+      auto load_a = [&](int st, int kt) {
+        const uint32_t sw = ring + st * G::STAGE;
+#pragma unroll
+        for (int q = 0; q < GT_KSUB; ++q)
+          tma_load_2d(sw + G::W_BYTES + q * G::ABOX, &tmA, (kt * GT_KSUB + q) * GT_BK, 0, full(st));
+      };
+      // prologue: weights of the first tile's first stages (the ring starts empty)
+      const int pre = blockIdx.x < tiles ? min(ksteps, G::STAGES) : 0;
+      for (int kt = 0; kt < pre; ++kt) {
+        mbar_expect_tx(full(kt), G::STAGE);
+        ctl->pending[kt] = 0;
+        load_w(kt, kt, col_of(blockIdx.x));
+      }
+      griddep_wait();
+      for (int kt = 0; kt < pre; ++kt) load_a(kt, kt);
+      int issued = 0;
       for (int tile = blockIdx.x; tile < tiles && !*abort_flag; tile += gridDim.x) {
         const int col_lo = col_of(tile);
-        for (int kt = 0; kt < ksteps; ++kt) {
-          if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
-          mbar_expect_tx(full(stage), G::STAGE);
-          ctl->pending[stage] = (int)phase;
-          const uint32_t sw = ring + stage * G::STAGE;
-#pragma unroll
-          for (int q = 0; q < GT_KSUB; ++q) {
-            const int x = (kt * GT_KSUB + q) * GT_BK;
-            tma_load_2d(sw + q * G::WBOX, &tmW, x, col_lo, full(stage));
-            tma_load_2d(sw + (GT_KSUB + q) * G::WBOX, &tmW, x, col_lo + half, full(stage));
-            tma_load_2d(sw + G::W_BYTES + q * G::ABOX, &tmA, x, 0, full(stage));
+        for (int kt = 0; kt < ksteps; ++kt, ++issued) {
+          if (issued >= pre) {
+            if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
+            mbar_expect_tx(full(stage), G::STAGE);
+            ctl->pending[stage] = (int)phase;
+            load_w(stage, kt, col_lo);
+            load_a(stage, kt);
           }
           if (++stage == G::STAGES) {
             stage = 0;
@@ -112,8 +138,11 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
           }
         }
       }
+    } else {
+      griddep_wait();
     }
   } else {
+    griddep_wait();
     // consumers: warp w owns rows 8w..8w+7 of both strips
     int stage = 0;
     uint32_t phase = 0;
@@ -204,8 +233,17 @@ cudaError_t launch_mb(const bf16* A, int lda, const bf16* W, int K, const EpiPar
     attr = true;
   }
   const int tiles = ep.N / GT_ROWS;
-  gemv_tma_kernel<MB><<<tiles < num_sms ? tiles : num_sms, GT_THREADS, smem, stream>>>(ma, mw, K, ep, status);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(tiles < num_sms ? tiles : num_sms);
+  cfg.blockDim = dim3(GT_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<MB>, ma, mw, K, ep, status);
 }
 
 }  // namespace

@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_kernel(const float* __rest
                                                              const int* __restrict__ rows, int d,
                                                              const float* __restrict__ gamma, float eps,
                                                              bf16* __restrict__ u, float* __restrict__ x_out) {
+  griddep_launch_dependents();  // a programmatic dependent may start as these blocks leave
   __shared__ float red[RN_THREADS / 32];
   constexpr int MAXC = RN_MAXV / 2;  // 8-element chunks per thread: d <= 8192
   const int t = blockIdx.x;

@@ -18,6 +18,10 @@ SMALL128 = synth.ModelShape("small-d128", L=6, d=512, n_q=4, n_kv=2, d_h=128, ff
 # head (5120) GEMMs of the tail and of decode take the TMA-fed skinny kernel (>= 76 tiles)
 MEDIUM = synth.ModelShape("medium-wide", L=4, d=1024, n_q=32, n_kv=8, d_h=128, ffn=4864, vocab=5120,
                           rope_theta=500000.0)
+# GQA group of 8 query heads per KV head (the Llama-3.1-70B ratio): the largest group the
+# single-row attention kernels take as rows of one MMA operand
+GQA8 = synth.ModelShape("small-gqa8", L=4, d=512, n_q=16, n_kv=2, d_h=128, ffn=768, vocab=1024,
+                        rope_theta=500000.0)
 # Q/K/V bias (Qwen-style), single KV head
 SMALL_BIAS = synth.ModelShape("small-bias", L=4, d=640, n_q=5, n_kv=1, d_h=128, ffn=704, vocab=1024,
                               rope_theta=1000000.0, qkv_bias=True)

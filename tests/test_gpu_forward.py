@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_helpers import KV_REL_TOL, LOGIT_ABS_TOL, MEDIUM, SMALL128, rel_l2
+from gpu_helpers import GQA8, KV_REL_TOL, LOGIT_ABS_TOL, MEDIUM, SMALL128, rel_l2
 from oracle import model as OM
 
 pytestmark = pytest.mark.gpu
@@ -177,4 +177,27 @@ def test_wide_skinny_gemms_prefill_tail_and_decode():
         c2, ref2 = OM.swiftkv_decode_step(cfg, w, caches[s], toks[s], l, g)
         assert float(np.abs(lg2[s] - ref2).max()) <= LOGIT_ABS_TOL
         _check_kv(m, kv, s, lens[s] + 1, c2)
+    assert m.status() == 0
+
+
+def test_gqa8_prefill_decode_and_long_tail():
+    """Eight query heads per KV head (the 70B ratio): prompt tiles, a tail row with more than
+    one 256-key split, one-token chunks and decode steps against the oracle."""
+    import torch
+    from swiftkv_prefill_skipping_gb300 import api
+    l, g = 2, 2
+    lens = [700, 33, 1]
+    m, kv, batch, w, cfg = _setup(GQA8, l, g, lens, reserve=2)
+    seq = [batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]] for s in range(3)]
+    lg = api.prefill(m, torch.as_tensor(batch.tokens, device="cuda"), batch.cu_seqlens, kv).cpu().numpy()
+    caches, refs = OM.swiftkv_prefill(cfg, w, seq, l, g)
+    for s in range(3):
+        assert float(np.abs(lg[s] - refs[s]).max()) <= LOGIT_ABS_TOL, s
+        _check_kv(m, kv, s, lens[s], caches[s])
+    toks = [OM.greedy(r) for r in refs]
+    lg2, _ = api.decode_step(m, torch.tensor(toks, dtype=torch.int32, device="cuda"), lens, kv)
+    lg2 = lg2.cpu().numpy()
+    for s in range(3):
+        _, ref2 = OM.swiftkv_decode_step(cfg, w, caches[s], toks[s], l, g)
+        assert float(np.abs(lg2[s] - ref2).max()) <= LOGIT_ABS_TOL, s
     assert m.status() == 0

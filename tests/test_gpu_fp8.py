@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_helpers import LOGIT_ABS_TOL, SMALL128, SMALL_BIAS
+from gpu_helpers import GQA8, LOGIT_ABS_TOL, SMALL128, SMALL_BIAS
 from oracle import model as OM
 
 pytestmark = pytest.mark.gpu
@@ -53,13 +53,14 @@ def _check_cache(m, kv, s, n, caches):
                 assert np.all(np.abs(got_scale - ref_scale) <= amax / 448.0 * 2.0 ** -7 + 1e-30), which
 
 
-@pytest.mark.parametrize("case", ["tiny_d64", "small_d128", "bias_gqa5"])
+@pytest.mark.parametrize("case", ["tiny_d64", "small_d128", "bias_gqa5", "gqa8"])
 def test_fp8_prefill_codes_scales_and_logits(case):
     import torch
     from swiftkv_prefill_skipping_gb300 import api
     shape, l, g, lens = {"tiny_d64": (synth.TINY, 2, 2, [1, 17, 130, 64]),
                          "small_d128": (SMALL128, 2, 2, [300, 77, 5]),
-                         "bias_gqa5": (SMALL_BIAS, 2, 1, [129, 40])}[case]
+                         "bias_gqa5": (SMALL_BIAS, 2, 1, [129, 40]),
+                         "gqa8": (GQA8, 2, 2, [700, 33, 1])}[case]
     m, kv, batch, w, cfg = _setup(shape, l, g, lens)
     lg = api.prefill(m, torch.as_tensor(batch.tokens, device="cuda"), batch.cu_seqlens, kv).cpu().numpy()
     assert m.status() == 0
