@@ -226,8 +226,9 @@ int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspa
  * cp.async one (impl 5). */
 int swiftkv_set_gemm_impl(swiftkv_model* m, int impl);
 
-/* Kernel family for the prompt tokens' attention: 0 = tcgen05 with TMA-staged paged K/V
- * (default; d_head 128), 1 = warp-level mma.sync (always used for d_head 64). */
+/* Kernel family for the prompt tokens' attention: 0 = tcgen05 with TMA-staged paged K/V,
+ * two 128-row query tiles per CTA (default; d_head 128), 1 = warp-level mma.sync (always
+ * used for d_head 64), 2 = tcgen05 with one 128-row query tile per CTA (cross-check). */
 int swiftkv_set_attention_impl(swiftkv_model* m, int impl);
 
 /* Kernel self-test entry (no model needed): C = A * B^T on the current device.

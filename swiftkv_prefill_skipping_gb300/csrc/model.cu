@@ -268,7 +268,7 @@ struct Ctx {
   const swiftkv_kv_pages* kv;
   bf16* const* k_dev;  // device arrays of pool pointers
   bf16* const* v_dev;
-  bool tc_attn = false;  // prefill attention on tcgen05 (128-row query tiles)
+  bool tc_attn = false;  // prefill attention on tcgen05 (attn_impl 0: 256-row tile pairs, 2: 128-row tiles)
   const int* ctx = nullptr;  // device [P]: cached tokens before each chunk (nullptr: none)
   int nshort = 0;            // rows of short chunks, attended one row at a time (w.srow / w.sseq)
   SplitPlan sp_short{};      // key-split plan of those rows
@@ -415,7 +415,11 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode",
           prefill ? (ntiles > 0) + (x.nshort > 0 ? launches(x.sp_short) : 0) : launches(x.sp_rows), attn_flops,
           0.0);
-  if (prefill && x.tc_attn)
+  if (prefill && x.tc_attn && m->attn_impl == 0)
+    e = launch_attention_prefill_tc2(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
+                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
+                                     m->Nq, m->status, x.s);
+  else if (prefill && x.tc_attn)
     e = launch_attention_prefill_tc(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
                                     m->Nq, m->status, x.s);
@@ -746,7 +750,7 @@ int swiftkv_set_gemm_impl(swiftkv_model* m, int impl) {
 
 int swiftkv_set_attention_impl(swiftkv_model* m, int impl) {
   if (!m) return fail(SWIFTKV_EINVAL, "null model");
-  if (impl != 0 && impl != 1) return fail(SWIFTKV_EINVAL, "attention impl %d", impl);
+  if (impl < 0 || impl > 2) return fail(SWIFTKV_EINVAL, "attention impl %d", impl);
   m->attn_impl = impl;
   return SWIFTKV_OK;
 }
@@ -866,8 +870,8 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   if ((long long)T * std::max(m->Fp, m->cfg.d) >= (1LL << 31)) return fail(SWIFTKV_EUNSUPPORTED, "batch too large");
   CK(cudaSetDevice(m->device));
 
-  const bool tc_attn = m->attn_impl == 0 && m->cfg.d_head == 128;
-  const int tile_rows = tc_attn ? 128 : 64;
+  const bool tc_attn = m->attn_impl != 1 && m->cfg.d_head == 128;
+  const int tile_rows = tc_attn ? (m->attn_impl == 0 ? 256 : 128) : 64;
   // Chunks of at most kShortChunk rows (decode tokens) are attended one row at a time by
   // the GQA-grouped single-row kernel: a 128-row query tile would be nearly empty and its CTA
   // per query head would read the sequence's keys once per head. The rest go in query

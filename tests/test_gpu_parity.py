@@ -187,14 +187,15 @@ def test_gemm_families_agree_within_oracle_tolerance():
 
 
 def test_attention_families_agree_within_oracle_tolerance():
-    """Prompt attention on tcgen05 (default at d_head 128) and on mma.sync: both within
-    the oracle tolerances, with prompts that end inside, at and past 128-row tiles."""
+    """Prompt attention on tcgen05 with two query tiles per CTA (default at d_head 128), on
+    tcgen05 with one tile, and on mma.sync: all within the oracle tolerances, with prompts
+    that end inside, at and past 128-row tiles and 256-row tile pairs."""
     from swiftkv_prefill_skipping_gb300 import api, binding
-    lens = [300, 129, 128, 1, 77, 257]
+    lens = [300, 129, 128, 1, 77, 257, 384, 600]
     batch = synth.prompt_batch(SMALL128.vocab, len(lens), 0, 0, lens=lens)
     idx, caches, ref_logits, _ = oracle_prefill(SMALL128, 4, 1, batch, gain_std=0.1)
     out = {}
-    for impl in (0, 1):
+    for impl in (0, 1, 2):
         m = api.load_synthetic(SMALL128, 4, 1, gain_std=0.1)
         binding.check(binding.lib().swiftkv_set_attention_impl(m.handle, impl))
         _, kv, logits = run_gpu_prefill(SMALL128, 4, 1, batch, model=m)
@@ -203,3 +204,5 @@ def test_attention_families_agree_within_oracle_tolerance():
         assert m.status() == 0
         out[impl] = logits.cpu().numpy()
     assert float(np.abs(out[0] - out[1]).max()) <= LOGIT_ABS_TOL
+    # the two tcgen05 kernels do the same arithmetic per row in the same order
+    assert np.array_equal(out[0], out[2])
