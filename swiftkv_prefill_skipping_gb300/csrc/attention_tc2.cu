@@ -265,8 +265,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
       }
       tc_fence_after();
       float sc[BKV];
-      tmem_ld32(tmem + lane_off + s_col + sb * BKV, sc);
-      tmem_ld32(tmem + lane_off + s_col + sb * BKV + 32, sc + 32);
+      tmem_ld64(tmem + lane_off + s_col + sb * BKV, sc);
       tc_fence_before();
       mbar_arrive(bar(ctl->s_empty[t][sb]));
       const bool interior = (j + 1) * BKV - 1 <= c0 + q0 && (j + 1) * BKV <= nk;  // no key masked in any row
@@ -277,9 +276,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
           if (key > qpos || key >= nk) sc[i] = -INFINITY;
         }
       }
-      float mx = -INFINITY;
+      // row max and row sum over 8 independent partials (short dependency chains), combined
+      // in a fixed order
+      float pm[8];
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) mx = fmaxf(mx, sc[i]);
+      for (int k = 0; k < 8; ++k) pm[k] = sc[k];
+#pragma unroll
+      for (int i = 8; i < BKV; ++i) pm[i & 7] = fmaxf(pm[i & 7], sc[i]);
+      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
       mx *= scale_log2;
       const bool move = mx > m + kStaleMax;
       if (__any_sync(0xffffffffu, move)) {
@@ -304,13 +308,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
         m = mn;
       }
       const float mneg = -m;
-      float rs = 0.f;
+      float ps[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) ps[k] = 0.f;
 #pragma unroll
       for (int i = 0; i < BKV; ++i) {
         sc[i] = ex2_approx(fmaf(sc[i], scale_log2, mneg));
-        rs += sc[i];
+        ps[i & 7] += sc[i];
       }
-      l += rs;
+      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
       // P buffer sb was last read by the P V of block j-2
       if (j >= 2 && !wait_pv(j - 2)) {
         ok = false;
