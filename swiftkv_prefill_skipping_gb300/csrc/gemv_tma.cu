@@ -2,7 +2,8 @@
 // weights at HBM rate: C = A * W^T with the shared epilogue.
 //
 // Persistent: one CTA per SM walks the weight tiles (64 rows: two 32-row strips `half`
-// apart, so RoPE and SwiGLU partners (n, n + half) stay in one thread) over the whole K.
+// apart, so RoPE and SwiGLU partners (n, n + half) stay in one thread; 32-row tiles of two
+// 16-row strips for weights with fewer than SMs / 2 64-row tiles) over the whole K.
 // One producer thread streams, per 256-deep k step, the tile's 32 x 64 weight boxes (four
 // per strip, so each weight row is read 512 contiguous bytes at a time) and the matching
 // slice of A (rows past M and columns past K zero-filled) with TMA into a ring of about
@@ -10,7 +11,7 @@
 // 8w..8w+7 of both strips) with ldmatrix and accumulate on mma.sync (bf16 in, fp32
 // accumulate, k in order), then run the epilogue from registers. No scratch; a row's
 // arithmetic does not depend on M. Used when the matrix has at least half as many tiles as
-// there are SMs (narrower ones leave SMs idle and take the cp.async kernel). All waits are
+// there are SMs (narrower ones would leave SMs idle and take the cp.async kernel). All waits are
 // bounded: on a timeout the CTA flags kStatusTimeout, drains its own copies and exits.
 #include <cuda.h>
 
@@ -24,18 +25,19 @@ namespace {
 
 using namespace tc;
 
-constexpr int GT_ROWS = 64;      // weight rows per tile (two 32-row strips)
 constexpr int GT_BK = 64;        // k per box: one 128-byte swizzle row
 constexpr int GT_KSUB = 4;       // boxes along k per stage (256 k)
-constexpr int GT_CONSUMERS = 4;  // warps
-constexpr int GT_THREADS = (GT_CONSUMERS + 1) * 32;
 constexpr int GT_RING_BYTES = 192 * 1024;
 constexpr int GT_MAX_STAGES = 24;
 
-template <int MB>
+// TR: weight rows per tile (two TR/2-row strips; 64, or 32 for weights with few rows);
+// TR/16 consumer warps each own 8 rows of both strips.
+template <int MB, int TR>
 struct Gt {
+  static constexpr int CONSUMERS = TR / 16;
+  static constexpr int THREADS = (CONSUMERS + 1) * 32;
   static constexpr int A_ROWS = MB * 16;
-  static constexpr int WBOX = GT_ROWS / 2 * GT_BK * 2;        // one 32 x 64 box: 4 KB
+  static constexpr int WBOX = TR / 2 * GT_BK * 2;             // one (TR/2) x 64 box
   static constexpr int ABOX = A_ROWS * GT_BK * 2;
   static constexpr int W_BYTES = 2 * GT_KSUB * WBOX;           // strip-major: [strip][ksub]
   static constexpr int A_BYTES = GT_KSUB * ABOX;
@@ -55,11 +57,11 @@ constexpr int gt_smem_bytes(int stage_bytes, int stages) { return 1024 + stages 
 // byte offset of 16-byte chunk `ch` of row `row` in a 128B-swizzled box (rows of 128 bytes)
 __device__ __forceinline__ uint32_t sw128(int row, int ch) { return (uint32_t)(row * 128 + ((ch ^ (row & 7)) << 4)); }
 
-template <int MB>
-__global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_constant__ CUtensorMap tmA,
+template <int MB, int TR>
+__global__ void __launch_bounds__(Gt<MB, TR>::THREADS, 1) gemv_tma_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                  const __grid_constant__ CUtensorMap tmW, int K,
                                                                  EpiParams ep, int* status) {
-  using G = Gt<MB>;
+  using G = Gt<MB, TR>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -69,8 +71,8 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = ep.M, N = ep.N;
   const int half = pair_half(ep);
-  const int strips = half / 32;
-  const int tiles = N / GT_ROWS;
+  const int strips = half / (TR / 2);
+  const int tiles = N / TR;
   const int ksteps = (K + GT_BK * GT_KSUB - 1) / (GT_BK * GT_KSUB);  // stages per tile
   auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
   auto empty = [&](int s) { return smem_u32(&ctl->empty[s]); };
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::STAGES; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), GT_CONSUMERS);
+      mbar_init(empty(s), G::CONSUMERS);
       ctl->pending[s] = -1;
     }
     ctl->abort = 0;
@@ -92,7 +94,7 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   // that kernel; everything that reads its output (A, and the epilogue's residual rows)
   // comes after griddepcontrol.wait.
   griddep_launch_dependents();
-  if (warp == GT_CONSUMERS) {
+  if (warp == G::CONSUMERS) {
     // producer
     if (lane == 0) {
       int stage = 0;
@@ -215,27 +217,27 @@ __global__ void __launch_bounds__(GT_THREADS, 1) gemv_tma_kernel(const __grid_co
   }
 }
 
-template <int MB>
+template <int MB, int TR>
 cudaError_t launch_mb(const bf16* A, int lda, const bf16* W, int K, const EpiParams& ep, int num_sms, int* status,
                       cudaStream_t stream) {
-  using G = Gt<MB>;
+  using G = Gt<MB, TR>;
   constexpr int smem = gt_smem_bytes(G::STAGE, G::STAGES);
   static_assert(smem <= 227 * 1024, "ring too large");
   static_assert(G::STAGE % 1024 == 0, "stages must keep 1024-byte alignment for the 128B swizzle");
   CUtensorMap ma, mw;
   if (!tma_map_bf16_2d(&ma, A, ep.M, K, lda, GT_BK, G::A_ROWS, true) ||
-      !tma_map_bf16_2d(&mw, W, ep.N, K, K, GT_BK, GT_ROWS / 2, true))
+      !tma_map_bf16_2d(&mw, W, ep.N, K, K, GT_BK, TR / 2, true))
     return cudaErrorNotSupported;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<MB, TR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  const int tiles = ep.N / GT_ROWS;
+  const int tiles = ep.N / TR;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles < num_sms ? tiles : num_sms);
-  cfg.blockDim = dim3(GT_THREADS);
+  cfg.blockDim = dim3(G::THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute at[1];
@@ -243,7 +245,16 @@ cudaError_t launch_mb(const bf16* A, int lda, const bf16* W, int K, const EpiPar
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<MB>, ma, mw, K, ep, status);
+  return cudaLaunchKernelEx(&cfg, gemv_tma_kernel<MB, TR>, ma, mw, K, ep, status);
+}
+
+template <int TR>
+cudaError_t launch_tr(const bf16* A, int lda, const bf16* W, int K, const EpiParams& ep, int num_sms, int* status,
+                      cudaStream_t stream) {
+  if (ep.M <= 16) return launch_mb<1, TR>(A, lda, W, K, ep, num_sms, status, stream);
+  if (ep.M <= 32) return launch_mb<2, TR>(A, lda, W, K, ep, num_sms, status, stream);
+  if (ep.M <= 48) return launch_mb<3, TR>(A, lda, W, K, ep, num_sms, status, stream);
+  return launch_mb<4, TR>(A, lda, W, K, ep, num_sms, status, stream);
 }
 
 }  // namespace
@@ -252,13 +263,12 @@ cudaError_t launch_gemv_tma(const bf16* A, int lda, const bf16* W, int K, const 
                             int* status, cudaStream_t stream) {
   const int half = pair_half(ep);
   if (ep.M < 1 || ep.M > 64 || K % GT_BK || ep.N % 128 || half % 32 || (2 * half) > 128 || lda % 8 ||
-      (reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(W) & 15) ||
-      2 * (ep.N / GT_ROWS) < num_sms)
+      (reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(W) & 15))
     return cudaErrorNotSupported;
-  if (ep.M <= 16) return launch_mb<1>(A, lda, W, K, ep, num_sms, status, stream);
-  if (ep.M <= 32) return launch_mb<2>(A, lda, W, K, ep, num_sms, status, stream);
-  if (ep.M <= 48) return launch_mb<3>(A, lda, W, K, ep, num_sms, status, stream);
-  return launch_mb<4>(A, lda, W, K, ep, num_sms, status, stream);
+  // 64-row tiles when there are enough of them for half the SMs, else 32-row tiles
+  if (2 * (ep.N / 64) >= num_sms) return launch_tr<64>(A, lda, W, K, ep, num_sms, status, stream);
+  if (2 * (ep.N / 32) >= num_sms) return launch_tr<32>(A, lda, W, K, ep, num_sms, status, stream);
+  return cudaErrorNotSupported;
 }
 
 }  // namespace skv

@@ -72,7 +72,9 @@ def test_gemv_matches_torch_fp32(M, N, K):
 # N / 64 >= 76 tiles (the TMA kernel's range on 152 SMs); K = 704 and 320 end inside a
 # 256-deep stage (the boxes past K read zeros)
 @pytest.mark.parametrize("M,N,K", [(1, 5120, 4096), (16, 9728, 512), (64, 5120, 14336), (37, 10240, 704),
-                                   (48, 128256, 256), (24, 7168, 5120), (5, 4864, 320)])
+                                   (48, 128256, 256), (24, 7168, 5120), (5, 4864, 320),
+                                   # 32-row tiles: N / 64 below half the SMs
+                                   (16, 4096, 4096), (1, 4096, 14336), (64, 4096, 704), (33, 2432, 512)])
 def test_tma_gemv_matches_torch_fp32(M, N, K):
     import torch
     Cm, ref = _run(6, M, N, K)
@@ -85,11 +87,11 @@ def test_tma_gemv_rejects_narrow_weights():
     import torch
     from swiftkv_prefill_skipping_gb300 import binding as B
     with pytest.raises(B.SwiftKVError) as e:
-        _run(6, 16, 4096, 4096)
+        _run(6, 16, 1024, 4096)
     assert e.value.code == -9
 
 
-@pytest.mark.parametrize("N,K", [(5120, 4096), (9728, 704), (7168, 5120)])
+@pytest.mark.parametrize("N,K", [(5120, 4096), (9728, 704), (7168, 5120), (4096, 4096)])
 def test_tma_gemv_rows_do_not_depend_on_batch_size(N, K):
     """A row's result is the same bits whatever M is."""
     import torch
