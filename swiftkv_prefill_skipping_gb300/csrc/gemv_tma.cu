@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(Gt<MB, TR>::THREADS, 1) gemv_tma_kernel(const 
   const int ksteps = (K + GT_BK * GT_KSUB - 1) / (GT_BK * GT_KSUB);  // stages per tile
   auto full = [&](int s) { return smem_u32(&ctl->full[s]); };
   auto empty = [&](int s) { return smem_u32(&ctl->empty[s]); };
-  auto col_of = [&](int tile) { return (tile / strips) * 2 * half + (tile % strips) * 32; };
+  auto col_of = [&](int tile) { return (tile / strips) * 2 * half + (tile % strips) * (TR / 2); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < G::STAGES; ++s) {
