@@ -1,9 +1,10 @@
 // Single-row GQA attention over the paged KV cache, split along the keys: decode tokens,
 // the last token of each prompt in the SwiftKV tail, and rows of short chunks.
 //
-// The work is a list of items v = (unit, KV head), a unit being keys [k0, k0 + 256) of row
-// b, so a long context is spread over many warps and short and long rows mix without
-// stragglers; the fixed split keeps every row's arithmetic independent of the batch. One CTA of 4 warps per SM; each warp walks its
+// The work is a list of items v = (unit, KV head), a unit being keys [k0, k0 + split) of row
+// b (split 128 for rows of up to 1024 keys, else 256), so a long context is spread over
+// many warps and short and long rows mix without stragglers; the split depends on the row's
+// own length only, so no row's arithmetic depends on the batch. One CTA of 4 warps per SM; each warp walks its
 // own items (v = global warp, + all warps, ...) one 16-key page at a time. Each (page, KV
 // head) block is 16*d_head*2 contiguous bytes in the pool; the warp stages K and V (and,
 // with an item's first page, its G query rows) with cp.async into a 2-slot ring of
@@ -673,10 +674,7 @@ cudaError_t launch_attention_decode_split_fp8(const bf16* q, int ldq, const uint
   return cudaErrorNotSupported;
 }
 
-int split_keys_for(int nkeys) {
-  (void)nkeys;
-  return kSplitKeys;
-}
+int split_keys_for(int nkeys) { return nkeys <= kShortRowKeys ? kSplitKeys / 2 : kSplitKeys; }
 
 void split_plan_host(const int* nkeys, int items, std::vector<int>* units, std::vector<int>* ubeg) {
   units->clear();

@@ -124,8 +124,11 @@ struct SplitPlan {
   float* part;
 };
 // Host: splits item b's nkeys[b] keys into units of split_keys_for(nkeys[b]) keys (a
-// multiple of 64 that depends on nothing but the row's own length).
+// multiple of 64 that depends on nothing but the row's own length): 128 for rows of up to
+// kShortRowKeys keys (more, smaller units keep short-context decode batches busy), 256 above
+// (fewer partials to combine for long contexts).
 constexpr int kSplitKeys = 256;
+constexpr int kShortRowKeys = 1024;
 int split_keys_for(int nkeys);
 void split_plan_host(const int* nkeys, int items, std::vector<int>* units, std::vector<int>* ubeg);
 size_t split_part_floats(int num_units, int n_q, int d_head);
