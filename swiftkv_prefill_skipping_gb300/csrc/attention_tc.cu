@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
+#include "attn_common.cuh"
 
 namespace skv {
 
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
-          w[e] = pack_f16(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
+          w[e] = pack_f16_sat(f.x, f.y);
         }
         vt[c] = rw;
       }
@@ -258,10 +259,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
       // in a fixed order
       float pm[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) pm[k] = sc[k];
-#pragma unroll
-      for (int i = 8; i < BKV; ++i) pm[i & 7] = fmaxf(pm[i & 7], sc[i]);
-      float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7])));
+      for (int k = 0; k < 8; ++k) {  // sc[k], sc[k + 8], ..., sc[k + 56] with three-input max
+        float v = fmax3f(sc[k], sc[k + 8], sc[k + 16]);
+        v = fmax3f(v, sc[k + 24], sc[k + 32]);
+        v = fmax3f(v, sc[k + 40], sc[k + 48]);
+        pm[k] = fmaxf(v, sc[k + 56]);
+      }
+      float mx = fmax3f(fmax3f(pm[0], pm[1], pm[2]), fmax3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
       mx *= scale_log2;
       const bool move = mx > m + kStaleMax;
       if (__any_sync(0xffffffffu, move)) {
