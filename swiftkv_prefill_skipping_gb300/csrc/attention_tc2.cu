@@ -1,9 +1,12 @@
 // Varlen causal GQA flash attention on tcgen05 (sm_103a), d_head = 128, two 128-row query
 // tiles per CTA sharing every K/V block, reading K/V straight out of the paged cache.
 //
-// One CTA = query rows [256p, 256p + 256) of one prompt chunk x one query head: tile A the
+// Work item = query rows [256p, 256p + 256) of one prompt chunk x one query head: tile A the
 // first 128 rows, tile B the next 128 (absent past the chunk's end). A chunk may follow ctx
-// cached tokens: its rows sit at positions ctx.. and see keys [0, ctx + row]. 12 warps:
+// cached tokens: its rows sit at positions ctx.. and see keys [0, ctx + row]. Persistent: one
+// CTA per SM walks its share of the items (heaviest first, alternate rounds reversed) with
+// TMEM, barriers and the K/V ring carried from item to item, so the next item's Q and K/V
+// loads and first S MMAs run while the softmax warps write the current item's output. 12 warps:
 //   warp 0      TMA: both Q tiles once (two 64-column halves each, 128B swizzle), then per
 //               64-key block the K and V rows of its four 16-token pages into a 3-stage ring
 //   warp 1      allocates all 512 TMEM columns; one lane issues, per block, S_A = Q_A K^T and
@@ -19,7 +22,9 @@
 //               O / l from TMEM to global memory.
 // While one tile's softmax warps work, the tensor core runs the other tile's MMAs, and each
 // K/V block is loaded and converted once for 256 query rows. Tile A needs up to 128 fewer
-// keys than tile B; its last blocks are skipped. All mbarrier waits are bounded; on a
+// keys than tile B; its last blocks are skipped. Between items, Q is reloaded once the last
+// S MMA of the item has completed (q_empty), and a tile's first P V of the next item waits
+// until its O has been read out of TMEM (o_empty). All mbarrier waits are bounded; on a
 // timeout the CTA flags kStatusTimeout, drains its own TMA copies and MMAs, frees TMEM and
 // exits.
 #include <cuda.h>
@@ -53,8 +58,9 @@ constexpr int O_COL = 256;
 constexpr float kStaleMax = 8.f;               // log2 headroom before O is rescaled
 
 struct Ctrl {
-  uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], v_ready[KV_STAGES];
+  uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], v_ready[KV_STAGES];
   uint64_t s_full[2][2], s_empty[2][2], p_full[2][2], pv_done[2][2], fin;  // [tile][buffer]
+  uint64_t o_empty[2];                                                     // [tile]
   uint32_t tmem_base;
   int abort;
   int pending[KV_STAGES + 1];
@@ -65,11 +71,43 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);  // Q (K-major) x K (K-major)
 constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true, true);  // P (K-major) x V (MN-major), fp16
 
+// One work item: query rows [256p, 256p + 256) of one chunk x one query head.
+struct Item {
+  int s, h, seq0, n, c0, nk, q0a, q0b, nblk_a, nblk_b, nblk;
+  bool has_b;
+};
+
+// This CTA's it-th item. Items are (tile, head) pairs, tile-major over the tile list (which is
+// sorted heaviest first); CTA c takes item c of every round of gridDim.x items, counted from
+// the other end in odd rounds, so every CTA gets a similar total. False past the last item.
+__device__ __forceinline__ bool item_at(int it, const int* __restrict__ tiles, int n_items, int n_q,
+                                        const int* __restrict__ cu, const int* __restrict__ ctx, Item& I) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const long long w = (long long)it * G + ((it & 1) ? (G - 1 - c) : c);
+  if (w >= n_items) return false;
+  const int tile = tiles[w / n_q];
+  I.h = (int)(w % n_q);
+  I.s = tile >> 16;
+  const int qp = tile & 0xffff;
+  I.seq0 = cu[I.s];
+  I.n = cu[I.s + 1] - I.seq0;
+  // the chunk's rows sit at positions c0.. after c0 cached keys; keys [0, nk) are visible
+  I.c0 = ctx ? ctx[I.s] : 0;
+  I.nk = I.c0 + I.n;
+  I.q0a = qp * 2 * BQ;
+  I.q0b = I.q0a + BQ;
+  I.has_b = I.q0b < I.n;
+  I.nblk_a = (min(I.nk, I.c0 + I.q0a + BQ) + BKV - 1) / BKV;
+  I.nblk_b = I.has_b ? (min(I.nk, I.c0 + I.q0b + BQ) + BKV - 1) / BKV : 0;
+  I.nblk = I.has_b ? I.nblk_b : I.nblk_a;  // blocks loaded (tile B's range covers tile A's)
+  return true;
+}
+
 __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
     const __grid_constant__ CUtensorMap tmV, const int* __restrict__ bt, int max_pages, int num_pages,
-    const int* __restrict__ cu, const int* __restrict__ ctx, const int* __restrict__ tiles, int n_q, int n_kv,
-    bf16* __restrict__ out, int ldo, float scale_log2, int* status) {
+    const int* __restrict__ cu, const int* __restrict__ ctx, const int* __restrict__ tiles, int n_items, int n_q,
+    int n_kv, bf16* __restrict__ out, int ldo, float scale_log2, int* status) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -81,23 +119,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
   volatile int* abort_flag = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tile = tiles[blockIdx.x];
-  const int s = tile >> 16, qp = tile & 0xffff;
-  const int h = blockIdx.y, kvh = h / (n_q / n_kv);
-  const int seq0 = cu[s], n = cu[s + 1] - seq0;
-  // the chunk's rows sit at positions c0.. after c0 cached keys; keys [0, nk) are visible
-  const int c0 = ctx ? ctx[s] : 0, nk = c0 + n;
-  const int q0a = qp * 2 * BQ, q0b = q0a + BQ;
-  const bool has_b = q0b < n;
-  const int nblk_a = (min(nk, c0 + q0a + BQ) + BKV - 1) / BKV;
-  const int nblk_b = has_b ? (min(nk, c0 + q0b + BQ) + BKV - 1) / BKV : 0;
-  const int nblk = has_b ? nblk_b : nblk_a;  // blocks loaded (tile B's range covers tile A's)
   const int pool_rows = num_pages * n_kv * kPageSize;
+  const int group = n_q / n_kv;
 
   auto bar = [&](uint64_t& b) { return smem_u32(&b); };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(ctl->q_full), 1);
+    mbar_init(bar(ctl->q_empty), 1);
     for (int i = 0; i < KV_STAGES; ++i) {
       mbar_init(bar(ctl->kv_full[i]), 1);
       mbar_init(bar(ctl->kv_empty[i]), 1);
@@ -105,13 +134,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
       ctl->pending[i] = -1;
     }
     ctl->pending[KV_STAGES] = -1;
-    for (int t = 0; t < 2; ++t)
+    for (int t = 0; t < 2; ++t) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(bar(ctl->s_full[t][i]), 1);
         mbar_init(bar(ctl->s_empty[t][i]), 128);
         mbar_init(bar(ctl->p_full[t][i]), 128);
         mbar_init(bar(ctl->pv_done[t][i]), 1);
       }
+      mbar_init(bar(ctl->o_empty[t]), 128);
+    }
     mbar_init(bar(ctl->fin), 1);
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -127,116 +158,147 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  Item I;
 
   if (warp == 0) {
     if (lane == 0) {
-      // Q: rows seq0 + q0 .. +127 of this head's 128 columns per tile (rows past the chunk
-      // are masked later; rows past the tensor read zeros)
-      mbar_expect_tx(bar(ctl->q_full), (has_b ? 2 : 1) * Q_BYTES);
-      ctl->pending[KV_STAGES] = 0;
-      for (int t = 0; t < (has_b ? 2 : 1); ++t) {
-        const int row = seq0 + (t ? q0b : q0a);
-        tma_load_2d(sQ + t * Q_BYTES, &tmQ, h * D, row, bar(ctl->q_full));
-        tma_load_2d(sQ + t * Q_BYTES + Q_BYTES / 2, &tmQ, h * D + 64, row, bar(ctl->q_full));
-      }
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int j = 0; j < nblk; ++j) {
-        if (!mbar_wait(bar(ctl->kv_empty[stage]), phase ^ 1, abort_flag)) break;
-        mbar_expect_tx(bar(ctl->kv_full[stage]), STAGE_BYTES);
-        ctl->pending[stage] = (int)phase;
-        const uint32_t sk = sKV + stage * STAGE_BYTES, sv = sk + K_BYTES;
-#pragma unroll
-        for (int pg = 0; pg < BKV / kPageSize; ++pg) {
-          const int key = j * BKV + pg * kPageSize;
-          int page = key < nk ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
-          // a page outside the pool reads rows past the tensor's end: TMA fills zeros
-          const int row = (page >= 0 && page < num_pages) ? (page * n_kv + kvh) * kPageSize : pool_rows;
-#pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            tma_load_2d(sk + hf * KV_HALF + pg * 2048, &tmK, hf * 64, row, bar(ctl->kv_full[stage]));
-            tma_load_2d(sv + hf * KV_HALF + pg * 2048, &tmV, hf * 64, row, bar(ctl->kv_full[stage]));
-          }
+      int kv_i = 0;  // K/V blocks loaded so far (all items): ring stage and phase
+      bool ok = true;
+      for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
+        const int kvh = I.h / group;
+        // Q of this item overwrites the previous item's, once its last S MMA has completed
+        if (it > 0 && !mbar_wait(bar(ctl->q_empty), (uint32_t)((it - 1) & 1), abort_flag)) break;
+        // Q: rows seq0 + q0 .. +127 of this head's 128 columns per tile (rows past the chunk
+        // are masked later; rows past the tensor read zeros)
+        mbar_expect_tx(bar(ctl->q_full), (I.has_b ? 2 : 1) * Q_BYTES);
+        ctl->pending[KV_STAGES] = it & 1;
+        for (int t = 0; t < (I.has_b ? 2 : 1); ++t) {
+          const int row = I.seq0 + (t ? I.q0b : I.q0a);
+          tma_load_2d(sQ + t * Q_BYTES, &tmQ, I.h * D, row, bar(ctl->q_full));
+          tma_load_2d(sQ + t * Q_BYTES + Q_BYTES / 2, &tmQ, I.h * D + 64, row, bar(ctl->q_full));
         }
-        if (++stage == KV_STAGES) {
-          stage = 0;
-          phase ^= 1;
+        for (int j = 0; j < I.nblk; ++j, ++kv_i) {
+          const int stage = kv_i % KV_STAGES;
+          const uint32_t phase = (uint32_t)((kv_i / KV_STAGES) & 1);
+          if (!mbar_wait(bar(ctl->kv_empty[stage]), phase ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(bar(ctl->kv_full[stage]), STAGE_BYTES);
+          ctl->pending[stage] = (int)phase;
+          const uint32_t sk = sKV + stage * STAGE_BYTES, sv = sk + K_BYTES;
+#pragma unroll
+          for (int pg = 0; pg < BKV / kPageSize; ++pg) {
+            const int key = j * BKV + pg * kPageSize;
+            int page = key < I.nk ? bt[(size_t)I.s * max_pages + (key >> 4)] : -1;
+            // a page outside the pool reads rows past the tensor's end: TMA fills zeros
+            const int row = (page >= 0 && page < num_pages) ? (page * n_kv + kvh) * kPageSize : pool_rows;
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+              tma_load_2d(sk + hf * KV_HALF + pg * 2048, &tmK, hf * 64, row, bar(ctl->kv_full[stage]));
+              tma_load_2d(sv + hf * KV_HALF + pg * 2048, &tmV, hf * 64, row, bar(ctl->kv_full[stage]));
+            }
+          }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      bool ok = mbar_wait(bar(ctl->q_full), 0, abort_flag);
-      if (ok) ctl->pending[KV_STAGES] = -1;
-      auto issue_s = [&](int t, int j) -> bool {
-        const int st = j % KV_STAGES;
-        const uint32_t ph = (uint32_t)((j / KV_STAGES) & 1);
-        if (!mbar_wait(bar(ctl->kv_full[st]), ph, abort_flag)) return false;
-        ctl->pending[st] = -1;
-        const int sb = j & 1;
-        if (!mbar_wait(bar(ctl->s_empty[t][sb]), (uint32_t)(((j >> 1) & 1) ^ 1), abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sk = sKV + st * STAGE_BYTES;
-        const uint32_t q = sQ + t * Q_BYTES;
+      // counters over all items: K/V blocks, S/P blocks of each tile, items that used each tile's O
+      int kv_base = 0, sp[2] = {0, 0}, oi[2] = {0, 0};
+      bool ok = true;
+      for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
+        if (!mbar_wait(bar(ctl->q_full), (uint32_t)(it & 1), abort_flag)) break;
+        ctl->pending[KV_STAGES] = -1;
+        auto issue_s = [&](int t, int j) -> bool {
+          const int kv = kv_base + j, st = kv % KV_STAGES;
+          if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((kv / KV_STAGES) & 1), abort_flag)) return false;
+          ctl->pending[st] = -1;
+          const int g = sp[t] + j, sb = g & 1;
+          if (!mbar_wait(bar(ctl->s_empty[t][sb]), (uint32_t)(((g >> 1) & 1) ^ 1), abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t sk = sKV + st * STAGE_BYTES;
+          const uint32_t q = sQ + t * Q_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32;
-          const uint32_t koff = (kk >> 2) * KV_HALF + (kk & 3) * 32;
-          tc_mma(tmem + t * 128 + sb * BKV, sdesc(q + off), sdesc(sk + koff), IDESC_S, kk != 0);
-        }
-        tc_commit(bar(ctl->s_full[t][sb]));
-        return true;
-      };
-      auto issue_pv = [&](int t, int j) -> bool {
-        const int pb = j & 1;
-        if (!mbar_wait(bar(ctl->p_full[t][pb]), (uint32_t)((j >> 1) & 1), abort_flag)) return false;
-        const int st = j % KV_STAGES;
-        if (!mbar_wait(bar(ctl->v_ready[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t sv = sKV + st * STAGE_BYTES + K_BYTES;
-        const uint32_t pbase = sP + (2 * t + pb) * P_BYTES;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (Q_BYTES / 2) + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * KV_HALF + (kk & 3) * 32;
+            tc_mma(tmem + t * 128 + sb * BKV, sdesc(q + off), sdesc(sk + koff), IDESC_S, kk != 0);
+          }
+          tc_commit(bar(ctl->s_full[t][sb]));
+          return true;
+        };
+        auto issue_pv = [&](int t, int j) -> bool {
+          const int g = sp[t] + j, pb = g & 1;
+          if (!mbar_wait(bar(ctl->p_full[t][pb]), (uint32_t)((g >> 1) & 1), abort_flag)) return false;
+          const int kv = kv_base + j, st = kv % KV_STAGES;
+          if (!mbar_wait(bar(ctl->v_ready[st]), (uint32_t)((kv / KV_STAGES) & 1), abort_flag)) return false;
+          // the first P V of an item overwrites O: the previous item's output must have left TMEM
+          if (j == 0 && oi[t] > 0 && !mbar_wait(bar(ctl->o_empty[t]), (uint32_t)((oi[t] - 1) & 1), abort_flag))
+            return false;
+          tc_fence_after();
+          const uint32_t sv = sKV + st * STAGE_BYTES + K_BYTES;
+          const uint32_t pbase = sP + (2 * t + pb) * P_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BKV / 16; ++kk) {
-          // P: K-major, rows of 64 keys; V: MN-major, 64-dim halves 8 KB apart, 8-key groups 1 KB apart
-          tc_mma(tmem + O_COL + t * 128, sdesc(pbase + kk * 32), sdesc_sw128(sv + kk * 2048, KV_HALF, 1024), IDESC_O,
-                 (j | kk) != 0);
+          for (int kk = 0; kk < BKV / 16; ++kk) {
+            // P: K-major, rows of 64 keys; V: MN-major, 64-dim halves 8 KB apart, 8-key groups 1 KB apart
+            tc_mma(tmem + O_COL + t * 128, sdesc(pbase + kk * 32), sdesc_sw128(sv + kk * 2048, KV_HALF, 1024),
+                   IDESC_O, (j | kk) != 0);
+          }
+          tc_commit(bar(ctl->pv_done[t][pb]));
+          return true;
+        };
+        // q_empty is committed after the item's last S MMA (block nblk - 1), so the next item's
+        // Q can load while this item's P V and softmax finish
+        const int last_s = I.nblk - 1;
+        ok = issue_s(0, 0);
+        if (ok && I.has_b) ok = issue_s(1, 0);
+        if (ok && last_s == 0) tc_commit(bar(ctl->q_empty));
+        for (int j = 0; ok && j < I.nblk; ++j) {
+          // S of the next block for both tiles first, so the tensor core has work while the
+          // softmax warps turn this block's S into P
+          if (j + 1 < I.nblk_a && !(ok = issue_s(0, j + 1))) break;
+          if (j + 1 < I.nblk_b && !(ok = issue_s(1, j + 1))) break;
+          if (j + 1 == last_s) tc_commit(bar(ctl->q_empty));
+          if (j < I.nblk_a && !(ok = issue_pv(0, j))) break;
+          if (j < I.nblk_b && !(ok = issue_pv(1, j))) break;
+          tc_commit(bar(ctl->kv_empty[(kv_base + j) % KV_STAGES]));
         }
-        tc_commit(bar(ctl->pv_done[t][pb]));
-        return true;
-      };
-      if (ok && nblk_a > 0) ok = issue_s(0, 0);
-      if (ok && nblk_b > 0) ok = issue_s(1, 0);
-      for (int j = 0; ok && j < nblk; ++j) {
-        // S of the next block for both tiles first, so the tensor core has work while the
-        // softmax warps turn this block's S into P
-        if (j + 1 < nblk_a && !issue_s(0, j + 1)) break;
-        if (j + 1 < nblk_b && !issue_s(1, j + 1)) break;
-        if (j < nblk_a && !issue_pv(0, j)) break;
-        if (j < nblk_b && !issue_pv(1, j)) break;
-        tc_commit(bar(ctl->kv_empty[j % KV_STAGES]));
+        kv_base += I.nblk;
+        sp[0] += I.nblk_a;
+        sp[1] += I.nblk_b;
+        oi[0] += 1;
+        oi[1] += I.has_b ? 1 : 0;
       }
     }
   } else if (warp < 4) {
     // V converters: each arrived V tile bf16 -> fp16 in place (exact inside fp16's normal
     // range, clamped to +-65504) so that P V runs with P at fp16 precision
     const int t = threadIdx.x - 64;
-    for (int j = 0; j < nblk; ++j) {
-      const int st = j % KV_STAGES;
-      if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) break;
-      uint4* vt = reinterpret_cast<uint4*>(smem + 2 * Q_BYTES + st * STAGE_BYTES + K_BYTES);
-#pragma unroll 4
-      for (int c = t; c < K_BYTES / 16; c += 64) {
-        uint4 rw = vt[c];
-        uint32_t* w = reinterpret_cast<uint32_t*>(&rw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
-          w[e] = pack_f16_sat(f.x, f.y);
+    int kv_i = 0;
+    bool ok = true;
+    for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
+      for (int j = 0; j < I.nblk; ++j, ++kv_i) {
+        const int st = kv_i % KV_STAGES;
+        if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((kv_i / KV_STAGES) & 1), abort_flag)) {
+          ok = false;
+          break;
         }
-        vt[c] = rw;
+        uint4* vt = reinterpret_cast<uint4*>(smem + 2 * Q_BYTES + st * STAGE_BYTES + K_BYTES);
+#pragma unroll 4
+        for (int c = t; c < K_BYTES / 16; c += 64) {
+          uint4 rw = vt[c];
+          uint32_t* w = reinterpret_cast<uint32_t*>(&rw);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
+            w[e] = pack_f16_sat(f.x, f.y);
+          }
+          vt[c] = rw;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bar(ctl->v_ready[st]));
       }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(ctl->v_ready[st]));
     }
   } else {
     // softmax / output warps of tile t: thread <-> query row. O accumulates in TMEM across
@@ -244,123 +306,131 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
     // 2^kStaleMax (they then stay <= 256, fine for fp16); only when a row's max moves further
     // is O rescaled, by the warp, in TMEM, after the previous block's P V has landed.
     const int t = (warp - 4) >> 2;
-    const int nb = t ? nblk_b : nblk_a;
-    const int q0 = t ? q0b : q0a;
     const int q4 = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q4 * 32 + lane;
-    const int qrow = q0 + r;     // row within the chunk
-    const int qpos = c0 + qrow;  // its position
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t s_col = t * 128, o_col = O_COL + t * 128;
-    float m = -INFINITY, l = 0.f;
-    bool ok = true;
-    auto wait_pv = [&](int j) -> bool {
-      return mbar_wait(bar(ctl->pv_done[t][j & 1]), (uint32_t)((j >> 1) & 1), abort_flag);
+    auto wait_pv = [&](int g) -> bool {
+      return mbar_wait(bar(ctl->pv_done[t][g & 1]), (uint32_t)((g >> 1) & 1), abort_flag);
     };
-
-    for (int j = 0; j < nb; ++j) {
-      const int sb = j & 1;
-      if (!mbar_wait(bar(ctl->s_full[t][sb]), (uint32_t)((j >> 1) & 1), abort_flag)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      float sc[BKV];
-      tmem_ld64(tmem + lane_off + s_col + sb * BKV, sc);
-      tc_fence_before();
-      mbar_arrive(bar(ctl->s_empty[t][sb]));
-      const bool interior = (j + 1) * BKV - 1 <= c0 + q0 && (j + 1) * BKV <= nk;  // no key masked in any row
-      if (!interior) {
+    int sp = 0;  // S/P blocks of this tile over all items
+    bool ok = true;
+    for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
+      if (t == 1 && !I.has_b) continue;
+      const int nb = t ? I.nblk_b : I.nblk_a;
+      const int q0 = t ? I.q0b : I.q0a;
+      const int qrow = q0 + r;       // row within the chunk
+      const int qpos = I.c0 + qrow;  // its position
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < nb; ++j) {
+        const int g = sp + j, sb = g & 1;
+        if (!mbar_wait(bar(ctl->s_full[t][sb]), (uint32_t)((g >> 1) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sc[BKV];
+        tmem_ld64(tmem + lane_off + s_col + sb * BKV, sc);
+        tc_fence_before();
+        mbar_arrive(bar(ctl->s_empty[t][sb]));
+        const bool interior = (j + 1) * BKV - 1 <= I.c0 + q0 && (j + 1) * BKV <= I.nk;  // no key masked in any row
+        if (!interior) {
+#pragma unroll
+          for (int i = 0; i < BKV; ++i) {
+            const int key = j * BKV + i;
+            if (key > qpos || key >= I.nk) sc[i] = -INFINITY;
+          }
+        }
+        // row max and row sum over 8 independent partials (short dependency chains), combined
+        // in a fixed order
+        float pm[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {  // sc[k], sc[k + 8], ..., sc[k + 56] with three-input max
+          float v = fmax3f(sc[k], sc[k + 8], sc[k + 16]);
+          v = fmax3f(v, sc[k + 24], sc[k + 32]);
+          v = fmax3f(v, sc[k + 40], sc[k + 48]);
+          pm[k] = fmaxf(v, sc[k + 56]);
+        }
+        float mx = fmax3f(fmax3f(pm[0], pm[1], pm[2]), fmax3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
+        mx *= scale_log2;
+        const bool move = mx > m + kStaleMax;
+        if (__any_sync(0xffffffffu, move)) {
+          const float mn = move ? mx : m;
+          const float factor = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
+          if (j > 0) {  // O holds blocks 0..j-1: wait for the last of them, rescale the warp's rows
+            if (!wait_pv(g - 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < D; c += 32) {
+              float v[32];
+              tmem_ld32(tmem + lane_off + o_col + c, v);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] *= factor;
+              tmem_st32(tmem + lane_off + o_col + c, v);
+            }
+          }
+          l *= factor;
+          m = mn;
+        }
+        const float mneg = -m;
+        float ps[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ps[k] = 0.f;
 #pragma unroll
         for (int i = 0; i < BKV; ++i) {
-          const int key = j * BKV + i;
-          if (key > qpos || key >= nk) sc[i] = -INFINITY;
+          sc[i] = ex2_approx(fmaf(sc[i], scale_log2, mneg));
+          ps[i & 7] += sc[i];
         }
-      }
-      // row max and row sum over 8 independent partials (short dependency chains), combined
-      // in a fixed order
-      float pm[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {  // sc[k], sc[k + 8], ..., sc[k + 56] with three-input max
-        float v = fmax3f(sc[k], sc[k + 8], sc[k + 16]);
-        v = fmax3f(v, sc[k + 24], sc[k + 32]);
-        v = fmax3f(v, sc[k + 40], sc[k + 48]);
-        pm[k] = fmaxf(v, sc[k + 56]);
-      }
-      float mx = fmax3f(fmax3f(pm[0], pm[1], pm[2]), fmax3f(pm[3], pm[4], pm[5]), fmaxf(pm[6], pm[7]));
-      mx *= scale_log2;
-      const bool move = mx > m + kStaleMax;
-      if (__any_sync(0xffffffffu, move)) {
-        const float mn = move ? mx : m;
-        const float factor = (m == -INFINITY) ? 0.f : ex2_approx(m - mn);
-        if (j > 0) {  // O holds blocks 0..j-1: wait for the last of them, rescale the warp's rows
-          if (!wait_pv(j - 1)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-#pragma unroll
-          for (int c = 0; c < D; c += 32) {
-            float v[32];
-            tmem_ld32(tmem + lane_off + o_col + c, v);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] *= factor;
-            tmem_st32(tmem + lane_off + o_col + c, v);
-          }
+        l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+        // P buffer sb was last read by the P V of block g - 2 (for j < 2 that block belongs to
+        // an earlier item, whose final wait below already covered it)
+        if (j >= 2 && !wait_pv(g - 2)) {
+          ok = false;
+          break;
         }
-        l *= factor;
-        m = mn;
+        unsigned char* prow = sP_gen + (2 * t + sb) * P_BYTES + r * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 u;
+          u.x = pack_f16(sc[8 * c], sc[8 * c + 1]);
+          u.y = pack_f16(sc[8 * c + 2], sc[8 * c + 3]);
+          u.z = pack_f16(sc[8 * c + 4], sc[8 * c + 5]);
+          u.w = pack_f16(sc[8 * c + 6], sc[8 * c + 7]);
+          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(ctl->p_full[t][sb]));
       }
-      const float mneg = -m;
-      float ps[8];
+      if (ok) ok = wait_pv(sp + nb - 1);
+      if (ok) {
+        tc_fence_after();
+        const float inv = 1.f / l;
+        bf16* dst = out + (size_t)(I.seq0 + min(qrow, I.n - 1)) * ldo + I.h * D;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) ps[k] = 0.f;
+        for (int c = 0; c < D; c += 32) {
+          float v[32];
+          tmem_ld32(tmem + lane_off + o_col + c, v);
+          if (qrow < I.n) {
 #pragma unroll
-      for (int i = 0; i < BKV; ++i) {
-        sc[i] = ex2_approx(fmaf(sc[i], scale_log2, mneg));
-        ps[i & 7] += sc[i];
-      }
-      l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      // P buffer sb was last read by the P V of block j-2
-      if (j >= 2 && !wait_pv(j - 2)) {
-        ok = false;
-        break;
-      }
-      unsigned char* prow = sP_gen + (2 * t + sb) * P_BYTES + r * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 u;
-        u.x = pack_f16(sc[8 * c], sc[8 * c + 1]);
-        u.y = pack_f16(sc[8 * c + 2], sc[8 * c + 3]);
-        u.z = pack_f16(sc[8 * c + 4], sc[8 * c + 5]);
-        u.w = pack_f16(sc[8 * c + 6], sc[8 * c + 7]);
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
-      }
-      fence_proxy_async_smem();
-      tc_fence_before();
-      mbar_arrive(bar(ctl->p_full[t][sb]));
-    }
-    if (ok && nb > 0) ok = wait_pv(nb - 1);
-    if (ok && nb > 0) {
-      tc_fence_after();
-      const float inv = 1.f / l;
-      bf16* dst = out + (size_t)(seq0 + min(qrow, n - 1)) * ldo + h * D;
-#pragma unroll
-      for (int c = 0; c < D; c += 32) {
-        float v[32];
-        tmem_ld32(tmem + lane_off + o_col + c, v);
-        if (qrow < n) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 u;
-            u.x = pack_bf16(v[e] * inv, v[e + 1] * inv);
-            u.y = pack_bf16(v[e + 2] * inv, v[e + 3] * inv);
-            u.z = pack_bf16(v[e + 4] * inv, v[e + 5] * inv);
-            u.w = pack_bf16(v[e + 6] * inv, v[e + 7] * inv);
-            *reinterpret_cast<uint4*>(dst + c + e) = u;
+            for (int e = 0; e < 32; e += 8) {
+              uint4 u;
+              u.x = pack_bf16(v[e] * inv, v[e + 1] * inv);
+              u.y = pack_bf16(v[e + 2] * inv, v[e + 3] * inv);
+              u.z = pack_bf16(v[e + 4] * inv, v[e + 5] * inv);
+              u.w = pack_bf16(v[e + 6] * inv, v[e + 7] * inv);
+              *reinterpret_cast<uint4*>(dst + c + e) = u;
+            }
           }
         }
+        // O has left TMEM: the next item's first P V may overwrite it
+        tc_fence_before();
+        mbar_arrive(bar(ctl->o_empty[t]));
       }
+      sp += nb;
     }
   }
 
@@ -395,9 +465,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
 cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
                                          const int* block_table, int max_pages, int num_pages, const int* cu,
                                          const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
-                                         int d_head, bf16* out, int ldo, int* status, cudaStream_t stream) {
+                                         int d_head, bf16* out, int ldo, int num_sms, int* status,
+                                         cudaStream_t stream) {
   if (num_tiles <= 0) return cudaSuccess;
-  if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8) return cudaErrorNotSupported;
+  if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8 || num_sms < 1) return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
   const int pool_rows = num_pages * n_kv * kPageSize;
   if (!tma_map_bf16_2d(&mq, q, T, n_q * D, ldq, 64, BQ, true) ||
@@ -411,9 +482,9 @@ cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf
     attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-  dim3 grid(num_tiles, n_q);
-  attn_tc2_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, block_table, max_pages, num_pages, cu, ctx, tiles,
-                                                         n_q, n_kv, out, ldo, scale_log2, status);
+  const int n_items = num_tiles * n_q;
+  attn_tc2_kernel<<<n_items < num_sms ? n_items : num_sms, THREADS, SMEM_BYTES, stream>>>(
+      mq, mk, mv, block_table, max_pages, num_pages, cu, ctx, tiles, n_items, n_q, n_kv, out, ldo, scale_log2, status);
   return cudaGetLastError();
 }
 

@@ -418,7 +418,7 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   if (prefill && x.tc_attn && m->attn_impl == 0)
     e = launch_attention_prefill_tc2(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
                                      x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
-                                     m->Nq, m->status, x.s);
+                                     m->Nq, m->num_sms, m->status, x.s);
   else if (prefill && x.tc_attn)
     e = launch_attention_prefill_tc(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
