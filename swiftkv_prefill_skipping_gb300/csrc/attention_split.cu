@@ -24,6 +24,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "pdl.cuh"
 
 namespace skv {
 
@@ -50,6 +51,7 @@ __global__ void __launch_bounds__(SW * 32, 1) attn_split_kernel(
   constexpr int CH = D / 8;  // 16-byte chunks per row
   extern __shared__ __align__(128) unsigned char smem[];
   griddep_launch_dependents();  // a programmatic dependent may start as these blocks leave
+  griddep_wait();               // itself launched as one: q and the cache rows are fresh
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   bf16* ring = reinterpret_cast<bf16*>(smem) + (size_t)warp * SSTAGES * S::STAGE;
   const int G = n_q / n_kv;
@@ -295,6 +297,7 @@ __global__ void __launch_bounds__(SW * 32, 1) attn_split_fp8_kernel(
   using S = Sp8<D>;
   extern __shared__ __align__(128) unsigned char smem[];
   griddep_launch_dependents();
+  griddep_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* ring = smem + (size_t)warp * SSTAGES8 * S::STAGE;
   const int G = n_q / n_kv;
@@ -549,6 +552,7 @@ __global__ void __launch_bounds__(CMB_THREADS) attn_split_combine(const int* __r
   __shared__ float s_w[CMB_MAX_W];
   __shared__ float s_mx[SMAXG], s_den[SMAXG];
   griddep_launch_dependents();
+  griddep_wait();  // launched as a programmatic dependent of the split kernel: its partials
   const int b = blockIdx.x, kvh = blockIdx.y;
   const int u0 = ubeg[b], ns = ubeg[b + 1] - u0;
   if (ns <= 1) return;  // written directly by its only unit
@@ -618,14 +622,12 @@ cudaError_t split_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_po
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const int total = plan.num_units * n_kv;
   const int ctas = std::min((total + SW - 1) / SW, num_sms);
-  attn_split_kernel<D><<<ctas, SW * 32, smem, stream>>>(q, ldq, k_pool, v_pool, bt, max_pages, num_pages, qpos, rows,
-                                                        seqs, plan.units, plan.num_units, n_q, n_kv, out, ldo,
-                                                        plan.part, scale_log2);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(attn_split_kernel<D>, dim3(ctas), dim3(SW * 32), smem, stream, q, ldq, k_pool, v_pool,
+                             bt, max_pages, num_pages, qpos, rows, seqs, (const int*)plan.units, plan.num_units, n_q,
+                             n_kv, out, ldo, plan.part, scale_log2);
   if (e != cudaSuccess || !plan.any_split) return e;
-  attn_split_combine<D><<<dim3(plan.num_items, n_kv), CMB_THREADS, 0, stream>>>(rows, plan.ubeg, n_q, n_kv,
-                                                                                plan.part, out, ldo);
-  return cudaGetLastError();
+  return launch_pdl(attn_split_combine<D>, dim3(plan.num_items, n_kv), dim3(CMB_THREADS), 0, stream, rows,
+                    (const int*)plan.ubeg, n_q, n_kv, (const float*)plan.part, out, ldo);
 }
 
 template <int D>
@@ -646,14 +648,12 @@ cudaError_t split_fp8_d(const bf16* q, int ldq, const uint8_t* k8, const uint8_t
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const int total = plan.num_units * n_kv;
   const int ctas = std::min((total + SW - 1) / SW, num_sms);
-  attn_split_fp8_kernel<D><<<ctas, SW * 32, smem, stream>>>(q, ldq, k8, v8, ks, vs, bt, max_pages, num_pages, qpos,
-                                                            rows, seqs, plan.units, plan.num_units, n_q, n_kv, out,
-                                                            ldo, plan.part, scale_log2);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(attn_split_fp8_kernel<D>, dim3(ctas), dim3(SW * 32), smem, stream, q, ldq, k8, v8, ks,
+                             vs, bt, max_pages, num_pages, qpos, rows, seqs, (const int*)plan.units, plan.num_units,
+                             n_q, n_kv, out, ldo, plan.part, scale_log2);
   if (e != cudaSuccess || !plan.any_split) return e;
-  attn_split_combine<D><<<dim3(plan.num_items, n_kv), CMB_THREADS, 0, stream>>>(rows, plan.ubeg, n_q, n_kv,
-                                                                                plan.part, out, ldo);
-  return cudaGetLastError();
+  return launch_pdl(attn_split_combine<D>, dim3(plan.num_items, n_kv), dim3(CMB_THREADS), 0, stream, rows,
+                    (const int*)plan.ubeg, n_q, n_kv, (const float*)plan.part, out, ldo);
 }
 
 }  // namespace

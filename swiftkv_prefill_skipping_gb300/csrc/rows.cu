@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "pdl.cuh"
 
 namespace skv {
 
@@ -130,6 +131,7 @@ __global__ void __launch_bounds__(RN_THREADS) rmsnorm_kernel(const float* __rest
                                                              const float* __restrict__ gamma, float eps,
                                                              bf16* __restrict__ u, float* __restrict__ x_out) {
   griddep_launch_dependents();  // a programmatic dependent may start as these blocks leave
+  griddep_wait();               // itself launched as one: x is the previous kernel's output
   __shared__ float red[RN_THREADS / 32];
   constexpr int MAXC = RN_MAXV / 2;  // 8-element chunks per thread: d <= 8192
   const int t = blockIdx.x;
@@ -394,8 +396,7 @@ cudaError_t launch_embed_rmsnorm(const int* tokens, int T, const bf16* embed, in
 cudaError_t launch_rmsnorm(const float* x, const int* rows, int T, int d, const float* gamma,
                            float eps, bf16* u, float* x_out, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  rmsnorm_kernel<<<T, RN_THREADS, 0, stream>>>(x, rows, d, gamma, eps, u, x_out);
-  return cudaGetLastError();
+  return launch_pdl(rmsnorm_kernel, dim3(T), dim3(RN_THREADS), 0, stream, x, rows, d, gamma, eps, u, x_out);
 }
 
 cudaError_t launch_argmax(const float* logits, int rows, int V, int* out, cudaStream_t stream) {
