@@ -5,7 +5,7 @@ import numpy as np
 import pytest
 
 import synth
-from gpu_helpers import (KV_REL_TOL, LOGIT_ABS_TOL, SMALL128, SMALL_BIAS, compare_prefill, oracle_prefill,
+from gpu_helpers import (GQA8, KV_REL_TOL, LOGIT_ABS_TOL, SMALL128, SMALL_BIAS, compare_prefill, oracle_prefill,
                          rel_l2, run_gpu_prefill, untouched_rows_are_zero)
 
 pytestmark = pytest.mark.gpu
@@ -190,6 +190,7 @@ def test_attention_families_agree_within_oracle_tolerance():
     """Prompt attention on tcgen05 with two query tiles per CTA (default at d_head 128), on
     tcgen05 with one tile, and on mma.sync: all within the oracle tolerances, with prompts
     that end inside, at and past 128-row tiles and 256-row tile pairs."""
+    import torch
     from swiftkv_prefill_skipping_gb300 import api, binding
     lens = [300, 129, 128, 1, 77, 257, 384, 600]
     batch = synth.prompt_batch(SMALL128.vocab, len(lens), 0, 0, lens=lens)
@@ -202,7 +203,37 @@ def test_attention_families_agree_within_oracle_tolerance():
         kv_err, lg_err = compare_prefill(kv, logits, batch, idx, caches, ref_logits, m.num_caches)
         assert kv_err <= KV_REL_TOL and lg_err <= LOGIT_ABS_TOL, (impl, kv_err, lg_err)
         assert m.status() == 0
-        out[impl] = logits.cpu().numpy()
-    assert float(np.abs(out[0] - out[1]).max()) <= LOGIT_ABS_TOL
-    # the two tcgen05 kernels do the same arithmetic per row in the same order
-    assert np.array_equal(out[0], out[2])
+        out[impl] = (logits.cpu().numpy(), kv)
+    assert float(np.abs(out[0][0] - out[1][0]).max()) <= LOGIT_ABS_TOL
+    # the two tcgen05 kernels do the same arithmetic per row in the same order: every cache
+    # after the first depends on all rows' prompt-attention outputs, and matches bit for bit
+    # (the logits also pass through the single-row tail attention, which impl 2 runs on
+    # another kernel, so they agree within the tolerance only)
+    assert torch.equal(out[0][1].k, out[2][1].k) and torch.equal(out[0][1].v, out[2][1].v)
+    assert float(np.abs(out[0][0] - out[2][0]).max()) <= LOGIT_ABS_TOL
+
+
+def test_persistent_attention_many_items_per_cta_bit_exact():
+    """The default prompt attention is persistent: one CTA per SM walks its share of the
+    (256-row tile pair, query head) items, carrying TMEM, barriers and the K/V ring from item
+    to item. With ~12 items per CTA (60 ragged prompts x 16 query heads), items with and
+    without a second 128-row tile and prompts ending exactly at tile boundaries, it must give
+    exactly the one-tile kernel's prompt-attention outputs (same arithmetic per row): every
+    cache after the first depends on all of them and must match bit for bit. The logits also
+    pass through the single-row tail attention, which impl 2 runs on another kernel, so they
+    agree within the oracle tolerance only."""
+    import torch
+    from swiftkv_prefill_skipping_gb300 import api, binding
+    lens = synth.uniform_int(7, 21, 60, 5, 700)
+    lens[:6] = [128, 256, 257, 129, 512, 384]
+    batch = synth.prompt_batch(GQA8.vocab, len(lens), 0, 0, lens=lens)
+    out = {}
+    for impl in (0, 2):
+        m = api.load_synthetic(GQA8, 2, 1, gain_std=0.1)
+        binding.check(binding.lib().swiftkv_set_attention_impl(m.handle, impl))
+        _, kv, logits = run_gpu_prefill(GQA8, 2, 1, batch, model=m)
+        assert m.status() == 0
+        assert not torch.isnan(logits).any()
+        out[impl] = (logits, kv)
+    assert torch.equal(out[0][1].k, out[2][1].k) and torch.equal(out[0][1].v, out[2][1].v)
+    assert float((out[0][0] - out[2][0]).abs().max()) <= LOGIT_ABS_TOL
