@@ -227,8 +227,12 @@ int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspa
 int swiftkv_set_gemm_impl(swiftkv_model* m, int impl);
 
 /* Kernel family for the prompt tokens' attention: 0 = tcgen05 with TMA-staged paged K/V,
- * two 128-row query tiles per CTA (default; d_head 128), 1 = warp-level mma.sync (always
- * used for d_head 64), 2 = tcgen05 with one 128-row query tile per CTA (cross-check). */
+ * persistent, two 128-row query tiles per work item (default; d_head 128), 1 = warp-level
+ * mma.sync (always used for d_head 64), 2 = tcgen05 with one 128-row query tile per CTA
+ * (cross-check: the same prompt-attention outputs as 0, bit for bit). The single-row
+ * attention (decode tokens, the last-token tail, chunks of at most 4 rows) runs on the
+ * key-split kernel under 0 and on the per-(row, KV head) kernel under 1 and 2, so logits
+ * differ between settings by rounding. An FP8 cache always uses the key-split kernel. */
 int swiftkv_set_attention_impl(swiftkv_model* m, int impl);
 
 /* Kernel self-test entry (no model needed): C = A * B^T on the current device.
