@@ -495,7 +495,10 @@ def run_ours(args, w, rank, world, local_rank):
                                          "peak_source": peak_src},
             "executed_tflops": exec_tflops,
             "executed_frac_of_peak": {"burst": exec_tflops / peak_burst, "sustained": exec_tflops / peak_sus},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
+            "roofline": roofline,
+            "step_roofline": step_roofline(prof, args.steps, ms_per_step, peak_sus,
+                                           float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))),
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "kv_cache": kv_cache_info(model, w),
             "decode": decode,
             "clocks": clocks,
@@ -507,6 +510,23 @@ def run_ours(args, w, rank, world, local_rank):
         print(json.dumps(line), flush=True)
     model.free()
     return 0
+
+
+def step_roofline(prof: dict, steps: int, ms_per_step: float, peak_tflops: float, hbm_gbs: float) -> dict:
+    """End-to-end roofline of one step: the sum over kernel classes of
+    max(FLOPs / bf16 peak, bytes / HBM bandwidth), from the algorithmic FLOPs and bytes each
+    class records, against the measured step time. Classes that record neither (plan,
+    host uploads) count zero; the single-row attention records FLOPs only."""
+    t = 0.0
+    per = {}
+    for name, v in prof.items():
+        tf = (v["flops"] or 0.0) / (peak_tflops * 1e12)
+        tb = (v["bytes"] or 0.0) / (hbm_gbs * 1e9)
+        per[name] = 1e3 * max(tf, tb) / steps
+        t += per[name]
+    return {"t_roofline_ms": t, "ms_per_step": ms_per_step, "frac": t / ms_per_step if ms_per_step > 0 else None,
+            "peak_tflops": peak_tflops, "hbm_gbs": hbm_gbs,
+            "per_class_ms": dict(sorted(per.items(), key=lambda kv_: -kv_[1]))}
 
 
 def kv_cache_info(model, w) -> dict:

@@ -46,3 +46,20 @@ def test_l2_note_of_the_timed_workloads():
     import synth
     for name in ("llama8b_l16", "qwen14b_l24_g4", "llama70b_l40"):
         assert bench.l2_note(synth.WORKLOADS[name].shape).startswith("inputs larger than L2")
+
+
+def test_step_roofline_arithmetic():
+    """Sum over classes of max(FLOPs / peak, bytes / bandwidth), per step, against the step."""
+    sys.path.insert(0, ROOT)
+    import bench
+    prof = {  # totals over 2 steps
+        "gemm": {"flops": 2 * 1.0e12, "bytes": 2 * 1.0e9, "ms": 2.4, "calls": 2, "kernels": 2},    # 1.0 ms vs 0.1 ms
+        "norm": {"flops": 0.0, "bytes": 2 * 5.0e9, "ms": 1.2, "calls": 2, "kernels": 2},           # 0.5 ms
+        "plan": {"flops": 0.0, "bytes": 0.0, "ms": 0.1, "calls": 2, "kernels": 2},                 # 0
+    }
+    r = bench.step_roofline(prof, steps=2, ms_per_step=2.0, peak_tflops=1000.0, hbm_gbs=10000.0)
+    assert abs(r["per_class_ms"]["gemm"] - 1.0) < 1e-12
+    assert abs(r["per_class_ms"]["norm"] - 0.5) < 1e-12
+    assert r["per_class_ms"]["plan"] == 0.0
+    assert abs(r["t_roofline_ms"] - 1.5) < 1e-12 and abs(r["frac"] - 0.75) < 1e-12
+    assert list(r["per_class_ms"]) == ["gemm", "norm", "plan"]
