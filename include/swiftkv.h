@@ -238,8 +238,8 @@ int swiftkv_set_attention_impl(swiftkv_model* m, int impl);
 /* Kernel self-test entry (no model needed): C = A * B^T on the current device.
  *   A  device bf16 [M][K] row-major; B device bf16 [N][K] row-major; C device float [M][N]
  *   impl 0 = tcgen05 single CTA, 1 = mma.sync tiles, 2 = skinny split-K (M <= 64; allocates
- *   and frees its own scratch and synchronises the device), 3 = tcgen05 with CTA pairs
- *   sharing the weight tile by TMA multicast, 4 = tcgen05 CTA pairs (cta_group::2),
+ *   and frees its own scratch and synchronises the device), 3 = not used (SWIFTKV_EINVAL),
+ *   4 = tcgen05 CTA pairs (cta_group::2),
  *   5 = skinny, one CTA per pair of 16-column strips over the whole K (M <= 64),
  *   6 = skinny, persistent, TMA-fed, 64-row weight tiles over the whole K (M <= 64 and
  *       N / 64 >= SMs / 2, else SWIFTKV_EUNSUPPORTED)

@@ -368,11 +368,10 @@ cudaError_t prefill_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_
                       int max_pages, int num_pages, const int* cu, const int* ctx, const int* tiles,
                       int num_tiles, int n_q, int n_kv, bf16* out, int ldo, cudaStream_t stream) {
   constexpr int smem = (ABQ + 4 * ABKV) * D * 2;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_prefill_kernel<D>), smem, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   dim3 grid(num_tiles, n_q);

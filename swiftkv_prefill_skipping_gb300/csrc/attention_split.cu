@@ -613,11 +613,10 @@ cudaError_t split_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_po
                     int n_q, int n_kv, bf16* out, int ldo, int num_sms, cudaStream_t stream) {
   constexpr int smem = Sp<D>::SMEM;
   static_assert(smem <= 227 * 1024, "rings must fit in shared memory");
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_split_kernel<D>), smem, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const int total = plan.num_units * n_kv;
@@ -638,12 +637,10 @@ cudaError_t split_fp8_d(const bf16* q, int ldq, const uint8_t* k8, const uint8_t
   constexpr int smem = Sp8<D>::SMEM;
   static_assert(smem <= 227 * 1024, "rings must fit in shared memory");
   static_assert(Sp8<D>::STAGE % 16 == 0, "ring slots must keep 16-byte alignment");
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(attn_split_fp8_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_split_fp8_kernel<D>), smem, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const int total = plan.num_units * n_kv;

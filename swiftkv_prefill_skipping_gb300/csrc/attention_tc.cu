@@ -382,11 +382,10 @@ cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf1
       !tma_map_bf16_2d(&mk, k_pool, pool_rows, D, D, 64, kPageSize, true) ||
       !tma_map_bf16_2d(&mv, v_pool, pool_rows, D, D, 64, kPageSize, true))
     return cudaErrorNotSupported;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(attn_tc_kernel), SMEM_BYTES, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   dim3 grid(num_tiles, n_q);

@@ -365,11 +365,10 @@ static cudaError_t launch_gemv_mb(const bf16* A, int lda, const bf16* B, int K, 
                                   cudaStream_t stream) {
   constexpr int smem = 4 * GV_STAGES * (32 + MB * 16) * GV_LD * 2;
   static_assert(4 * MB * 16 * 32 * 4 <= smem, "reduction buffer must fit the rings");
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<MB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_kernel<MB>), smem, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   gemv_kernel<MB><<<ep.N / 32, 128, smem, stream>>>(A, lda, B, K, ep);
   return cudaGetLastError();
@@ -399,12 +398,10 @@ size_t skinny_scratch_bytes(int M, int N, int K, int num_sms) {
 
 cudaError_t launch_gemm_tiled(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
                               cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kTiledSmem);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm_tiled_kernel), kTiledSmem, smem_attr);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   dim3 grid(ep.N / TN, (ep.M + TM - 1) / TM);
   gemm_tiled_kernel<<<grid, TTHREADS, kTiledSmem, stream>>>(A, lda, B, K, ep);
@@ -415,12 +412,10 @@ template <int MB>
 static cudaError_t launch_skinny_mb(const bf16* A, int lda, const bf16* B, int K, int M, int N,
                                     int splits, float* part, cudaStream_t stream) {
   constexpr int smem = SSTAGES * (MB * 16 + SN) * SLD * 2;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_skinny_kernel<MB>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm_skinny_kernel<MB>), smem, smem_attr);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   dim3 grid(N / SN, splits);
   gemm_skinny_kernel<MB><<<grid, STHREADS, smem, stream>>>(A, lda, B, K, M, N, K / splits, part);

@@ -61,11 +61,6 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   nt = r / gm;
 }
 
-// MC: CTAs per cluster along M. With MC == 2 the two CTAs of a cluster compute m-tiles
-// 2p and 2p+1 of the same n-tile; each loads its own A tile and half of the shared B tile,
-// multicast into both CTAs, so each SM reads 32 KB instead of 48 KB from L2 per stage. A
-// ring stage is refilled only when both CTAs' MMAs have released it.
-template <int MC>
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                                                              const __grid_constant__ CUtensorMap tmB,
                                                              EpiParams ep, int K, int* status) {
@@ -78,11 +73,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   const int M = ep.M, N = ep.N;
   const int m_tiles = (M + BM - 1) / BM;
   const int n_tiles = (N + BN - 1) / BN;
-  // scheduling unit: MC vertically adjacent m-tiles of one n-tile
-  const int m_units = (m_tiles + MC - 1) / MC;
-  const int num_units = m_units * n_tiles;
-  const int crank = MC > 1 ? (int)cluster_ctarank() : 0;
-  const int first_unit = blockIdx.x / MC, unit_stride = gridDim.x / MC;
+  const int num_units = m_tiles * n_tiles;
+  const int first_unit = blockIdx.x, unit_stride = gridDim.x;
   const int kblocks = K / BK;
   volatile int* abort_flag = &ctl->abort;
 
@@ -94,7 +86,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full(s), 1);
-      mbar_init(empty(s), MC);
+      mbar_init(empty(s), 1);
       ctl->pending[s] = -1;
     }
     for (int a = 0; a < 2; ++a) {
@@ -116,7 +108,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   }
   tc_fence_before();
   __syncthreads();
-  if (MC > 1) cluster_sync();  // the peer's barriers exist before anything is multicast to it
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
@@ -125,22 +116,15 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       int stage = 0;
       uint32_t phase = 0;
       for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride) {
-        int mu, nt;
-        tile_coords(u, m_units, n_tiles, mu, nt);
-        const int mt = mu * MC + crank;
+        int mt, nt;
+        tile_coords(u, m_tiles, n_tiles, mt, nt);
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
           mbar_expect_tx(full(stage), STAGE_BYTES);
           ctl->pending[stage] = (int)phase;
           const uint32_t sa = sbase + stage * STAGE_BYTES;
           tma_load_2d(sa, &tmA, kb * BK, mt * BM, full(stage));
-          if (MC == 1) {
-            tma_load_2d(sa + A_BYTES, &tmB, kb * BK, nt * BN, full(stage));
-          } else {
-            constexpr int part = BN / MC;
-            tma_load_2d_mc(sa + A_BYTES + crank * part * BK * 2, &tmB, kb * BK, nt * BN + crank * part, full(stage),
-                           (uint16_t)((1u << MC) - 1));
-          }
+          tma_load_2d(sa + A_BYTES, &tmB, kb * BK, nt * BN, full(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -170,8 +154,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc_mma(d, sdesc(sa + kk * 32), sdesc(sa + A_BYTES + kk * 32), IDESC, (kb | kk) != 0);
-          if (MC == 1) tc_commit(empty(stage));
-          else tc_commit_mc(empty(stage), (uint16_t)((1u << MC) - 1));
+          tc_commit(empty(stage));
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -188,9 +171,8 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
     for (int u = first_unit; u < num_units; u += unit_stride, ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
-      int mu, nt;
-      tile_coords(u, m_units, n_tiles, mu, nt);
-      const int mt = mu * MC + crank;
+      int mt, nt;
+      tile_coords(u, m_tiles, n_tiles, mt, nt);
       if (!mbar_wait(tfull(acc), aph, abort_flag)) break;
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
@@ -233,7 +215,6 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
   tc_fence_after();
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
-  if (MC > 1) cluster_sync();  // no CTA leaves while its peer may still multicast into it
 }
 
 
@@ -244,7 +225,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
 // (32 KB per stage instead of 48 KB), so each SM writes 64 B/clk into shared memory and the
 // tensor core reads 64 B/clk from it: together within shared-memory bandwidth, where the
 // 1-SM 128 x 256 tile needs ~192 B/clk. The even CTA issues the MMAs; both CTAs' TMA loads
-// complete on its ring barriers; its commits are multicast to both CTAs; each CTA reads
+// complete on its ring barriers; each of its commits arrives on the barrier of both CTAs; each CTA reads
 // its own 128 accumulator rows from its own TMEM and releases them on the even CTA's barrier.
 constexpr int P_STAGES = 6;
 constexpr int P_STAGE_BYTES = 2 * BM * BK * 2;  // A half 16 KB + B half 16 KB
@@ -427,42 +408,24 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_pair_kernel(const __grid_c
 
 }  // namespace
 
-template <int MC>
-static cudaError_t launch_tc_mc(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& ep, int K,
-                                int num_sms, int* status, cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_kernel<MC>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+static cudaError_t launch_tc_single(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& ep, int K,
+                                    int num_sms, int* status, cudaStream_t stream) {
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm_tc_kernel), SMEM_BYTES, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
-  const int m_units = ((ep.M + BM - 1) / BM + MC - 1) / MC;
-  const int units = m_units * ((ep.N + BN - 1) / BN);
-  const int clusters = units < num_sms / MC ? units : num_sms / MC;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * MC);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = MC;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<MC>, ta, tb, ep, K, status);
+  const int units = ((ep.M + BM - 1) / BM) * ((ep.N + BN - 1) / BN);
+  gemm_tc_kernel<<<units < num_sms ? units : num_sms, THREADS, SMEM_BYTES, stream>>>(ta, tb, ep, K, status);
+  return cudaSuccess;
 }
 
 static cudaError_t launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, const EpiParams& ep, int K,
                                   int num_sms, int* status, cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemm_tc_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemm_tc_pair_kernel), P_SMEM_BYTES, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int m_units = ((ep.M + BM - 1) / BM + 1) / 2;
   const int units = m_units * ((ep.N + BN - 1) / BN);
@@ -487,14 +450,14 @@ cudaError_t launch_gemm_tc(const bf16* A, int lda, const bf16* B, int K, const E
   if (ep.M < 1 || ep.N < 1 || K < BK || K % BK || ep.N % 128 || lda % 8 ||
       (reinterpret_cast<uintptr_t>(A) & 15) || (reinterpret_cast<uintptr_t>(B) & 15))
     return cudaErrorNotSupported;
+  if (mode != 0 && mode != 2) return cudaErrorNotSupported;
   CUtensorMap ta, tb;
   const int b_rows = mode == 0 ? BN : BN / 2;
   if (!tma_map_bf16_2d(&ta, A, ep.M, K, lda, BK, BM, true) || !tma_map_bf16_2d(&tb, B, ep.N, K, K, BK, b_rows, true))
     return cudaErrorNotSupported;
   cudaError_t e;
   if (mode == 2) e = launch_tc_pair(ta, tb, ep, K, num_sms, status, stream);
-  else if (mode == 1) e = launch_tc_mc<2>(ta, tb, ep, K, num_sms, status, stream);
-  else e = launch_tc_mc<1>(ta, tb, ep, K, num_sms, status, stream);
+  else e = launch_tc_single(ta, tb, ep, K, num_sms, status, stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -228,11 +228,10 @@ cudaError_t launch_mb(const bf16* A, int lda, const bf16* W, int K, const EpiPar
   if (!tma_map_bf16_2d(&ma, A, ep.M, K, lda, GT_BK, G::A_ROWS, true) ||
       !tma_map_bf16_2d(&mw, W, ep.N, K, K, GT_BK, TR / 2, true))
     return cudaErrorNotSupported;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel<MB, TR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static PerDeviceOnce smem_attr;
+  {
+    cudaError_t e = set_max_dynamic_smem(reinterpret_cast<const void*>(gemv_tma_kernel<MB, TR>), smem, smem_attr);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int tiles = ep.N / TR;
   cudaLaunchConfig_t cfg = {};

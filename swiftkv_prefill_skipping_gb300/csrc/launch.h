@@ -5,11 +5,30 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <vector>
 
 #include "common.cuh"
 
 namespace skv {
+
+// Raises a kernel's dynamic shared-memory limit on the current device, once per device: the
+// attribute belongs to the device that is current when it is set, so a process driving
+// several GPUs sets it on each. Safe to call from several threads (setting it twice is
+// harmless; the per-device bit is atomic). Devices past 63 set it on every call.
+struct PerDeviceOnce {
+  std::atomic<uint64_t> done{0};
+};
+inline cudaError_t set_max_dynamic_smem(const void* func, int bytes, PerDeviceOnce& once) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (once.done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) once.done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Records `msg` as the calling thread's swiftkv_last_error() and returns `code`.
 int set_error(int code, const char* msg);
@@ -29,8 +48,8 @@ cudaError_t launch_gemv_tma(const bf16* A, int lda, const bf16* W, int K, const 
                             int* status, cudaStream_t stream);
 // tcgen05 (TMEM accumulator, TMA-fed) GEMM; returns cudaErrorNotSupported if the shape is not
 // handled, so the caller can fall back to launch_gemm_tiled.
-// mode 0: one CTA per 128 x 256 tile; 1: CTA pairs share the weight tile through TMA
-// multicast; 2: CTA pairs run tcgen05.mma.cta_group::2 on 256 x 256 tiles.
+// mode 0: one CTA per 128 x 256 tile; 2: CTA pairs run tcgen05.mma.cta_group::2 on
+// 256 x 256 tiles (any other mode: cudaErrorNotSupported).
 cudaError_t launch_gemm_tc(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
                            int num_sms, int* status, cudaStream_t stream, int mode = 0);
 

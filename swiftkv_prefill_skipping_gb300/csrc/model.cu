@@ -758,6 +758,7 @@ int swiftkv_set_attention_impl(swiftkv_model* m, int impl) {
 int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,
                       swiftkv_stream stream) {
   if (!A || !B || !C || M < 1 || N < 1 || K < 1) return fail(SWIFTKV_EINVAL, "bad gemm arguments");
+  if (impl < 0 || impl > 6 || impl == 3) return fail(SWIFTKV_EINVAL, "gemm impl %d", impl);
   if (K % 64 || N % 128) return fail(SWIFTKV_EUNSUPPORTED, "gemm needs K %% 64 == 0 and N %% 128 == 0");
   cudaStream_t s = (cudaStream_t)stream;
   int dev = 0, sms = 0;
@@ -780,8 +781,8 @@ int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int 
   cudaError_t e = cudaSuccess;
   const bf16* a = static_cast<const bf16*>(A);
   const bf16* b = static_cast<const bf16*>(B);
-  if (impl == 0 || impl == 3 || impl == 4) {
-    e = launch_gemm_tc(a, K, b, K, ep, sms, st, s, impl == 0 ? 0 : (impl == 3 ? 1 : 2));
+  if (impl == 0 || impl == 4) {
+    e = launch_gemm_tc(a, K, b, K, ep, sms, st, s, impl == 0 ? 0 : 2);
   } else if (impl == 1) {
     e = launch_gemm_tiled(a, K, b, K, ep, s);
   } else if (impl == 5) {

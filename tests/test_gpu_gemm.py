@@ -34,7 +34,7 @@ def _run(impl, M, N, K, seed=0):
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-@pytest.mark.parametrize("impl", [0, 1, 3, 4])
+@pytest.mark.parametrize("impl", [0, 1, 4])
 def test_gemm_matches_torch_fp32(impl, M, N, K):
     import torch
     Cm, ref = _run(impl, M, N, K)
