@@ -199,6 +199,8 @@ def oracle_sample_time(w, weights, tokens):
 
 
 L2_BYTES = 129e6  # GB300 L2
+PROFILED_PASS_NOTE = ("per-launch CUDA events on the launch stream over a second pass of the same K steps, "
+                      "right after the uninstrumented timed region that gives `value`")
 
 
 def l2_note(shape) -> str:
@@ -346,21 +348,36 @@ def run_ours(args, w, rank, world, local_rank):
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.4)
-    binding.check(binding.lib().swiftkv_profile_begin(model.handle))
+    # the timed region: K steps with no instrumentation
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
-    entries = (binding.ProfileEntry * 64)()
-    n_ent = binding.check(binding.lib().swiftkv_profile_end(model.handle, entries, 64))
     clocks = sampler.stop()
     barrier()
     ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     ms_per_step = ms / args.steps
     T_all = sum_over_ranks(T, world, dev)
     value = whole_job_throughput(T_all, args.steps, ms / 1e3)
+
+    # where the time goes: the same K steps again, every launch bracketed by CUDA events on
+    # its own stream (swiftkv_profile_begin/end); only the per-kernel breakdown and the
+    # roofline come from this pass, never `value`
+    binding.check(binding.lib().swiftkv_profile_begin(model.handle))
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    p0.record(stream)
+    for _ in range(args.steps):
+        step()
+    p1.record(stream)
+    torch.cuda.synchronize()
+    entries = (binding.ProfileEntry * 64)()
+    n_ent = binding.check(binding.lib().swiftkv_profile_end(model.handle, entries, 64))
+    ms_profiled = p0.elapsed_time(p1) / args.steps
+    st = model.status()
+    if st != 0:
+        raise RuntimeError(f"device status word {st} after the timed steps")
 
     prof = {}
     for i in range(n_ent):
@@ -387,13 +404,15 @@ def run_ours(args, w, rank, world, local_rank):
                         "unit": "TFLOP/s", "frac": ach / peak_sus,
                         "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step)",
                         "traffic": traffic_per_launch(dom_name), "launch_avg_ms": d["ms"] / d["calls"],
-                        "algorithmic_flops_per_launch": d["flops"] / d["calls"]}
+                        "algorithmic_flops_per_launch": d["flops"] / d["calls"],
+                        "timing": PROFILED_PASS_NOTE}
         else:
             ach = d["bytes"] / (d["ms"] / 1e3) / 1e9
             roofline = {"kernel": dom_name, "bound": "hbm", "achieved": ach, "peak": float(peaks["hbm_gbs"]),
                         "unit": "GB/s", "frac": ach / float(peaks["hbm_gbs"]),
                         "peak_source": f"{peak_src} hbm_gbs", "traffic": traffic_per_launch(dom_name),
-                        "launch_avg_ms": d["ms"] / d["calls"]}
+                        "launch_avg_ms": d["ms"] / d["calls"], "algorithmic_bytes_per_launch": d["bytes"] / d["calls"],
+                        "timing": PROFILED_PASS_NOTE}
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     e2e = None
@@ -498,6 +517,7 @@ def run_ours(args, w, rank, world, local_rank):
             "roofline": roofline,
             "step_roofline": step_roofline(prof, args.steps, ms_per_step, peak_sus,
                                            float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))),
+            "ms_per_step_profiled": ms_profiled,
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches,
             "kv_cache": kv_cache_info(model, w),
             "decode": decode,
@@ -515,8 +535,9 @@ def run_ours(args, w, rank, world, local_rank):
 def step_roofline(prof: dict, steps: int, ms_per_step: float, peak_tflops: float, hbm_gbs: float) -> dict:
     """End-to-end roofline of one step: the sum over kernel classes of
     max(FLOPs / bf16 peak, bytes / HBM bandwidth), from the algorithmic FLOPs and bytes each
-    class records, against the measured step time. Classes that record neither (plan,
-    host uploads) count zero; the single-row attention records FLOPs only."""
+    class records, against the measured (uninstrumented) step time. Classes that record
+    neither (plan, host uploads) count zero; attention classes record both their FLOPs and
+    the K/V, Q and output bytes they must move."""
     t = 0.0
     per = {}
     for name, v in prof.items():
@@ -590,6 +611,18 @@ def traffic_per_launch(kernel: str):
     return b if h.hexdigest()[:16] == digest else None
 
 
+def relaunch_ranks(n: int) -> int:
+    """`bench.py --gpus N` outside torchrun: start N ranks on this node (one per GPU) through
+    torch.distributed.run on 127.0.0.1 and return its exit status."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.abspath(__file__), *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -605,9 +638,18 @@ def main():
                     help="greedy decode steps timed after the prefill (default: the workload's own)")
     args = ap.parse_args()
     w = synth.WORKLOADS[args.workload]
+    if args.gpus < 1:
+        log(f"--gpus {args.gpus}: need at least one GPU")
+        return 2
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return relaunch_ranks(args.gpus)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        log(f"--gpus {args.gpus} does not match WORLD_SIZE={world}: launch one rank per GPU "
+            f"(torchrun --nproc-per-node {args.gpus}) or pass --gpus {world}")
+        return 2
     if args.impl == "reference":
         return run_reference(args, w, rank, world)
     if world > 1:

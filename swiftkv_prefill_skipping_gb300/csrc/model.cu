@@ -308,6 +308,11 @@ int upload_split(Ctx& x, const HostSplit& h, int* dst, SplitPlan* p) {
   return SWIFTKV_OK;
 }
 
+// Bytes of one key's K and V vectors over every KV head in a cache (codes + scales for FP8).
+double kv_bytes_per_key(const swiftkv_model* m, bool fp8) {
+  return 2.0 * m->cfg.n_kv * (fp8 ? m->cfg.d_head + 4.0 : 2.0 * m->cfg.d_head);
+}
+
 cudaEvent_t prof_event(swiftkv_model* m) {
   if (m->ev_used == m->ev_pool.size()) {
     cudaEvent_t e;
@@ -381,7 +386,7 @@ int norm(Ctx& x, const float* src, const int* rows, int T, const float* gamma, b
 // Attention output + O projection + MLP of layer j for rows [0, M) of (xres, q), reading
 // the layer's cache; `prefill` selects the varlen prompt kernel, else one query per row.
 int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, bf16* hb, bool prefill,
-               const int* qpos, int ntiles, const char* gname, double attn_flops) {
+               const int* qpos, int ntiles, const char* gname, double attn_flops, double attn_bytes) {
   swiftkv_model* m = x.m;
   const auto& c = m->cfg;
   const LayerW& L = m->layers[j];
@@ -414,7 +419,7 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   {
   Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode",
           prefill ? (ntiles > 0) + (x.nshort > 0 ? launches(x.sp_short) : 0) : launches(x.sp_rows), attn_flops,
-          0.0);
+          attn_bytes);
   if (prefill && x.tc_attn && m->attn_impl == 0)
     e = launch_attention_prefill_tc2(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
                                      x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
@@ -933,12 +938,18 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
     CK(cudaMemcpyAsync(x.w.tokens, tokens, (size_t)T * 4, cudaMemcpyHostToDevice, s));
     tok = x.w.tokens;
   }
-  double attn_flops = 0, tail_keys = 0;  // causal score/PV flops; keys seen by the last rows
+  // algorithmic attention work per layer: causal score/PV flops; bytes = Q and O rows plus
+  // every key's K and V vectors of each KV head read once (prompt rows); the last rows read
+  // their sequence's keys once per layer
+  double attn_flops = 0, tail_keys = 0;
   for (int i = 0; i < P; ++i) {
     const double n = cu[i + 1] - cu[i], c0 = ctx ? ctx[i] : 0;
     attn_flops += 4.0 * m->cfg.n_q * m->cfg.d_head * (n * c0 + n * (n + 1) / 2);
     tail_keys += c0 + n;
   }
+  const double kv_key_bytes = kv_bytes_per_key(m, x.fp8);
+  const double attn_bytes = tail_keys * kv_key_bytes + 2.0 * T * m->Nq * 2;
+  const double tail_bytes = tail_keys * kv_key_bytes + 2.0 * P * m->Nq * 2;
   {
   Prof pr(m, s, "plan", 1 + (P + 1 + kBlobInts - 1) / kBlobInts + ((int)tiles.size() + kBlobInts - 1) / kBlobInts +
           (4 * m->C + kBlobInts - 1) / kBlobInts + (ctx ? (P + kBlobInts - 1) / kBlobInts : 0) +
@@ -982,7 +993,7 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
     }
     RET(qkv(x, j, T, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_layers"));
     RET(layer_rest(x, j, T, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, true, nullptr, (int)tiles.size(),
-                   "gemm_layers", attn_flops));
+                   "gemm_layers", attn_flops, attn_bytes));
   }
   // caches of every skipped layer / AcrossKV group from x_l
   if (m->G > 0) RET(wide_kv(x, T, x.w.x, x.w.u, x.w.positions, x.w.slots));
@@ -991,7 +1002,7 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   for (int j = m->l; j < c.L; ++j) {
     RET(qkv(x, j, P, x.w.ut, x.w.qt, x.w.last_pos, nullptr, "gemm_tail"));
     RET(layer_rest(x, j, P, x.w.xt, x.w.qt, x.w.at, x.w.ut, x.w.ht, false, x.w.last_pos, 0, "gemm_tail",
-                   4.0 * c.n_q * c.d_head * tail_keys));
+                   4.0 * c.n_q * c.d_head * tail_keys, tail_bytes));
     RET(norm(x, x.w.xt, nullptr, P, j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final, x.w.ut, nullptr));
   }
   EpiParams el = epi_base(x, EPI_STORE_F32, P, c.vocab);
@@ -1041,7 +1052,11 @@ int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   x.s = s;
   x.kv = kv;
   std::vector<int> nk(B);
-  for (int b = 0; b < B; ++b) nk[b] = seq_lens[b] + 1;
+  double dec_keys = 0;
+  for (int b = 0; b < B; ++b) {
+    nk[b] = seq_lens[b] + 1;
+    dec_keys += nk[b];
+  }
   const HostSplit hs = make_split(nk);
   x.fp8 = kv->kv_dtype == 1;
   RET(ensure_workspace(m, B, B, m->C, 1, skinny_part_bytes(m, B), &x.w, hs.ints(),
@@ -1060,7 +1075,8 @@ int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* 
       RET(norm(x, x.w.x, nullptr, B, m->layers[j].g_attn, x.w.u, nullptr));
     }
     RET(qkv(x, j, B, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_decode"));
-    RET(layer_rest(x, j, B, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, false, x.w.positions, 0, "gemm_decode", 0.0));
+    RET(layer_rest(x, j, B, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, false, x.w.positions, 0, "gemm_decode",
+                   4.0 * c.n_q * c.d_head * dec_keys, dec_keys * kv_bytes_per_key(m, x.fp8) + 2.0 * B * m->Nq * 2));
     RET(norm(x, x.w.x, nullptr, B, j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final, x.w.u, nullptr));
   }
   EpiParams el = epi_base(x, EPI_STORE_F32, B, c.vocab);

@@ -10,10 +10,10 @@ ARGS = [sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_l
         "--ref-sample-tokens", "16"]
 
 
-def _run(env_extra=None):
-    env = dict(os.environ)
+def _run(env_extra=None, extra_args=()):
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
     env.update(env_extra or {})
-    return subprocess.run(ARGS, capture_output=True, text=True, cwd=ROOT, timeout=600, env=env)
+    return subprocess.run(ARGS + list(extra_args), capture_output=True, text=True, cwd=ROOT, timeout=600, env=env)
 
 
 def test_reference_arm_prints_the_contract_line():
@@ -36,8 +36,31 @@ def test_reference_arm_prints_the_contract_line():
 
 
 def test_reference_arm_other_ranks_exit_quietly():
-    out = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    out = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"}, ["--gpus", "2"])
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_gpus_flag_must_match_the_launched_ranks():
+    """A --gpus count that disagrees with the ranks torchrun started is refused, on both arms,
+    before any work."""
+    for impl in ("reference", "ours"):
+        env = {"RANK": "0", "WORLD_SIZE": "2", "LOCAL_RANK": "0"}
+        out = subprocess.run([sys.executable, "bench.py", "--impl", impl, "--gpus", "1"], capture_output=True,
+                             text=True, cwd=ROOT, timeout=600,
+                             env={**{k: v for k, v in os.environ.items()}, **env})
+        assert out.returncode == 2, (impl, out.returncode, out.stderr[-2000:])
+        assert "does not match WORLD_SIZE" in out.stderr and out.stdout.strip() == ""
+
+
+def test_gpus_flag_without_torchrun_launches_that_many_ranks():
+    """bench.py --gpus 2 run directly starts two ranks itself; rank 0 alone prints the line,
+    and it reports the two GPUs (the reference arm needs no GPU, so this runs on the CPU)."""
+    out = _run(None, ["--gpus", "2"])
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, out.stdout
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2
 
 
 def test_l2_note_of_the_timed_workloads():
