@@ -214,7 +214,7 @@ def l2_note(shape) -> str:
     return f"weights {weight_bytes / 1e6:.1f} MB fit in L2: a parity configuration, not a timing one"
 
 
-def workload_config(w, batch):
+def workload_config(w, batch, norm_fusion=0):
     if w.mixed:
         chunks = ", ".join(f"{n}@{c}" for c, n in w.mix_chunks)
         return {
@@ -227,6 +227,7 @@ def workload_config(w, batch):
             "l": w.l, "g": w.g, "L": w.shape.L, "kv_cache": w.kv_dtype,
             "l2": l2_note(w.shape),
             "parallelism": "replicas (one independent serving step per GPU)",
+            "norm_fusion": norm_fusion,
         }
     return {
         "workload": f"{w.name}: {w.shape.name} shape bf16 random-init N(0,0.02), SwiftKV l={w.l}, "
@@ -236,6 +237,7 @@ def workload_config(w, batch):
         "l": w.l, "g": w.g, "L": w.shape.L, "kv_cache": w.kv_dtype,
         "l2": l2_note(w.shape),
         "parallelism": "replicas (one independent prefill per GPU)",
+        "norm_fusion": norm_fusion,
     }
 
 
@@ -310,6 +312,7 @@ def run_ours(args, w, rank, world, local_rank):
             model.load_globals(wts)
             if want_cpu:
                 raw_globals = wts
+    binding.check(binding.lib().swiftkv_set_norm_fusion(model.handle, args.norm_fusion))
     log(f"[ours] rank {rank}: weights generated + loaded in {time.time() - t0:.1f}s "
         f"({model.memory()[0] / 2**30:.1f} GiB on device)")
     kv = api.KVCache(model, batch.num_pages, batch.block_table, device=dev, dtype=w.kv_dtype)
@@ -508,7 +511,7 @@ def run_ours(args, w, rank, world, local_rank):
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded random-init weights and token ids; no dataset)",
-            "config": workload_config(w, batch),
+            "config": workload_config(w, batch, args.norm_fusion),
             "dense_equiv_tflops": dense_tflops,
             "dense_equiv_frac_of_peak": {"burst": dense_tflops / peak_burst, "sustained": dense_tflops / peak_sus,
                                          "peak_source": peak_src},
@@ -634,6 +637,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-sample-tokens", type=int, default=512)
     ap.add_argument("--ref-sample-tokens", type=int, default=128)
+    ap.add_argument("--norm-fusion", type=int, choices=(0, 1), default=0,
+                    help="prompt rows' RMSNorm inside the GEMM epilogues (1) or as its own pass (0, default)")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="greedy decode steps timed after the prefill (default: the workload's own)")
     args = ap.parse_args()

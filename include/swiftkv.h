@@ -226,6 +226,31 @@ int swiftkv_memory(const swiftkv_model* m, size_t* weight_bytes, size_t* workspa
  * cp.async one (impl 5). */
 int swiftkv_set_gemm_impl(swiftkv_model* m, int impl);
 
+/* How the rows that run layers one token at a time (the last-token tail of the skipped
+ * layers, decode tokens) go through a layer after its attention. 1 (default) = one launch per
+ * GEMM and per RMSNorm, each GEMM a programmatic dependent that starts streaming its weights
+ * while the kernel before it finishes. 0 = one cooperative persistent launch per layer: O
+ * (+residual), RMSNorm, gate/up (+SwiGLU), down (+residual), the next RMSNorm and the next
+ * layer's Q (tail) or Q/K/V (decode), separated by grid-wide barriers, each SM streaming its
+ * share of all those weights back to back; measured slower than 1 at the Qwen2.5-14B decode
+ * shape (its ~3 us of prefetched weights per SM do not cover a barrier and a norm phase), kept
+ * as a cross-check. Both give every row the same kernels' arithmetic order; where a device
+ * cannot take the cooperative launch, 0 falls back to 1. Returns SWIFTKV_EINVAL for other
+ * values. */
+int swiftkv_set_rows_impl(swiftkv_model* m, int impl);
+
+/* Where the RMSNorm of the prompt rows runs (batches of more than 64 rows on the tcgen05
+ * GEMMs). 0 (default) = a separate RMSNorm pass before each GEMM that reads normalised rows:
+ * the GEMM input is bf16(gamma * x / rms(x)), rounded where the model definition rounds it.
+ * 1 = inside the GEMM epilogues: the O and down GEMMs also write bf16(gamma * x) and per-tile
+ * sums of squares of x, and the next GEMM scales its fp32 accumulators by the row's 1/rms, so
+ * no pass re-reads the fp32 residual stream (about 3 % faster on the Llama-3.1-8B-shaped
+ * prefill). Mode 1 rounds the GEMM input at another point (gamma * x instead of
+ * gamma * x / rms), so its results move by about one bf16 ulp against mode 0 and the
+ * definition. The tail and decode rows always use the exact separate pass.
+ * Returns SWIFTKV_EINVAL for other values. */
+int swiftkv_set_norm_fusion(swiftkv_model* m, int on);
+
 /* Kernel family for the prompt tokens' attention: 0 = tcgen05 with TMA-staged paged K/V,
  * persistent, two 128-row query tiles per work item (default; d_head 128), 1 = warp-level
  * mma.sync (always used for d_head 64), 2 = tcgen05 with one 128-row query tile per CTA
@@ -247,6 +272,21 @@ int swiftkv_set_attention_impl(swiftkv_model* m, int impl);
  * Requires K % 64 == 0 and N % 128 == 0. */
 int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,
                       swiftkv_stream stream);
+
+/* Test-only entry for the bounded waits of the tcgen05 kernels (no model needed; the pages
+ * define no such operation: it checks this library's own failure handling). Every mbarrier
+ * wait in the library gives up after a time limit instead of spinning forever; this runs
+ * that expiry path on purpose with a short limit: one CTA allocates TMEM, one warp waits
+ * on a barrier whose producer issues nothing, bounded by limit_ns nanoseconds of the GPU
+ * clock; when the limit passes the CTA raises SWIFTKV_STATUS_TIMEOUT in *status, a second
+ * waiting warp leaves its wait on seeing the abort, TMEM is freed and the kernel returns.
+ * No fault, no endless wait, and the context stays usable for the next call.
+ *   status      device int, OR-ed with SWIFTKV_STATUS_TIMEOUT (caller-owned)
+ *   elapsed_ns  device unsigned 64-bit or NULL: nanoseconds the expired wait took
+ *   limit_ns    1000 .. 100000000, else SWIFTKV_EINVAL
+ * Enqueued on `stream`; returns SWIFTKV_OK once launched, SWIFTKV_ECUDA on a launch error. */
+int swiftkv_selftest_wait_timeout(int* status, unsigned long long* elapsed_ns, long long limit_ns,
+                                  swiftkv_stream stream);
 
 /* swiftkv_gemm_bf16 with impl 2 (skinny split-K, M <= 64) for callers that may not
  * allocate device memory, e.g. a host that reserves the GPU's memory for its own pools

@@ -12,10 +12,10 @@ Sources (page titles, sections):
       for Inference".
 
 Precision. The pages run every model in BF16 ([S] section 5, hardware). The
-oracle therefore keeps weights, the KV cache and every input of a linear layer
-or attention contraction at bfloat16 values (``bf16``), and does all other
-arithmetic (norms, accumulations, RoPE angles, softmax, residual stream) in
-float64.
+oracle therefore keeps weights, the KV cache, the queries and every input of a
+linear layer at bfloat16 values (``bf16``), and does all other arithmetic
+(norms, accumulations, RoPE angles, softmax and its weights, residual stream)
+in float64.
 
 Layer indices are 0-based in code: layers 0..l-1 run in full (the pages'
 layers 1..l), layers l..L-1 are skipped for prompt tokens, and "x_l" (the
@@ -42,45 +42,42 @@ def bf16(x) -> np.ndarray:
     return np.ldexp(np.rint(m * 256.0) / 256.0, e)
 
 
+# Precision mode. float64 everywhere is the definition. Tests evaluate the same model with
+# every accumulation in float32 - the linear layers' dot products, the attention scores, the
+# softmax normaliser and the weighted sum of V, the RMSNorm mean of squares - the GPU path's
+# declared arithmetic (bfloat16 operands, float32 accumulation), to measure the rounding floor
+# any implementation with that precision faces against the definition. Pointwise functions
+# (exp, silu, RoPE angles) and the residual stream stay float64; nothing is rounded to a
+# format narrower than float32 beyond the model's own bfloat16 points.
+_LINEAR_ACC = [F64]
+
+
 def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * gamma."""
     x = np.asarray(x, dtype=F64)
-    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma, F64)
-
-
-# Precision modes. float64 everywhere is the definition. Tests evaluate the same model at
-# a lower declared precision to measure the rounding floor any implementation with that
-# precision faces against the definition:
-#   _LINEAR_ACC  accumulation type of the linear layers' dot products;
-#   _P_ROUND     rounding applied to the unnormalised softmax weights before they meet V
-#                (None = exact; the normalising sum always uses the unrounded weights).
-_LINEAR_ACC = [F64]
-_P_ROUND = [None]
+    acc = _LINEAR_ACC[-1]
+    if acc is F64:
+        ms = np.mean(x * x, axis=-1, keepdims=True)
+    else:  # squares and their sum accumulated in the precision mode's type
+        ms = np.mean((x * x).astype(acc), axis=-1, keepdims=True, dtype=acc).astype(F64)
+    return x / np.sqrt(ms + eps) * np.asarray(gamma, F64)
 
 
 class accumulate_in:
-    """Context manager: run the linear layers' dot products in `dtype` (inputs are
-    bfloat16 values, exact in float32) and, if `p_round` is given, round the softmax
-    weights with it before the weighted sum of V; everything else unchanged."""
+    """Context manager: run every accumulation (linear layers, attention scores, softmax sum
+    and weighted sum of V, RMSNorm mean of squares) in `dtype`; inputs that are bfloat16
+    values stay exact; everything else unchanged."""
 
-    def __init__(self, dtype, p_round=None):
+    def __init__(self, dtype):
         self.dtype = dtype
-        self.p_round = p_round
 
     def __enter__(self):
         _LINEAR_ACC.append(self.dtype)
-        _P_ROUND.append(self.p_round)
         return self
 
     def __exit__(self, *exc):
         _LINEAR_ACC.pop()
-        _P_ROUND.pop()
         return False
-
-
-def fp16(x) -> np.ndarray:
-    """Round to the nearest IEEE half-precision value (ties to even), as float64."""
-    return np.asarray(x, dtype=F64).astype(np.float16).astype(F64)
 
 
 def linear(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None,
@@ -129,18 +126,23 @@ def causal_gqa_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.
     allowed = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]
     out = np.empty(q.shape, dtype=F64)
     scale = 1.0 / np.sqrt(F64(d_h))
+    acc = _LINEAR_ACC[-1]
     for h in range(n_q):
         kv = h // grp
-        s = (q[:, h, :] @ k[:, kv, :].T) * scale
+        if acc is F64:
+            s = (q[:, h, :] @ k[:, kv, :].T) * scale
+        else:
+            s = (q[:, h, :].astype(acc) @ k[:, kv, :].T.astype(acc)).astype(F64) * scale
         s = np.where(allowed, s, -np.inf)
         s = s - s.max(axis=1, keepdims=True)
         p = np.exp(s)
-        rnd = _P_ROUND[-1]
-        if rnd is None:
+        if acc is F64:
             p = p / p.sum(axis=1, keepdims=True)
             out[:, h, :] = p @ v[:, kv, :]
-        else:
-            out[:, h, :] = (rnd(p) @ v[:, kv, :]) / p.sum(axis=1, keepdims=True)
+        else:  # unnormalised weights summed and applied to V in the mode's type, then divided
+            pa = p.astype(acc)
+            denom = pa.sum(axis=1, keepdims=True, dtype=acc).astype(F64)
+            out[:, h, :] = (pa @ v[:, kv, :].astype(acc)).astype(F64) / denom
     return out
 
 

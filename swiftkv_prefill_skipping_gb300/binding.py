@@ -27,8 +27,9 @@ STATUS_TIMEOUT = 4
 EXPORTS = ("swiftkv_cache_count", "swiftkv_model_create", "swiftkv_load_layer", "swiftkv_load_globals",
            "swiftkv_load_weights", "swiftkv_prefill", "swiftkv_prefill_host", "swiftkv_forward",
            "swiftkv_decode_step",
-           "swiftkv_status", "swiftkv_memory", "swiftkv_set_gemm_impl", "swiftkv_set_attention_impl", "swiftkv_gemm_bf16",
-           "swiftkv_gemm_skinny_noalloc",
+           "swiftkv_status", "swiftkv_memory", "swiftkv_set_gemm_impl", "swiftkv_set_attention_impl",
+           "swiftkv_set_norm_fusion", "swiftkv_set_rows_impl", "swiftkv_gemm_bf16",
+           "swiftkv_gemm_skinny_noalloc", "swiftkv_selftest_wait_timeout",
            "swiftkv_profile_begin", "swiftkv_profile_end",
            "swiftkv_last_error", "swiftkv_free")
 
@@ -91,8 +92,11 @@ def lib(path: str | None = None):
             L.swiftkv_memory.argtypes = [vp, C.POINTER(sz), C.POINTER(sz)]
             L.swiftkv_set_gemm_impl.argtypes = [vp, i]
             L.swiftkv_set_attention_impl.argtypes = [vp, i]
+            L.swiftkv_set_norm_fusion.argtypes = [vp, i]
+            L.swiftkv_set_rows_impl.argtypes = [vp, i]
             L.swiftkv_gemm_bf16.argtypes = [vp, vp, vp, i, i, i, i, vp, vp]
             L.swiftkv_gemm_skinny_noalloc.argtypes = [vp, vp, vp, i, i, i, vp]
+            L.swiftkv_selftest_wait_timeout.argtypes = [vp, vp, C.c_longlong, vp]
             L.swiftkv_profile_begin.argtypes = [vp]
             L.swiftkv_profile_end.argtypes = [vp, C.POINTER(ProfileEntry), i]
             L.swiftkv_last_error.restype = C.c_char_p

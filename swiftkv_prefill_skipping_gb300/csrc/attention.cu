@@ -3,9 +3,11 @@
 // attn_prefill_kernel: varlen prompts, one CTA per (64-row query tile, query head).
 //   Q tile and double-buffered 64-key K/V tiles are staged in XOR-swizzled shared
 //   memory with cp.async; each (page, head) block of 16 keys is 16*d_head*2
-//   contiguous bytes. S = Q K^T runs on mma.sync bf16 tensor cores, O += P V on fp16
-//   ones (V converted once per tile in shared memory, P kept at fp16 precision), both
-//   with fp32 accumulation; softmax is online (running max / sum in the log2 domain).
+//   contiguous bytes. S = Q K^T and O += P V run on mma.sync bf16 tensor cores with fp32
+//   accumulation; P V takes V in bf16 as cached and P as bf16 high + low parts (two MMAs,
+//   about 15 significant bits of P); softmax is online (running max / sum in the log2
+//   domain). FP8 cache: the pools hold the e4m3 codes as (exact) bf16 values, and each score
+//   is multiplied by its key's scale and each P by its value's scale (float32).
 //   Query tiles arrive longest-first (heaviest causal tiles scheduled first).
 // attn_decode_kernel: one query per sequence (decode tokens and the last prompt
 //   token of the SwiftKV tail), one CTA per (sequence, KV head) computing all query
@@ -24,10 +26,13 @@ constexpr int ABQ = 64, ABKV = 64, ATHREADS = 128;
 template <int D>
 __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     const bf16* __restrict__ q, int ldq, const bf16* __restrict__ kpool, const bf16* __restrict__ vpool,
+    const float* __restrict__ kscale, const float* __restrict__ vscale,
     const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ cu,
     const int* __restrict__ ctx, const int* __restrict__ tiles, int n_q, int n_kv, bf16* __restrict__ out, int ldo,
     float scale_log2) {
   constexpr int CH = D / 8;  // 16-byte chunks per row
+  __shared__ float s_scale[2][2][ABKV];  // FP8 cache: [buffer][key, value][key of the block]
+  const bool fp8 = kscale != nullptr;
   extern __shared__ __align__(128) unsigned char smem[];
   bf16* sQ = reinterpret_cast<bf16*>(smem);
   bf16* sK = sQ + ABQ * D;
@@ -62,6 +67,14 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
       cp_async16(smem_u32(sK + buf * ABKV * D + swz(r, ch)), kpool + off, ok ? 16 : 0);
       cp_async16(smem_u32(sV + buf * ABKV * D + swz(r, ch)), vpool + off, ok ? 16 : 0);
     }
+    if (fp8 && tid < ABKV) {  // this block's scales (keys past the chunk or off the pool: 1)
+      const int key = kb * ABKV + tid;
+      const int page = key < nk ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
+      const bool ok = page >= 0 && page < num_pages;
+      const size_t si = ((size_t)page * n_kv + kvh) * kPageSize + (key & 15);
+      s_scale[buf][0][tid] = ok ? kscale[si] : 1.f;
+      s_scale[buf][1][tid] = ok ? vscale[si] : 1.f;
+    }
   };
 
   const int kv_end = min(nk, c0 + q0 + ABQ);  // keys needed: [0, kv_end)
@@ -95,23 +108,8 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     }
     const bf16* kb_s = sK + (kb & 1) * ABKV * D;
     const bf16* vb_s = sV + (kb & 1) * ABKV * D;
-    // V tile bf16 -> fp16 in place (exact inside fp16's normal range) so that P V can
-    // take P at fp16 precision: P in [0, 1] keeps 11 significant bits instead of 8.
-    {
-      uint4* vt = reinterpret_cast<uint4*>(sV + (kb & 1) * ABKV * D);
-      for (int c = tid; c < ABKV * D / 8; c += ATHREADS) {
-        uint4 raw = vt[c];
-        uint32_t* w = reinterpret_cast<uint32_t*>(&raw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
-          w[e] = pack_f16(fminf(fmaxf(f.x, -65504.f), 65504.f), fminf(fmaxf(f.y, -65504.f), 65504.f));
-        }
-        vt[c] = raw;
-      }
-      __syncthreads();
-    }
-
+    const float* ksc = s_scale[kb & 1][0];
+    const float* vsc = s_scale[kb & 1][1];
     float sc[ABKV / 8][4];
 #pragma unroll
     for (int i = 0; i < ABKV / 8; ++i)
@@ -137,8 +135,9 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         int k = key + e;
-        float va = (k <= pa_ && k < nk) ? sc[nb][e] * scale_log2 : -INFINITY;
-        float vb = (k <= pb_ && k < nk) ? sc[nb][2 + e] * scale_log2 : -INFINITY;
+        const float ks = fp8 ? ksc[k - kb * ABKV] : 1.f;  // FP8: the key's scale
+        float va = (k <= pa_ && k < nk) ? sc[nb][e] * ks * scale_log2 : -INFINITY;
+        float vb = (k <= pb_ && k < nk) ? sc[nb][2 + e] * ks * scale_log2 : -INFINITY;
         sc[nb][e] = va;
         sc[nb][2 + e] = vb;
         mx_a = fmaxf(mx_a, va);
@@ -167,6 +166,16 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     }
     l_a = l_a * al_a + ps_a;
     l_b = l_b * al_b + ps_b;
+    if (fp8) {  // P V with V = code x scale: the value scale rides on P
+#pragma unroll
+      for (int nb = 0; nb < ABKV / 8; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float vs = vsc[nb * 8 + 2 * (lane & 3) + e];
+          sc[nb][e] *= vs;
+          sc[nb][2 + e] *= vs;
+        }
+    }
 #pragma unroll
     for (int db = 0; db < D / 8; ++db) {
       o[db][0] *= al_a;
@@ -177,19 +186,21 @@ __global__ void __launch_bounds__(ATHREADS) attn_prefill_kernel(
     // O += P V
 #pragma unroll
     for (int kk = 0; kk < ABKV / 16; ++kk) {
-      uint32_t pa[4];
-      pa[0] = pack_f16(sc[2 * kk][0], sc[2 * kk][1]);
-      pa[1] = pack_f16(sc[2 * kk][2], sc[2 * kk][3]);
-      pa[2] = pack_f16(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
-      pa[3] = pack_f16(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
+      uint32_t ph[4], pl[4];
+      split_pair_bf16(sc[2 * kk][0], sc[2 * kk][1], ph[0], pl[0]);
+      split_pair_bf16(sc[2 * kk][2], sc[2 * kk][3], ph[1], pl[1]);
+      split_pair_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[2], pl[2]);
+      split_pair_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[3], pl[3]);
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
         uint32_t b0[2], b1[2];
         int row = kk * 16 + (lane & 15);
         int ch = dp * 2 + (lane >> 4);
         ldmatrix_x4_trans(smem_u32(vb_s + swz(row, ch)), b0[0], b0[1], b1[0], b1[1]);
-        mma_f16_16816(o[2 * dp], pa, b0);
-        mma_f16_16816(o[2 * dp + 1], pa, b1);
+        mma_bf16_16816(o[2 * dp], ph, b0);
+        mma_bf16_16816(o[2 * dp + 1], ph, b1);
+        mma_bf16_16816(o[2 * dp], pl, b0);
+        mma_bf16_16816(o[2 * dp + 1], pl, b1);
       }
     }
     __syncthreads();
@@ -364,9 +375,10 @@ __global__ void __launch_bounds__(DTHREADS) attn_decode_kernel(
 }
 
 template <int D>
-cudaError_t prefill_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool, const int* bt,
-                      int max_pages, int num_pages, const int* cu, const int* ctx, const int* tiles,
-                      int num_tiles, int n_q, int n_kv, bf16* out, int ldo, cudaStream_t stream) {
+cudaError_t prefill_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool, const float* k_scale,
+                      const float* v_scale, const int* bt, int max_pages, int num_pages, const int* cu,
+                      const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv, bf16* out, int ldo,
+                      cudaStream_t stream) {
   constexpr int smem = (ABQ + 4 * ABKV) * D * 2;
   static PerDeviceOnce smem_attr;
   {
@@ -375,24 +387,26 @@ cudaError_t prefill_d(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   dim3 grid(num_tiles, n_q);
-  attn_prefill_kernel<D><<<grid, ATHREADS, smem, stream>>>(q, ldq, k_pool, v_pool, bt, max_pages, num_pages,
-                                                          cu, ctx, tiles, n_q, n_kv, out, ldo, scale_log2);
+  attn_prefill_kernel<D><<<grid, ATHREADS, smem, stream>>>(q, ldq, k_pool, v_pool, k_scale, v_scale, bt, max_pages,
+                                                          num_pages, cu, ctx, tiles, n_q, n_kv, out, ldo, scale_log2);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
+                                     const float* k_scale, const float* v_scale,
                                      const int* block_table, int max_pages, int num_pages,
                                      const int* cu, const int* ctx, const int* tiles, int num_tiles, int n_q,
                                      int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream) {
   if (num_tiles <= 0) return cudaSuccess;
+  if (!k_scale != !v_scale) return cudaErrorNotSupported;
   if (d_head == 128)
-    return prefill_d<128>(q, ldq, k_pool, v_pool, block_table, max_pages, num_pages, cu, ctx, tiles,
-                          num_tiles, n_q, n_kv, out, ldo, stream);
+    return prefill_d<128>(q, ldq, k_pool, v_pool, k_scale, v_scale, block_table, max_pages, num_pages, cu, ctx,
+                          tiles, num_tiles, n_q, n_kv, out, ldo, stream);
   if (d_head == 64)
-    return prefill_d<64>(q, ldq, k_pool, v_pool, block_table, max_pages, num_pages, cu, ctx, tiles,
-                         num_tiles, n_q, n_kv, out, ldo, stream);
+    return prefill_d<64>(q, ldq, k_pool, v_pool, k_scale, v_scale, block_table, max_pages, num_pages, cu, ctx,
+                         tiles, num_tiles, n_q, n_kv, out, ldo, stream);
   return cudaErrorNotSupported;
 }
 

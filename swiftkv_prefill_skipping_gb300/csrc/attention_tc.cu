@@ -3,23 +3,27 @@
 //
 // One CTA = 128 query rows of one prompt chunk x one query head. A chunk may follow ctx
 // tokens already in the cache (chunked prefill, decode rows): its rows then sit at
-// positions ctx.. and see keys [0, ctx + row]. 8 warps:
+// positions ctx.. and see keys [0, ctx + row]. 6 warps:
 //   warp 0     TMA producer: the Q tile once (two 64-column halves, 128B swizzle), then
 //              per 64-key block the K and V rows of its four 16-token pages (each page
 //              row block is contiguous in the pool) into a 3-stage ring
 //   warp 1     allocates TMEM; one lane issues S = Q K^T (M=128, N=64, K=128) into one of
-//              two 64-column S buffers, and O += P V (M=128, N=128, K=64; fp16 operands,
-//              V used as an MN-major operand in the cache's own row layout) into one
-//              128-column accumulator; S of block j+1 is issued before P V of block j so the
-//              tensor core works while the softmax warps do
+//              two 64-column S buffers, and O += P V (M=128, N=128, K=64; bf16 operands: P
+//              read from TMEM as a high and a low part, two MMAs; V used as an MN-major
+//              operand in the cache's own row layout) into one 128-column accumulator; S of
+//              block j+1 is issued before P V of block j so the tensor core works while the
+//              softmax warps do; an S buffer is refilled only after the P V that read the P
+//              stored over it has completed
 //   warps 2-5  one thread per query row: tcgen05.ld its S row, causal/length mask (only on
 //              blocks that cross the diagonal or the prompt end), online softmax in the log2
 //              domain with a running max allowed to lag by up to 2^8 (O, accumulated across
 //              blocks in TMEM by the MMA, is rescaled in place only when it moves further),
-//              P (fp16) into shared memory in the swizzled K-major layout the MMA reads;
-//              finally O / l from TMEM to global memory
-// All mbarrier waits are bounded; on a timeout the CTA flags kStatusTimeout, drains its
-// own TMA copies and MMAs, frees TMEM and exits.
+//              P as bf16 high + low parts (about 15 significant bits) by tcgen05.st over
+//              the S columns it came from; finally O / l from TMEM to global memory
+// FP8 cache: the pools hold the e4m3 codes as (exact) bf16 values; the block's key and value
+// scales come with its K/V, each score is multiplied by its key's scale and each P by its
+// value's scale (float32). All mbarrier waits are bounded; on a timeout the CTA flags
+// kStatusTimeout, drains its own TMA copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -40,41 +44,43 @@ constexpr int D = 128;          // head dim
 constexpr int BQ = 128;         // query rows per CTA
 constexpr int BKV = 64;         // keys per block (4 pages)
 constexpr int KV_STAGES = 3;
-constexpr int THREADS = 256;
+constexpr int THREADS = 192;
 constexpr int Q_BYTES = BQ * D * 2;            // 32 KB (two 16 KB halves)
 constexpr int KV_HALF = BKV * 64 * 2;          // 8 KB: 64 keys x 64 dims
 constexpr int K_BYTES = 2 * KV_HALF;           // 16 KB
 constexpr int STAGE_BYTES = 2 * K_BYTES;       // K + V
-constexpr int P_BYTES = BQ * BKV * 2;          // 16 KB
+constexpr int SCALE_BYTES = 2 * BKV * 4;       // FP8 cache: the block's key scales, then value scales
 constexpr int TMEM_COLS = 256;                 // S: 2 x 64, O: 128 (accumulated across blocks)
 constexpr int S_COL = 0, O_COL = 128;
 constexpr float kStaleMax = 8.f;               // log2 headroom before O is rescaled
+constexpr int P_LO_COL = 32;                   // P over S: high parts in columns 0-31, low parts 32-63
 
 struct Ctrl {
-  uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], v_ready[KV_STAGES], s_full[2], s_empty[2],
-      p_full[2], pv_done[2], fin;
+  uint64_t q_full, kv_full[KV_STAGES], kv_empty[KV_STAGES], s_full[2], p_full[2], pv_done[2], fin;
   uint32_t tmem_base;
   int abort;
   int pending[KV_STAGES + 1];
 };
-constexpr int SMEM_BYTES = 1024 + Q_BYTES + KV_STAGES * STAGE_BYTES + 2 * P_BYTES + (int)sizeof(Ctrl);
+constexpr int SMEM_BYTES = 1024 + Q_BYTES + KV_STAGES * (STAGE_BYTES + SCALE_BYTES) + (int)sizeof(Ctrl);
 
 constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);  // Q (K-major) x K (K-major)
-constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true, true);  // P (K-major) x V (MN-major), fp16
+constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true);  // P (TMEM) x V (MN-major), bf16
 
 __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-    const __grid_constant__ CUtensorMap tmV, const int* __restrict__ bt, int max_pages, int num_pages,
-    const int* __restrict__ cu, const int* __restrict__ ctx, const int* __restrict__ tiles, int n_q, int n_kv,
-    bf16* __restrict__ out, int ldo, float scale_log2, int* status) {
+    const __grid_constant__ CUtensorMap tmV, const float* __restrict__ kscale, const float* __restrict__ vscale,
+    const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ cu,
+    const int* __restrict__ ctx, const int* __restrict__ tiles, int n_q, int n_kv, bf16* __restrict__ out, int ldo,
+    float scale_log2, int* status) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const uint32_t sQ = smem_u32(smem);
   const uint32_t sKV = sQ + Q_BYTES;
-  const uint32_t sP = sKV + KV_STAGES * STAGE_BYTES;
-  unsigned char* sP_gen = smem + Q_BYTES + KV_STAGES * STAGE_BYTES;
-  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + Q_BYTES + KV_STAGES * STAGE_BYTES + 2 * P_BYTES);
+  const uint32_t sScale = sKV + KV_STAGES * STAGE_BYTES;  // stage s at sScale + s * SCALE_BYTES
+  const float* sScale_gen = reinterpret_cast<const float*>(smem + Q_BYTES + KV_STAGES * STAGE_BYTES);
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + Q_BYTES + KV_STAGES * (STAGE_BYTES + SCALE_BYTES));
+  const bool fp8 = kscale != nullptr;
   volatile int* abort_flag = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -96,13 +102,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
     for (int i = 0; i < KV_STAGES; ++i) {
       mbar_init(bar(ctl->kv_full[i]), 1);
       mbar_init(bar(ctl->kv_empty[i]), 1);
-      mbar_init(bar(ctl->v_ready[i]), 64);
       ctl->pending[i] = -1;
     }
     ctl->pending[KV_STAGES] = -1;
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(ctl->s_full[i]), 1);
-      mbar_init(bar(ctl->s_empty[i]), 128);
       mbar_init(bar(ctl->p_full[i]), 128);
       mbar_init(bar(ctl->pv_done[i]), 1);
     }
@@ -133,19 +137,26 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
       uint32_t phase = 0;
       for (int j = 0; j < nblk; ++j) {
         if (!mbar_wait(bar(ctl->kv_empty[stage]), phase ^ 1, abort_flag)) break;
-        mbar_expect_tx(bar(ctl->kv_full[stage]), STAGE_BYTES);
+        mbar_expect_tx(bar(ctl->kv_full[stage]), STAGE_BYTES + (fp8 ? SCALE_BYTES : 0));
         ctl->pending[stage] = (int)phase;
         const uint32_t sk = sKV + stage * STAGE_BYTES, sv = sk + K_BYTES;
 #pragma unroll
         for (int pg = 0; pg < BKV / kPageSize; ++pg) {
           const int key = j * BKV + pg * kPageSize;
           int page = key < nk ? bt[(size_t)s * max_pages + (key >> 4)] : -1;
+          const bool valid = page >= 0 && page < num_pages;
           // a page outside the pool reads rows past the tensor's end: TMA fills zeros
-          const int row = (page >= 0 && page < num_pages) ? (page * n_kv + kvh) * kPageSize : pool_rows;
+          const int row = valid ? (page * n_kv + kvh) * kPageSize : pool_rows;
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             tma_load_2d(sk + hf * KV_HALF + pg * 2048, &tmK, hf * 64, row, bar(ctl->kv_full[stage]));
             tma_load_2d(sv + hf * KV_HALF + pg * 2048, &tmV, hf * 64, row, bar(ctl->kv_full[stage]));
+          }
+          if (fp8) {  // the page's 16 key and 16 value scales (page 0's for a page outside the pool)
+            const size_t srow = valid ? (size_t)row : (size_t)kvh * kPageSize;
+            const uint32_t ss = sScale + stage * SCALE_BYTES + pg * kPageSize * 4;
+            bulk_load(ss, kscale + srow, kPageSize * 4, bar(ctl->kv_full[stage]));
+            bulk_load(ss + BKV * 4, vscale + srow, kPageSize * 4, bar(ctl->kv_full[stage]));
           }
         }
         if (++stage == KV_STAGES) {
@@ -164,7 +175,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
         if (!mbar_wait(bar(ctl->kv_full[st]), ph, abort_flag)) return false;
         ctl->pending[st] = -1;
         const int sb = j & 1;
-        if (!mbar_wait(bar(ctl->s_empty[sb]), (uint32_t)(((j >> 1) & 1) ^ 1), abort_flag)) return false;
+        // the buffer holds P of block j - 2 until the P V that reads it has completed
+        if (j >= 2 && !mbar_wait(bar(ctl->pv_done[sb]), (uint32_t)(((j - 2) >> 1) & 1), abort_flag)) return false;
         tc_fence_after();
         const uint32_t sk = sKV + st * STAGE_BYTES;
 #pragma unroll
@@ -183,47 +195,26 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
         const uint32_t ph = (uint32_t)((j >> 1) & 1);
         if (!mbar_wait(bar(ctl->p_full[pb]), ph, abort_flag)) break;
         const int st = j % KV_STAGES;
-        if (!mbar_wait(bar(ctl->v_ready[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) break;
         tc_fence_after();
         const uint32_t sv = sKV + st * STAGE_BYTES + K_BYTES;
-        const uint32_t pbase = sP + pb * P_BYTES;
+        const uint32_t pcol = tmem + S_COL + pb * BKV;
 #pragma unroll
         for (int kk = 0; kk < BKV / 16; ++kk) {
-          // P: K-major, rows of 64 keys; V: MN-major, 64-dim halves 8 KB apart, 8-key groups 1 KB apart
-          tc_mma(tmem + O_COL, sdesc(pbase + kk * 32), sdesc_sw128(sv + kk * 2048, KV_HALF, 1024), IDESC_O,
-                 (j | kk) != 0);
+          // P: 16 keys = 8 TMEM columns per MMA (high part, then low part); V: MN-major,
+          // 64-dim halves 8 KB apart, 8-key groups 1 KB apart
+          const uint64_t vdesc = sdesc_sw128(sv + kk * 2048, KV_HALF, 1024);
+          tc_mma_ts(tmem + O_COL, pcol + kk * 8, vdesc, IDESC_O, (j | kk) != 0);
+          tc_mma_ts(tmem + O_COL, pcol + P_LO_COL + kk * 8, vdesc, IDESC_O, 1);
         }
         tc_commit(bar(ctl->pv_done[pb]));
         tc_commit(bar(ctl->kv_empty[st]));
       }
     }
-  } else if (warp >= 6) {
-    // V converters: each arrived V tile bf16 -> fp16 in place (exact inside fp16's normal
-    // range, clamped to +-65504) so that P V runs with P at fp16 precision
-    const int t = threadIdx.x - 192;
-    for (int j = 0; j < nblk; ++j) {
-      const int st = j % KV_STAGES;
-      if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) break;
-      uint4* vt = reinterpret_cast<uint4*>(smem + Q_BYTES + st * STAGE_BYTES + K_BYTES);
-#pragma unroll 4
-      for (int c = t; c < K_BYTES / 16; c += 64) {
-        uint4 rw = vt[c];
-        uint32_t* w = reinterpret_cast<uint32_t*>(&rw);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
-          w[e] = pack_f16_sat(f.x, f.y);
-        }
-        vt[c] = rw;
-      }
-      fence_proxy_async_smem();
-      mbar_arrive(bar(ctl->v_ready[st]));
-    }
   } else {
     // softmax / output warps: thread <-> query row. O accumulates in TMEM across blocks; the
     // probabilities use a running max that may lag the true one by up to 2^kStaleMax (they
-    // then stay <= 256, fine for fp16); only when a row's max moves further is O rescaled,
-    // by the warp, in TMEM, after the previous block's P V has landed.
+    // then stay <= 256); only when a row's max moves further is O rescaled, by the warp, in
+    // TMEM, after the previous block's P V has landed.
     const int q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int qrow = q0 + r;     // row within the chunk
@@ -245,8 +236,19 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
       float sc[BKV];
       tmem_ld32(tmem + lane_off + S_COL + sb * BKV, sc);
       tmem_ld32(tmem + lane_off + S_COL + sb * BKV + 32, sc + 32);
-      tc_fence_before();
-      mbar_arrive(bar(ctl->s_empty[sb]));
+      const float* kvs = nullptr;  // FP8: this block's key scales, then value scales
+      if (fp8) {
+        // the stage's scales arrived with its K/V (kv_full): wait on it directly so their
+        // shared-memory writes are visible to this thread (the phase has long completed)
+        const int st = j % KV_STAGES;
+        if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((j / KV_STAGES) & 1), abort_flag)) {
+          ok = false;
+          break;
+        }
+        kvs = sScale_gen + st * (SCALE_BYTES / 4);
+#pragma unroll
+        for (int i = 0; i < BKV; ++i) sc[i] *= kvs[i];
+      }
       const bool interior = (j + 1) * BKV - 1 <= c0 + q0 && (j + 1) * BKV <= nk;  // no key masked in any row
       if (!interior) {
 #pragma unroll
@@ -299,22 +301,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
         ps[i & 7] += sc[i];
       }
       l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-      // P buffer sb was last read by the P V of block j-2
-      if (j >= 2 && !wait_pv(j - 2)) {
-        ok = false;
-        break;
-      }
-      unsigned char* prow = sP_gen + sb * P_BYTES + r * 128;
+      if (fp8) {  // P V with V = code x scale: the value scale rides on P
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 u;
-        u.x = pack_f16(sc[8 * c], sc[8 * c + 1]);
-        u.y = pack_f16(sc[8 * c + 2], sc[8 * c + 3]);
-        u.z = pack_f16(sc[8 * c + 4], sc[8 * c + 5]);
-        u.w = pack_f16(sc[8 * c + 6], sc[8 * c + 7]);
-        *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
+        for (int i = 0; i < BKV; ++i) sc[i] *= kvs[BKV + i];
       }
-      fence_proxy_async_smem();
+      // P over this block's S columns (read above), as bf16 high and low parts
+      {
+        uint32_t pw[2 * 32];
+        split_p_bf16(sc, pw);
+        tmem_st64(tmem + lane_off + S_COL + sb * BKV, pw);
+      }
       tc_fence_before();
       mbar_arrive(bar(ctl->p_full[sb]));
     }
@@ -371,11 +367,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc_kernel(
 }  // namespace
 
 cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
-                                        const int* block_table, int max_pages, int num_pages, const int* cu,
-                                        const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
-                                        int d_head, bf16* out, int ldo, int* status, cudaStream_t stream) {
+                                        const float* k_scale, const float* v_scale, const int* block_table,
+                                        int max_pages, int num_pages, const int* cu, const int* ctx, const int* tiles,
+                                        int num_tiles, int n_q, int n_kv, int d_head, bf16* out, int ldo, int* status,
+                                        cudaStream_t stream) {
   if (num_tiles <= 0) return cudaSuccess;
-  if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8) return cudaErrorNotSupported;
+  if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8 || (!k_scale != !v_scale) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 15) || (reinterpret_cast<uintptr_t>(v_scale) & 15))
+    return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
   const int pool_rows = num_pages * n_kv * kPageSize;
   if (!tma_map_bf16_2d(&mq, q, T, n_q * D, ldq, 64, BQ, true) ||
@@ -389,8 +388,9 @@ cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf1
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   dim3 grid(num_tiles, n_q);
-  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, block_table, max_pages, num_pages, cu, ctx,
-                                                        tiles, n_q, n_kv, out, ldo, scale_log2, status);
+  attn_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(mq, mk, mv, k_scale, v_scale, block_table, max_pages,
+                                                        num_pages, cu, ctx, tiles, n_q, n_kv, out, ldo, scale_log2,
+                                                        status);
   return cudaGetLastError();
 }
 

@@ -6,27 +6,34 @@
 // cached tokens: its rows sit at positions ctx.. and see keys [0, ctx + row]. Persistent: one
 // CTA per SM walks its share of the items (heaviest first, alternate rounds reversed) with
 // TMEM, barriers and the K/V ring carried from item to item, so the next item's Q and K/V
-// loads and first S MMAs run while the softmax warps write the current item's output. 12 warps:
+// loads and first S MMAs run while the softmax warps write the current item's output. 11 warps:
 //   warp 0      TMA: both Q tiles once (two 64-column halves each, 128B swizzle), then per
-//               64-key block the K and V rows of its four 16-token pages into a 3-stage ring
-//   warp 1      allocates all 512 TMEM columns; one lane issues, per block, S_A = Q_A K^T and
-//               S_B = Q_B K^T (M=128, N=64, K=128; each tile's S double-buffered) ahead of
-//               O_A += P_A V and O_B += P_B V (M=128, N=128, K=64; fp16 operands, V as an
-//               MN-major operand in the cache's own row layout), O_A / O_B in TMEM
-//   warps 2-3   V converters: each V tile bf16 -> fp16 in place, once for both tiles
-//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: one thread per query row
+//               64-key block the K and V rows of its four 16-token pages into a 4-stage ring
+//   warps 1, 2  MMA issue for tile A and tile B (warp 1 also allocates all 512 TMEM columns):
+//               one lane issues, per block, S = Q K^T (M=128, N=64, K=128; double-buffered)
+//               ahead of O += P V (M=128, N=128, K=64, bf16 operands: P read from TMEM, where
+//               the softmax warps left it over its S, as a high and a low part, two MMAs; V an
+//               MN-major operand in the cache's own row layout); each tile's pipeline waits
+//               only on its own softmax, and a K/V stage is released when both tiles' MMAs
+//               that read it have completed
+//   warps 3-6   softmax of tile A, warps 7-10 softmax of tile B: one thread per query row
 //               (tcgen05.ld of its S row, causal/length mask only on blocks that cross the
 //               diagonal or the chunk end, online softmax in the log2 domain with a running
 //               max allowed to lag by up to 2^8 -- O is rescaled in TMEM only past that --, P
-//               (fp16) into shared memory in the swizzled K-major layout the MMA reads), then
-//               O / l from TMEM to global memory.
+//               split into bf16 high + low parts (about 15 significant bits) and stored by
+//               tcgen05.st over the S columns it came from), then O / l from TMEM to global
+//               memory.
 // While one tile's softmax warps work, the tensor core runs the other tile's MMAs, and each
-// K/V block is loaded and converted once for 256 query rows. Tile A needs up to 128 fewer
-// keys than tile B; its last blocks are skipped. Between items, Q is reloaded once the last
-// S MMA of the item has completed (q_empty), and a tile's first P V of the next item waits
-// until its O has been read out of TMEM (o_empty). All mbarrier waits are bounded; on a
-// timeout the CTA flags kStatusTimeout, drains its own TMA copies and MMAs, frees TMEM and
-// exits.
+// K/V block is loaded once for 256 query rows. Tile A needs up to 128 fewer keys than tile B;
+// its last blocks are skipped. An S buffer is refilled only after the P V that read the P
+// stored over it has completed. Between items, Q is reloaded once the last S MMA of the item
+// has completed (q_empty), and a tile's first P V of the next item waits until its O has been
+// read out of TMEM (o_empty). FP8 cache: the K/V pools hold the e4m3 codes as (exact) bf16
+// values; the TMA warp also brings each block's 64 key and 64 value scales into the stage,
+// and the softmax multiplies each score by its key's scale and each P by its value's scale
+// (float32) before the split, so K and V enter as code x scale without a bf16 rounding of
+// the product. All mbarrier waits are bounded; on a timeout the CTA flags kStatusTimeout,
+// drains its own TMA copies and MMAs, frees TMEM and exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,30 +53,32 @@ using namespace tc;
 constexpr int D = 128;          // head dim
 constexpr int BQ = 128;         // query rows per tile
 constexpr int BKV = 64;         // keys per block (4 pages)
-constexpr int KV_STAGES = 3;
-constexpr int THREADS = 384;
+constexpr int KV_STAGES = 4;
+constexpr int THREADS = 352;
+constexpr int SOFTMAX_WARP0 = 3;
 constexpr int Q_BYTES = BQ * D * 2;            // 32 KB per tile (two 16 KB halves)
 constexpr int KV_HALF = BKV * 64 * 2;          // 8 KB: 64 keys x 64 dims
 constexpr int K_BYTES = 2 * KV_HALF;           // 16 KB
 constexpr int STAGE_BYTES = 2 * K_BYTES;       // K + V
-constexpr int P_BYTES = BQ * BKV * 2;          // 16 KB
+constexpr int SCALE_BYTES = 2 * BKV * 4;       // FP8 cache: the block's key scales, then value scales
 constexpr int TMEM_COLS = 512;                 // S_A: 0, 64; S_B: 128, 192; O_A: 256; O_B: 384
+constexpr int P_LO_COL = 32;                   // P over S: high parts in columns 0-31, low parts 32-63
 constexpr int O_COL = 256;
 constexpr float kStaleMax = 8.f;               // log2 headroom before O is rescaled
 
 struct Ctrl {
-  uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES], v_ready[KV_STAGES];
-  uint64_t s_full[2][2], s_empty[2][2], p_full[2][2], pv_done[2][2], fin;  // [tile][buffer]
+  uint64_t q_full, q_empty, kv_full[KV_STAGES], kv_empty[KV_STAGES];
+  uint64_t s_full[2][2], p_full[2][2], pv_done[2][2], fin[2];  // [tile][buffer]
   uint64_t o_empty[2];                                                     // [tile]
   uint32_t tmem_base;
   int abort;
   int pending[KV_STAGES + 1];
 };
-constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + KV_STAGES * STAGE_BYTES + 4 * P_BYTES + (int)sizeof(Ctrl);
+constexpr int SMEM_BYTES = 1024 + 2 * Q_BYTES + KV_STAGES * (STAGE_BYTES + SCALE_BYTES) + (int)sizeof(Ctrl);
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 
 constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);  // Q (K-major) x K (K-major)
-constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true, true);  // P (K-major) x V (MN-major), fp16
+constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true);  // P (TMEM) x V (MN-major), bf16
 
 // One work item: query rows [256p, 256p + 256) of one chunk x one query head.
 struct Item {
@@ -105,17 +114,19 @@ __device__ __forceinline__ bool item_at(int it, const int* __restrict__ tiles, i
 
 __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
     const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-    const __grid_constant__ CUtensorMap tmV, const int* __restrict__ bt, int max_pages, int num_pages,
-    const int* __restrict__ cu, const int* __restrict__ ctx, const int* __restrict__ tiles, int n_items, int n_q,
-    int n_kv, bf16* __restrict__ out, int ldo, float scale_log2, int* status) {
+    const __grid_constant__ CUtensorMap tmV, const float* __restrict__ kscale, const float* __restrict__ vscale,
+    const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ cu,
+    const int* __restrict__ ctx, const int* __restrict__ tiles, int n_items, int n_q, int n_kv,
+    bf16* __restrict__ out, int ldo, float scale_log2, int* status) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const uint32_t sQ = smem_u32(smem);  // tile t at sQ + t * Q_BYTES
   const uint32_t sKV = sQ + 2 * Q_BYTES;
-  const uint32_t sP = sKV + KV_STAGES * STAGE_BYTES;  // tile t, buffer b at sP + (2t + b) * P_BYTES
-  unsigned char* sP_gen = smem + 2 * Q_BYTES + KV_STAGES * STAGE_BYTES;
-  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + 2 * Q_BYTES + KV_STAGES * STAGE_BYTES + 4 * P_BYTES);
+  const uint32_t sScale = sKV + KV_STAGES * STAGE_BYTES;  // stage s at sScale + s * SCALE_BYTES
+  const float* sScale_gen = reinterpret_cast<const float*>(smem + 2 * Q_BYTES + KV_STAGES * STAGE_BYTES);
+  Ctrl* ctl = reinterpret_cast<Ctrl*>(smem + 2 * Q_BYTES + KV_STAGES * (STAGE_BYTES + SCALE_BYTES));
+  const bool fp8 = kscale != nullptr;
   volatile int* abort_flag = &ctl->abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -126,24 +137,23 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
 
   if (threadIdx.x == 0) {
     mbar_init(bar(ctl->q_full), 1);
-    mbar_init(bar(ctl->q_empty), 1);
+    mbar_init(bar(ctl->q_empty), 2);  // both tiles' last S MMA of the item
     for (int i = 0; i < KV_STAGES; ++i) {
       mbar_init(bar(ctl->kv_full[i]), 1);
-      mbar_init(bar(ctl->kv_empty[i]), 1);
-      mbar_init(bar(ctl->v_ready[i]), 64);
+      mbar_init(bar(ctl->kv_empty[i]), 2);  // both tiles' MMAs done with the stage
       ctl->pending[i] = -1;
     }
     ctl->pending[KV_STAGES] = -1;
     for (int t = 0; t < 2; ++t) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(bar(ctl->s_full[t][i]), 1);
-        mbar_init(bar(ctl->s_empty[t][i]), 128);
         mbar_init(bar(ctl->p_full[t][i]), 128);
         mbar_init(bar(ctl->pv_done[t][i]), 1);
       }
       mbar_init(bar(ctl->o_empty[t]), 128);
     }
-    mbar_init(bar(ctl->fin), 1);
+    mbar_init(bar(ctl->fin[0]), 1);
+    mbar_init(bar(ctl->fin[1]), 1);
     ctl->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -184,38 +194,67 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
             ok = false;
             break;
           }
-          mbar_expect_tx(bar(ctl->kv_full[stage]), STAGE_BYTES);
+          mbar_expect_tx(bar(ctl->kv_full[stage]), STAGE_BYTES + (fp8 ? SCALE_BYTES : 0));
           ctl->pending[stage] = (int)phase;
           const uint32_t sk = sKV + stage * STAGE_BYTES, sv = sk + K_BYTES;
 #pragma unroll
           for (int pg = 0; pg < BKV / kPageSize; ++pg) {
             const int key = j * BKV + pg * kPageSize;
             int page = key < I.nk ? bt[(size_t)I.s * max_pages + (key >> 4)] : -1;
+            const bool valid = page >= 0 && page < num_pages;
             // a page outside the pool reads rows past the tensor's end: TMA fills zeros
-            const int row = (page >= 0 && page < num_pages) ? (page * n_kv + kvh) * kPageSize : pool_rows;
+            const int row = valid ? (page * n_kv + kvh) * kPageSize : pool_rows;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
               tma_load_2d(sk + hf * KV_HALF + pg * 2048, &tmK, hf * 64, row, bar(ctl->kv_full[stage]));
               tma_load_2d(sv + hf * KV_HALF + pg * 2048, &tmV, hf * 64, row, bar(ctl->kv_full[stage]));
             }
+            if (fp8) {  // the page's 16 key and 16 value scales (page 0's for a page outside the pool)
+              const size_t srow = valid ? (size_t)row : (size_t)kvh * kPageSize;
+              const uint32_t ss = sScale + stage * SCALE_BYTES + pg * kPageSize * 4;
+              bulk_load(ss, kscale + srow, kPageSize * 4, bar(ctl->kv_full[stage]));
+              bulk_load(ss + BKV * 4, vscale + srow, kPageSize * 4, bar(ctl->kv_full[stage]));
+            }
           }
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 || warp == 2) {
     if (lane == 0) {
-      // counters over all items: K/V blocks, S/P blocks of each tile, items that used each tile's O
-      int kv_base = 0, sp[2] = {0, 0}, oi[2] = {0, 0};
+      // tile t's MMAs. Counters over all items: K/V blocks, S/P blocks of this tile, items
+      // that used this tile's O
+      const int t = warp - 1;
+      int kv_base = 0, sp = 0, oi = 0;
       bool ok = true;
       for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
-        if (!mbar_wait(bar(ctl->q_full), (uint32_t)(it & 1), abort_flag)) break;
-        ctl->pending[KV_STAGES] = -1;
-        auto issue_s = [&](int t, int j) -> bool {
+        const int nb = t ? I.nblk_b : I.nblk_a;  // blocks this tile reads (0: no tile B)
+        // Releases block j's K/V stage for a block this tile does not read. The arrival counts
+        // toward that block's phase only once the block has been loaded (kv_full), so it can
+        // never complete an earlier phase the other tile's MMAs still depend on.
+        auto release_unread = [&](int j) -> bool {
           const int kv = kv_base + j, st = kv % KV_STAGES;
           if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((kv / KV_STAGES) & 1), abort_flag)) return false;
           ctl->pending[st] = -1;
-          const int g = sp[t] + j, sb = g & 1;
-          if (!mbar_wait(bar(ctl->s_empty[t][sb]), (uint32_t)(((g >> 1) & 1) ^ 1), abort_flag)) return false;
+          mbar_arrive(bar(ctl->kv_empty[st]));
+          return true;
+        };
+        // this item's Q has been loaded, so the previous item's q_empty phase has completed
+        if (!mbar_wait(bar(ctl->q_full), (uint32_t)(it & 1), abort_flag)) break;
+        ctl->pending[KV_STAGES] = -1;
+        if (nb == 0) {  // no tile B in this item: release its Q and K/V stages
+          mbar_arrive(bar(ctl->q_empty));
+          for (int j = 0; ok && j < I.nblk; ++j) ok = release_unread(j);
+          kv_base += I.nblk;
+          continue;
+        }
+        auto issue_s = [&](int j) -> bool {
+          const int kv = kv_base + j, st = kv % KV_STAGES;
+          if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((kv / KV_STAGES) & 1), abort_flag)) return false;
+          ctl->pending[st] = -1;
+          const int g = sp + j, sb = g & 1;
+          // the buffer holds P of block g - 2 until the P V that reads it has completed
+          if (g >= 2 && !mbar_wait(bar(ctl->pv_done[t][sb]), (uint32_t)(((g - 2) >> 1) & 1), abort_flag))
+            return false;
           tc_fence_after();
           const uint32_t sk = sKV + st * STAGE_BYTES;
           const uint32_t q = sQ + t * Q_BYTES;
@@ -228,84 +267,54 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
           tc_commit(bar(ctl->s_full[t][sb]));
           return true;
         };
-        auto issue_pv = [&](int t, int j) -> bool {
-          const int g = sp[t] + j, pb = g & 1;
+        auto issue_pv = [&](int j) -> bool {
+          const int g = sp + j, pb = g & 1;
           if (!mbar_wait(bar(ctl->p_full[t][pb]), (uint32_t)((g >> 1) & 1), abort_flag)) return false;
-          const int kv = kv_base + j, st = kv % KV_STAGES;
-          if (!mbar_wait(bar(ctl->v_ready[st]), (uint32_t)((kv / KV_STAGES) & 1), abort_flag)) return false;
           // the first P V of an item overwrites O: the previous item's output must have left TMEM
-          if (j == 0 && oi[t] > 0 && !mbar_wait(bar(ctl->o_empty[t]), (uint32_t)((oi[t] - 1) & 1), abort_flag))
+          if (j == 0 && oi > 0 && !mbar_wait(bar(ctl->o_empty[t]), (uint32_t)((oi - 1) & 1), abort_flag))
             return false;
           tc_fence_after();
+          const int st = (kv_base + j) % KV_STAGES;
           const uint32_t sv = sKV + st * STAGE_BYTES + K_BYTES;
-          const uint32_t pbase = sP + (2 * t + pb) * P_BYTES;
+          const uint32_t pcol = tmem + t * 128 + pb * BKV;
 #pragma unroll
           for (int kk = 0; kk < BKV / 16; ++kk) {
-            // P: K-major, rows of 64 keys; V: MN-major, 64-dim halves 8 KB apart, 8-key groups 1 KB apart
-            tc_mma(tmem + O_COL + t * 128, sdesc(pbase + kk * 32), sdesc_sw128(sv + kk * 2048, KV_HALF, 1024),
-                   IDESC_O, (j | kk) != 0);
+            // P: 16 keys = 8 TMEM columns per MMA (high part, then low part); V: MN-major,
+            // 64-dim halves 8 KB apart, 8-key groups 1 KB apart
+            const uint64_t vdesc = sdesc_sw128(sv + kk * 2048, KV_HALF, 1024);
+            tc_mma_ts(tmem + O_COL + t * 128, pcol + kk * 8, vdesc, IDESC_O, (j | kk) != 0);
+            tc_mma_ts(tmem + O_COL + t * 128, pcol + P_LO_COL + kk * 8, vdesc, IDESC_O, 1);
           }
           tc_commit(bar(ctl->pv_done[t][pb]));
+          tc_commit(bar(ctl->kv_empty[st]));
           return true;
         };
-        // q_empty is committed after the item's last S MMA (block nblk - 1), so the next item's
-        // Q can load while this item's P V and softmax finish
-        const int last_s = I.nblk - 1;
-        ok = issue_s(0, 0);
-        if (ok && I.has_b) ok = issue_s(1, 0);
-        if (ok && last_s == 0) tc_commit(bar(ctl->q_empty));
-        for (int j = 0; ok && j < I.nblk; ++j) {
-          // S of the next block for both tiles first, so the tensor core has work while the
-          // softmax warps turn this block's S into P
-          if (j + 1 < I.nblk_a && !(ok = issue_s(0, j + 1))) break;
-          if (j + 1 < I.nblk_b && !(ok = issue_s(1, j + 1))) break;
-          if (j + 1 == last_s) tc_commit(bar(ctl->q_empty));
-          if (j < I.nblk_a && !(ok = issue_pv(0, j))) break;
-          if (j < I.nblk_b && !(ok = issue_pv(1, j))) break;
-          tc_commit(bar(ctl->kv_empty[(kv_base + j) % KV_STAGES]));
-        }
-        kv_base += I.nblk;
-        sp[0] += I.nblk_a;
-        sp[1] += I.nblk_b;
-        oi[0] += 1;
-        oi[1] += I.has_b ? 1 : 0;
-      }
-    }
-  } else if (warp < 4) {
-    // V converters: each arrived V tile bf16 -> fp16 in place (exact inside fp16's normal
-    // range, clamped to +-65504) so that P V runs with P at fp16 precision
-    const int t = threadIdx.x - 64;
-    int kv_i = 0;
-    bool ok = true;
-    for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
-      for (int j = 0; j < I.nblk; ++j, ++kv_i) {
-        const int st = kv_i % KV_STAGES;
-        if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((kv_i / KV_STAGES) & 1), abort_flag)) {
-          ok = false;
-          break;
-        }
-        uint4* vt = reinterpret_cast<uint4*>(smem + 2 * Q_BYTES + st * STAGE_BYTES + K_BYTES);
-#pragma unroll 4
-        for (int c = t; c < K_BYTES / 16; c += 64) {
-          uint4 rw = vt[c];
-          uint32_t* w = reinterpret_cast<uint32_t*>(&rw);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&w[e]));
-            w[e] = pack_f16_sat(f.x, f.y);
+        // q_empty is committed after this tile's last S MMA of the item, so the next item's Q
+        // can load while this item's P V and softmax finish
+        ok = issue_s(0);
+        if (ok && nb == 1) tc_commit(bar(ctl->q_empty));
+        for (int j = 0; ok && j < nb; ++j) {
+          // S of the next block first, so the tensor core has work while the softmax warps
+          // turn this block's S into P
+          if (j + 1 < nb) {
+            if (!(ok = issue_s(j + 1))) break;
+            if (j + 2 == nb) tc_commit(bar(ctl->q_empty));
           }
-          vt[c] = rw;
+          if (!(ok = issue_pv(j))) break;
         }
-        fence_proxy_async_smem();
-        mbar_arrive(bar(ctl->v_ready[st]));
+        // blocks of the item past this tile's last (tile A needs fewer keys than tile B)
+        for (int j = nb; ok && j < I.nblk; ++j) ok = release_unread(j);
+        kv_base += I.nblk;
+        sp += nb;
+        oi += 1;
       }
     }
   } else {
     // softmax / output warps of tile t: thread <-> query row. O accumulates in TMEM across
     // blocks; the probabilities use a running max that may lag the true one by up to
-    // 2^kStaleMax (they then stay <= 256, fine for fp16); only when a row's max moves further
-    // is O rescaled, by the warp, in TMEM, after the previous block's P V has landed.
-    const int t = (warp - 4) >> 2;
+    // 2^kStaleMax (they then stay <= 256); only when a row's max moves further is O
+    // rescaled, by the warp, in TMEM, after the previous block's P V has landed.
+    const int t = (warp - SOFTMAX_WARP0) >> 2;
     const int q4 = warp & 3;  // TMEM lane quarter this warp may access
     const int r = q4 * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
@@ -313,9 +322,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
     auto wait_pv = [&](int g) -> bool {
       return mbar_wait(bar(ctl->pv_done[t][g & 1]), (uint32_t)((g >> 1) & 1), abort_flag);
     };
-    int sp = 0;  // S/P blocks of this tile over all items
+    int sp = 0;   // S/P blocks of this tile over all items
+    int kvb = 0;  // K/V blocks over all items (ring stage of block j: (kvb + j) % KV_STAGES)
     bool ok = true;
-    for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
+    for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); kvb += I.nblk, ++it) {
       if (t == 1 && !I.has_b) continue;
       const int nb = t ? I.nblk_b : I.nblk_a;
       const int q0 = t ? I.q0b : I.q0a;
@@ -331,8 +341,19 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
         tc_fence_after();
         float sc[BKV];
         tmem_ld64(tmem + lane_off + s_col + sb * BKV, sc);
-        tc_fence_before();
-        mbar_arrive(bar(ctl->s_empty[t][sb]));
+        const float* kvs = nullptr;  // FP8: this block's key scales, then value scales
+        if (fp8) {
+          // the stage's scales arrived with its K/V (kv_full); wait on it directly so their
+          // shared-memory writes are visible to this thread (the phase has long completed)
+          const int kv = kvb + j, st = kv % KV_STAGES;
+          if (!mbar_wait(bar(ctl->kv_full[st]), (uint32_t)((kv / KV_STAGES) & 1), abort_flag)) {
+            ok = false;
+            break;
+          }
+          kvs = sScale_gen + st * (SCALE_BYTES / 4);
+#pragma unroll
+          for (int i = 0; i < BKV; ++i) sc[i] *= kvs[i];
+        }
         const bool interior = (j + 1) * BKV - 1 <= I.c0 + q0 && (j + 1) * BKV <= I.nk;  // no key masked in any row
         if (!interior) {
 #pragma unroll
@@ -385,23 +406,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
           ps[i & 7] += sc[i];
         }
         l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-        // P buffer sb was last read by the P V of block g - 2 (for j < 2 that block belongs to
-        // an earlier item, whose final wait below already covered it)
-        if (j >= 2 && !wait_pv(g - 2)) {
-          ok = false;
-          break;
-        }
-        unsigned char* prow = sP_gen + (2 * t + sb) * P_BYTES + r * 128;
+        if (fp8) {  // P V with V = code x scale: the value scale rides on P
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 u;
-          u.x = pack_f16(sc[8 * c], sc[8 * c + 1]);
-          u.y = pack_f16(sc[8 * c + 2], sc[8 * c + 3]);
-          u.z = pack_f16(sc[8 * c + 4], sc[8 * c + 5]);
-          u.w = pack_f16(sc[8 * c + 6], sc[8 * c + 7]);
-          *reinterpret_cast<uint4*>(prow + ((c ^ (r & 7)) << 4)) = u;
+          for (int i = 0; i < BKV; ++i) sc[i] *= kvs[BKV + i];
         }
-        fence_proxy_async_smem();
+        // P over this block's S columns (read above), as bf16 high and low parts
+        {
+          uint32_t pw[2 * 32];
+          split_p_bf16(sc, pw);
+          tmem_st64(tmem + lane_off + s_col + sb * BKV, pw);
+        }
         tc_fence_before();
         mbar_arrive(bar(ctl->p_full[t][sb]));
       }
@@ -447,10 +461,11 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
         }
       }
     }
-    if (threadIdx.x == 32) {
-      tc_commit(bar(ctl->fin));
+    if (threadIdx.x == 32 || threadIdx.x == 64) {  // MMAs each issuing thread has in flight
+      const uint32_t f = bar(ctl->fin[threadIdx.x == 64]);
+      tc_commit(f);
       const uint64_t t0 = global_ns();
-      while (!mbar_try_wait(bar(ctl->fin), 0) && global_ns() - t0 < kTimeoutNs) {
+      while (!mbar_try_wait(f, 0) && global_ns() - t0 < kTimeoutNs) {
       }
     }
     __syncthreads();
@@ -463,12 +478,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
 }  // namespace
 
 cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
+                                         const float* k_scale, const float* v_scale,
                                          const int* block_table, int max_pages, int num_pages, const int* cu,
                                          const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
                                          int d_head, bf16* out, int ldo, int num_sms, int* status,
                                          cudaStream_t stream) {
   if (num_tiles <= 0) return cudaSuccess;
-  if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8 || num_sms < 1) return cudaErrorNotSupported;
+  if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8 || num_sms < 1 || (!k_scale != !v_scale) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 15) || (reinterpret_cast<uintptr_t>(v_scale) & 15))
+    return cudaErrorNotSupported;
   CUtensorMap mq, mk, mv;
   const int pool_rows = num_pages * n_kv * kPageSize;
   if (!tma_map_bf16_2d(&mq, q, T, n_q * D, ldq, 64, BQ, true) ||
@@ -483,7 +501,8 @@ cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
   const int n_items = num_tiles * n_q;
   attn_tc2_kernel<<<n_items < num_sms ? n_items : num_sms, THREADS, SMEM_BYTES, stream>>>(
-      mq, mk, mv, block_table, max_pages, num_pages, cu, ctx, tiles, n_items, n_q, n_kv, out, ldo, scale_log2, status);
+      mq, mk, mv, k_scale, v_scale, block_table, max_pages, num_pages, cu, ctx, tiles, n_items, n_q, n_kv, out, ldo,
+      scale_log2, status);
   return cudaGetLastError();
 }
 

@@ -51,7 +51,40 @@ struct EpiParams {
   int cache_base;            // EPI_QKV: the layer's cache; EPI_WIDE_KV: first skipped cache
   bf16* kv_stage;            // non-null (FP8 cache): K (after RoPE) and V rows go here instead,
   int kv_stage_ld;           //   [M][kv_stage_ld] at their K/V column, for the quantize pass
+  // FP8 cache quantized in the epilogue (tcgen05 GEMMs; ks_pools non-null): k_pools / v_pools
+  // hold uint8 e4m3 code pools, ks_pools / vs_pools the float scale pools [pages][n_kv][16];
+  // exp_k / exp_v (optional) receive the codes as bf16 for the prompt-tile attention
+  float* const* ks_pools;
+  float* const* vs_pools;
+  bf16* exp_k;
+  bf16* exp_v;
+  // RMSNorm fused into the GEMMs on either side of it (prompt rows on the tcgen05 GEMMs):
+  const float* norm_part;    // non-null: the A operand holds bf16(gamma * x) of residual rows x and
+  int norm_parts;            //   the kernel scales row m's accumulators by rsqrt(S_m / dim + eps),
+  float norm_inv_dim;        //   S_m = the sum, in index order, of norm_part[m][0 .. norm_parts)
+  float norm_eps;
+  bf16* xb_out;              // EPI_RESID, non-null: also stores bf16(xb_gamma * updated row) at
+  const float* xb_gamma;     //   [m][ldo] (xb_gamma NULL: 1), the next norm's input, and the row's
+  float* ss_out;             //   sum of squares per 256-column GEMM tile at [m][norm_tiles(N)]
 };
+
+// Partial sums of squares an EPI_RESID row of width n leaves in ss_out: one per 256-column tile.
+constexpr int kNormTile = 256;
+constexpr int kMaxNormTiles = 32;  // widths up to 8192
+__host__ __device__ __forceinline__ int norm_tiles(int n) { return (n + kNormTile - 1) / kNormTile; }
+
+// Row scale of the fused RMSNorm: rsqrt(mean of squares + eps) with the tile sums added in
+// index order (independent loads, one dependent add chain).
+__device__ __forceinline__ float fused_norm_scale(const EpiParams& p, int m) {
+  const float* s = p.norm_part + (size_t)m * p.norm_parts;
+  float v[kMaxNormTiles];
+#pragma unroll
+  for (int i = 0; i < kMaxNormTiles; ++i) v[i] = i < p.norm_parts ? s[i] : 0.f;
+  float acc = 0.f;
+#pragma unroll
+  for (int i = 0; i < kMaxNormTiles; ++i) acc += v[i];
+  return rsqrtf(acc * p.norm_inv_dim + p.norm_eps);
+}
 
 __host__ __device__ __forceinline__ int pair_half(const EpiParams& p) {
   return (p.kind == EPI_QKV || p.kind == EPI_WIDE_KV) ? (p.d_head >> 1) : 64;
@@ -197,8 +230,10 @@ __device__ __forceinline__ void store_bf16x32(bf16* dst, const float* v) {
 // Same epilogue as apply_pair for the 32 pairs (n_lo + i, n_hi + i), i < 32, with
 // 16-byte vector stores. A chunk never straddles a Q/K/V region or a head because
 // half is a multiple of 32 and region widths are multiples of d_head.
-__device__ __forceinline__ void apply_chunk32(const EpiParams& p, int m, int n_lo, int n_hi, float* a,
+// Returns, for EPI_RESID with xb_out, the sum of squares of the updated values (0 otherwise).
+__device__ __forceinline__ float apply_chunk32(const EpiParams& p, int m, int n_lo, int n_hi, float* a,
                                               float* b) {
+  float ssq = 0.f;
   switch (p.kind) {
     case EPI_STORE_F32: {
       float* o = p.out_f32 + (size_t)m * p.ldo;
@@ -219,6 +254,29 @@ __device__ __forceinline__ void apply_chunk32(const EpiParams& p, int m, int n_l
         y.x += b[i]; y.y += b[i + 1]; y.z += b[i + 2]; y.w += b[i + 3];
         *reinterpret_cast<float4*>(o + n_lo + i) = x;
         *reinterpret_cast<float4*>(o + n_hi + i) = y;
+        a[i] = x.x; a[i + 1] = x.y; a[i + 2] = x.z; a[i + 3] = x.w;
+        b[i] = y.x; b[i + 1] = y.y; b[i + 2] = y.z; b[i + 3] = y.w;
+      }
+      if (p.xb_out) {
+        // the chunk's sum of squares (four interleaved partial sums combined in a fixed order)
+        // and the next GEMM's input, bf16(gamma * x)
+        float q[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          q[i & 3] = fmaf(a[i], a[i], q[i & 3]);
+          q[i & 3] = fmaf(b[i], b[i], q[i & 3]);
+        }
+        ssq = (q[0] + q[1]) + (q[2] + q[3]);
+        if (p.xb_gamma) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            a[i] *= p.xb_gamma[n_lo + i];
+            b[i] *= p.xb_gamma[n_hi + i];
+          }
+        }
+        bf16* xb = p.xb_out + (size_t)m * p.ldo;
+        store_bf16x32(xb + n_lo, a);
+        store_bf16x32(xb + n_hi, b);
       }
       break;
     }
@@ -289,6 +347,7 @@ __device__ __forceinline__ void apply_chunk32(const EpiParams& p, int m, int n_l
     default:
       break;
   }
+  return ssq;
 }
 
 // ---------------------------------------------------------------------------- float8 e4m3
@@ -301,6 +360,88 @@ __device__ __forceinline__ uint16_t e4m3x2_from_f32(float lo, float hi) {
 __device__ __forceinline__ uint32_t f16x2_from_e4m3x2(uint32_t codes16) {
   __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)codes16, __NV_E4M3);
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// ---------------------------------------------------------------------------- FP8 cache epilogue
+//
+// Per-token FP8 quantization fused into the QKV / wide-KV epilogue of the tcgen05 GEMMs: the
+// epilogue thread of a row holds every column of one K or V head (the 2 * half columns of a
+// pair block), so it rounds the head's values to bf16 (the values a bf16 cache would hold),
+// takes their max magnitude, and writes scale = amax / 448 and the e4m3 codes of value /
+// scale (float32 division, round to nearest even) - the arithmetic of the separate quantize
+// pass - straight into the cache.
+
+// Whether the pair block starting at column n0 is a K or V head quantized in the epilogue.
+__device__ __forceinline__ bool fp8_head_block(const EpiParams& p, int n0) {
+  return p.ks_pools != nullptr && (p.kind == EPI_WIDE_KV || (p.kind == EPI_QKV && n0 >= p.q_cols));
+}
+
+// Bias and (for K) RoPE of the K/V columns (n_lo + i, n_hi + i), i < 32, in place.
+__device__ __forceinline__ void kv_chunk_prep(const EpiParams& p, int m, int n_lo, int n_hi, float* a, float* b) {
+  if (p.bias) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      a[i] += p.bias[n_lo + i];
+      b[i] += p.bias[n_hi + i];
+    }
+  }
+  const int dh = p.d_head, kvc = p.n_kv * dh;
+  const int c = p.kind == EPI_QKV ? n_lo - p.q_cols : n_lo % (2 * kvc);
+  if (c < kvc) {
+    const int pos = p.positions[m], i0 = c % dh;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) rope_rotate(p, pos, i0 + i, a[i], b[i]);
+  }
+}
+
+// Codes, scale and expansion of the head whose pair block starts at column n0 for row m; pk
+// holds its 2 * half values as bf16 pairs in dimension order, amax their largest magnitude.
+__device__ __forceinline__ void store_head_fp8(const EpiParams& p, int m, int n0, const uint32_t* pk, float amax) {
+  const int slot = p.slots[m];
+  if (slot < 0) return;
+  const int dh = p.d_head, kvc = p.n_kv * dh;
+  int c, cache;
+  if (p.kind == EPI_QKV) {
+    c = n0 - p.q_cols;
+    cache = p.cache_base;
+  } else {
+    const int grp = n0 / (2 * kvc);
+    c = n0 - grp * 2 * kvc;
+    cache = p.cache_base + grp;
+  }
+  const bool is_k = c < kvc;
+  const int head = (is_k ? c : c - kvc) / dh;
+  const size_t rowoff = ((size_t)(slot >> 4) * p.n_kv + head) * kPageSize + (slot & 15);
+  const float scale = amax / 448.f;
+  uint8_t* dst = reinterpret_cast<uint8_t* const*>(is_k ? p.k_pools : p.v_pools)[cache] + rowoff * dh;
+  bf16* ex = is_k ? p.exp_k : p.exp_v;
+  for (int q = 0; q < dh / 16; ++q) {  // 16 dimensions per 16-byte store
+    uint32_t w[4], e[8];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      uint32_t cc = 0;
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const uint32_t pr = pk[q * 8 + r * 2 + h2];
+        const float v0 = __uint_as_float(pr << 16), v1 = __uint_as_float(pr & 0xffff0000u);
+        const uint16_t c2 = scale > 0.f ? e4m3x2_from_f32(v0 / scale, v1 / scale) : (uint16_t)0;
+        cc |= (uint32_t)c2 << (16 * h2);
+        if (ex) {
+          const uint32_t hh = f16x2_from_e4m3x2(c2);
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hh));
+          e[r * 2 + h2] = pack_bf16_(f.x, f.y);
+        }
+      }
+      w[r] = cc;
+    }
+    *reinterpret_cast<uint4*>(dst + q * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (ex) {
+      bf16* er = ex + rowoff * dh + q * 16;
+      *reinterpret_cast<uint4*>(er) = make_uint4(e[0], e[1], e[2], e[3]);
+      *reinterpret_cast<uint4*>(er + 8) = make_uint4(e[4], e[5], e[6], e[7]);
+    }
+  }
+  (is_k ? p.ks_pools : p.vs_pools)[cache][rowoff] = scale;
 }
 
 // ---------------------------------------------------------------------------- programmatic launch
@@ -369,6 +510,16 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two softmax weights p0, p1 (>= 0, finite) as bfloat16 high and low parts, packed bf16x2
+// with p0's part in the low half: the high part is the float32 encoding with its low 16 bits
+// cleared, the low part the remainder (exact in float32) rounded to the nearest bf16, so
+// hi + lo equals p to within 2^-15 |p|.
+__device__ __forceinline__ void split_pair_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+  hi = __byte_perm(b0, b1, 0x7632);
+  lo = pack_bf16(p0 - __uint_as_float(b0 & 0xffff0000u), p1 - __uint_as_float(b1 & 0xffff0000u));
 }
 
 }  // namespace skv

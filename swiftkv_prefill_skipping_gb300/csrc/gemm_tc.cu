@@ -30,6 +30,7 @@ namespace {
 using namespace tc;
 
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+static_assert(BN == kNormTile, "fused RMSNorm sums of squares are kept per 256-column GEMM tile");
 constexpr int A_BYTES = BM * BK * 2;          // 16 KB
 constexpr int B_BYTES = BN * BK * 2;          // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -177,16 +178,47 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const float rs = (ep.norm_part && row < M) ? fused_norm_scale(ep, row) : 1.f;
+      float ssq = 0.f;  // fused RMSNorm: the row's sum of squares over this 256-column tile
       for (int b0 = 0; b0 < BN; b0 += 2 * half) {
         const int ncol = nt * BN + b0;
         if (ncol >= N) break;
+        if (fp8_head_block(ep, ncol)) {
+          // one K or V head of an FP8 cache: bf16 values, their max, codes and scale
+          uint32_t pk[64];
+          float amax = 0.f;
+          for (int c = 0; c < half; c += 32) {
+            float lo[32], hi[32];
+            tmem_ld32(tb + b0 + c, lo);
+            tmem_ld32(tb + b0 + half + c, hi);
+            if (row < M) kv_chunk_prep(ep, row, ncol + c, ncol + half + c, lo, hi);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const uint32_t pl = pack_bf16_(lo[i], lo[i + 1]), ph = pack_bf16_(hi[i], hi[i + 1]);
+              pk[(c + i) >> 1] = pl;
+              pk[(half + c + i) >> 1] = ph;
+              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(pl << 16))), fabsf(__uint_as_float(pl & 0xffff0000u)));
+              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(ph << 16))), fabsf(__uint_as_float(ph & 0xffff0000u)));
+            }
+          }
+          if (row < M) store_head_fp8(ep, row, ncol, pk, amax);
+          continue;
+        }
         for (int c = 0; c < half; c += 32) {
           float lo[32], hi[32];
           tmem_ld32(tb + b0 + c, lo);
           tmem_ld32(tb + b0 + half + c, hi);
-          if (row < M) apply_chunk32(ep, row, ncol + c, ncol + half + c, lo, hi);
+          if (ep.norm_part) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              lo[i] *= rs;
+              hi[i] *= rs;
+            }
+          }
+          if (row < M) ssq += apply_chunk32(ep, row, ncol + c, ncol + half + c, lo, hi);
         }
       }
+      if (ep.ss_out && row < M) ep.ss_out[(size_t)row * norm_tiles(N) + nt] = ssq;
       tc_fence_before();
       mbar_arrive(tempty(acc));
     }
@@ -362,16 +394,47 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_pair_kernel(const __grid_c
       tc_fence_after();
       const int row = mt * BM + q * 32 + lane;
       const uint32_t tb = tmem + ((uint32_t)(q * 32) << 16) + acc * BN;
+      const float rs = (ep.norm_part && row < M) ? fused_norm_scale(ep, row) : 1.f;
+      float ssq = 0.f;  // fused RMSNorm: the row's sum of squares over this 256-column tile
       for (int b0 = 0; b0 < BN; b0 += 2 * half) {
         const int ncol = nt * BN + b0;
         if (ncol >= N) break;
+        if (fp8_head_block(ep, ncol)) {
+          // one K or V head of an FP8 cache: bf16 values, their max, codes and scale
+          uint32_t pk[64];
+          float amax = 0.f;
+          for (int c = 0; c < half; c += 32) {
+            float lo[32], hi[32];
+            tmem_ld32(tb + b0 + c, lo);
+            tmem_ld32(tb + b0 + half + c, hi);
+            if (row < M) kv_chunk_prep(ep, row, ncol + c, ncol + half + c, lo, hi);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const uint32_t pl = pack_bf16_(lo[i], lo[i + 1]), ph = pack_bf16_(hi[i], hi[i + 1]);
+              pk[(c + i) >> 1] = pl;
+              pk[(half + c + i) >> 1] = ph;
+              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(pl << 16))), fabsf(__uint_as_float(pl & 0xffff0000u)));
+              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(ph << 16))), fabsf(__uint_as_float(ph & 0xffff0000u)));
+            }
+          }
+          if (row < M) store_head_fp8(ep, row, ncol, pk, amax);
+          continue;
+        }
         for (int c = 0; c < half; c += 32) {
           float lo[32], hi[32];
           tmem_ld32(tb + b0 + c, lo);
           tmem_ld32(tb + b0 + half + c, hi);
-          if (row < M) apply_chunk32(ep, row, ncol + c, ncol + half + c, lo, hi);
+          if (ep.norm_part) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              lo[i] *= rs;
+              hi[i] *= rs;
+            }
+          }
+          if (row < M) ssq += apply_chunk32(ep, row, ncol + c, ncol + half + c, lo, hi);
         }
       }
+      if (ep.ss_out && row < M) ep.ss_out[(size_t)row * norm_tiles(N) + nt] = ssq;
       tc_fence_before();
       mbar_arrive_cluster(mapa_shared(tempty(acc), 0));
     }

@@ -1,6 +1,7 @@
 // Internal launchers of the SwiftKV GB300 kernels (not part of the C ABI).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -46,6 +47,41 @@ cudaError_t launch_gemv(const bf16* A, int lda, const bf16* B, int K, const EpiP
 // outside its shapes, including matrices with fewer than num_sms / 2 tiles (launch_gemv then).
 cudaError_t launch_gemv_tma(const bf16* A, int lda, const bf16* W, int K, const EpiParams& ep, int num_sms,
                             int* status, cudaStream_t stream);
+// A chain of skinny GEMM and RMSNorm phases (M <= 64 rows) in one cooperative persistent
+// launch: phase p runs after every CTA has finished phase p - 1 (grid barrier on a
+// monotonically growing arrival counter; count_base is the count before the launch and is
+// advanced by the barriers the launch makes). Weights of later GEMM phases stream while
+// earlier phases run. cudaErrorNotSupported outside its shapes.
+constexpr int kChainMaxPhases = 6;
+struct ChainNorm {        // u[m][:] = bf16(rmsnorm(x[m][:]) * gamma), m < rows
+  const float* x;
+  const float* gamma;     // NULL: 1
+  bf16* u;
+  int rows, d, ldx, ldu;
+  float eps;
+};
+struct ChainStep {        // one phase: a GEMM (W != NULL) or an RMSNorm (W == NULL)
+  const bf16* A;
+  int lda;
+  const bf16* W;          // [N][K]
+  int K;
+  EpiParams ep;
+  ChainNorm norm;
+};
+struct ChainPhase {
+  CUtensorMap tmA, tmW;
+  EpiParams ep;
+  ChainNorm norm;
+  int is_norm, K, tiles, first_cta;  // tiles: 64-row weight tiles, or rows for a norm phase
+};
+struct ChainParams {
+  ChainPhase ph[kChainMaxPhases];
+  int n;
+  unsigned* count;
+  unsigned count_base;
+};
+cudaError_t launch_gemv_chain(const ChainStep* steps, int n, int num_sms, unsigned* count, unsigned* count_base,
+                              int* status, cudaStream_t stream);
 // tcgen05 (TMEM accumulator, TMA-fed) GEMM; returns cudaErrorNotSupported if the shape is not
 // handled, so the caller can fall back to launch_gemm_tiled.
 // mode 0: one CTA per 128 x 256 tile; 2: CTA pairs run tcgen05.mma.cta_group::2 on
@@ -87,12 +123,14 @@ cudaError_t launch_kv_quantize(const bf16* stage, int ld, int M, const int* slot
 // in its block-table row) of one cache into bf16 pools sk/sv of the same layout.
 cudaError_t launch_kv_dequant_pages(const int* items, int num_items, const int* block_table, int max_pages,
                                     int num_pages, int n_kv, int d_head, const uint8_t* k8, const uint8_t* v8,
-                                    const float* ks, const float* vs, bf16* sk, bf16* sv, cudaStream_t stream);
+                                    bf16* sk, bf16* sv, cudaStream_t stream);
 
 // ---- row kernels -------------------------------------------------------------------------
-// x[t] = embed[tok[t]] (fp32); u[t] = bf16(rmsnorm(x[t]) * gamma)
+// x[t] = embed[tok[t]] (fp32); u[t] = bf16(rmsnorm(x[t]) * gamma) (gamma NULL: 1), or with
+// ss_part (fused-norm path) u[t] = bf16(gamma * x[t]) and the row's sum of squares in
+// ss_part[t][0] (zeros in the other nparts - 1 slots)
 cudaError_t launch_embed_rmsnorm(const int* tokens, int T, const bf16* embed, int vocab, int d,
-                                 const float* gamma, float eps, float* x, bf16* u,
+                                 const float* gamma, float eps, float* x, bf16* u, float* ss_part, int nparts,
                                  cudaStream_t stream);
 // u[t] = bf16(rmsnorm(x[rows ? rows[t] : t]) * gamma); if x_out, x_out[t] = x[row] (gather).
 // gamma == nullptr means a gain of one.
@@ -107,7 +145,11 @@ cudaError_t launch_scale_columns(bf16* W, int rows, int K, const float* gamma, c
 // tiles: [num_tiles] (seq << 16 | q_tile) 64-row query tiles; cu: [P+1] device; ctx: [P]
 // device or nullptr: cached tokens before each chunk (row i at position ctx[s] + i sees
 // keys [0, ctx[s] + i]).
+// k_scale / v_scale (all three prompt kernels): NULL for a bf16 cache; for an FP8 cache the
+// pools hold the e4m3 codes as bf16 values and these the per-(page, head, row) float scales
+// [num_pages][n_kv][16]: scores take the key's scale and P the value's, in float32.
 cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool, const bf16* v_pool,
+                                     const float* k_scale, const float* v_scale,
                                      const int* block_table, int max_pages, int num_pages,
                                      const int* cu, const int* ctx, const int* tiles, int num_tiles, int n_q,
                                      int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream);
@@ -115,14 +157,14 @@ cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool,
 // only); tiles are 256-row tile pairs (seq << 16 | pair), heaviest first. Persistent: at most
 // num_sms CTAs, each walking its share of the (tile pair, head) items.
 cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
-                                         const int* block_table, int max_pages, int num_pages, const int* cu,
+                                         const float* k_scale, const float* v_scale, const int* block_table, int max_pages, int num_pages, const int* cu,
                                          const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
                                          int d_head, bf16* out, int ldo, int num_sms, int* status,
                                          cudaStream_t stream);
 // Same on tcgen05 (d_head 128 only; cudaErrorNotSupported otherwise). tiles are 128-row tiles;
 // T = rows of q. status receives kStatusTimeout if a bounded wait expires.
 cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
-                                        const int* block_table, int max_pages, int num_pages, const int* cu,
+                                        const float* k_scale, const float* v_scale, const int* block_table, int max_pages, int num_pages, const int* cu,
                                         const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
                                         int d_head, bf16* out, int ldo, int* status, cudaStream_t stream);
 // B single query rows: item b is row r = rows[b] of q / out (r = b if rows is null) at

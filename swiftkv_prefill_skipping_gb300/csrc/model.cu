@@ -61,6 +61,7 @@ struct Workspace {
   bf16 *kv_stage;         // FP8 cache: staged K/V rows before quantization
   bf16 *exp_k, *exp_v;    // FP8 cache: bf16 expansion of one cache for the prompt-tile attention
   int* deq_items;         // FP8 cache: (sequence, page) pairs of cached prefixes to expand
+  float *ss_attn, *ss_mlp;  // fused RMSNorm: per-256-column sums of squares of x after the O / down GEMM
 };
 
 constexpr int kShortChunk = 4;  // chunks up to this many rows take the single-row attention kernel
@@ -93,6 +94,10 @@ struct swiftkv_model {
   bool globals_loaded = false;
   int gemm_impl = 0;  // 0 tcgen05 CTA pairs, 1 mma.sync tiles, 2 tcgen05 single CTA (GEMMs with > 64 rows)
   int attn_impl = 0;  // 0 tcgen05 when d_head == 128, 1 mma.sync
+  bool norm_fusion = false;  // prompt rows: RMSNorm in the tcgen05 GEMM epilogues (else its own pass)
+  int rows_impl = 1;  // tail / decode rows after attention: 0 one chained launch, 1 a launch per GEMM / norm
+  unsigned* chain_count = nullptr;  // grid-barrier arrivals of the chained launches (device)
+  unsigned chain_base = 0;          // ... and their count so far (host)
   // profiling (swiftkv_profile_begin/end)
   bool prof_on = false;
   struct Rec {
@@ -193,6 +198,8 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
       stage_elems * 2,               // staged K/V rows (FP8 cache)
       exp_elems * 2, exp_elems * 2,  // bf16 expansion of one cache (FP8 cache)
       deq_ints * 4,                  // prefix pages to expand
+      (size_t)T * norm_tiles(c.d) * 4,  // fused RMSNorm sums of squares after attention
+      (size_t)T * norm_tiles(c.d) * 4,  // ... and after the MLP (or the embedding)
   };
   const int n = sizeof(sizes) / sizeof(sizes[0]);
   size_t off[32], total = 0;
@@ -244,6 +251,8 @@ int ensure_workspace(swiftkv_model* m, int T, int P, int C, int ntiles, size_t p
   w->exp_k = (bf16*)(b + off[26]);
   w->exp_v = (bf16*)(b + off[27]);
   w->deq_items = (int*)(b + off[28]);
+  w->ss_attn = (float*)(b + off[29]);
+  w->ss_mlp = (float*)(b + off[30]);
   return SWIFTKV_OK;
 }
 
@@ -278,6 +287,11 @@ struct Ctx {
   float* const* vs_dev = nullptr;
   bool expand = false;       // FP8: prompt tiles read a bf16 expansion of the layer's cache
   int n_deq = 0;             // FP8: prefix pages to expand per full layer (w.deq_items)
+  // RMSNorm fused into the prompt rows' tcgen05 GEMMs: the O and down epilogues leave
+  // bf16(gamma * x) in w.u (gamma: the next norm's gain) and per-tile sums of squares of x in
+  // w.ss_attn / w.ss_mlp, which the next GEMM's epilogue turns into the row's 1/rms; no
+  // separate norm pass over the prompt rows
+  bool fused = false;
 };
 
 // Host side of a key-split plan: units then ubeg in one vector (one upload).
@@ -339,12 +353,22 @@ struct Prof {
   ~Prof() {
     if (idx >= 0) cudaEventRecord(m->recs[idx].b, s);
   }
+  // The bracketed launch did not happen: drop the record (the last one taken).
+  void cancel() {
+    if (idx < 0) return;
+    m->recs.pop_back();
+    m->ev_used -= 2;
+    idx = -1;
+  }
 };
 
 int gemm(Ctx& x, const char* name, const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep,
          double flops) {
   const bool skinny = ep.M <= 64;
   const double bytes = (double)ep.N * K * 2 + (double)ep.M * K * 2;
+  const bool fused = ep.norm_part || ep.xb_out || ep.ks_pools;
+  if (fused && (skinny || x.m->gemm_impl == 1))
+    return fail(SWIFTKV_EUNSUPPORTED, "fused RMSNorm / FP8 epilogue needs the tcgen05 GEMM (M=%d)", ep.M);
   Prof pr(x.m, x.s, name, 1, flops, bytes);
   cudaError_t e;
   if (skinny) {
@@ -355,7 +379,7 @@ int gemm(Ctx& x, const char* name, const bf16* A, int lda, const bf16* B, int K,
     e = cudaErrorNotSupported;
     if (x.m->gemm_impl == 0) e = launch_gemm_tc(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s, 2);
     else if (x.m->gemm_impl == 2) e = launch_gemm_tc(A, lda, B, K, ep, x.m->num_sms, x.m->status, x.s, 0);
-    if (e == cudaErrorNotSupported) e = launch_gemm_tiled(A, lda, B, K, ep, x.s);
+    if (e == cudaErrorNotSupported && !fused) e = launch_gemm_tiled(A, lda, B, K, ep, x.s);
   }
   if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "gemm M=%d N=%d K=%d: %s", ep.M, ep.N, K, cudaGetErrorString(e));
   return SWIFTKV_OK;
@@ -377,6 +401,37 @@ EpiParams epi_base(Ctx& x, int kind, int M, int N) {
   return p;
 }
 
+// The GEMM's A operand is bf16(gamma * x) from the fused path; its epilogue applies the
+// RMSNorm row scale from the sums of squares in ss.
+void fuse_input(Ctx& x, EpiParams& e, const float* ss) {
+  e.norm_part = ss;
+  e.norm_parts = norm_tiles(x.m->cfg.d);
+  e.norm_inv_dim = 1.f / (float)x.m->cfg.d;
+  e.norm_eps = x.m->cfg.rms_eps;
+}
+
+// A residual-update GEMM of the fused path also leaves bf16(gamma * x) in xb (gamma: the gain
+// of the norm that reads x next; NULL for the wide KV GEMM, whose weights carry their gains)
+// and the new row's sums of squares in ss.
+void fuse_output(EpiParams& e, bf16* xb, const float* gamma, float* ss) {
+  e.xb_out = xb;
+  e.xb_gamma = gamma;
+  e.ss_out = ss;
+}
+
+// Whether an FP8 cache is quantized in the K/V GEMM's own epilogue: the tcgen05 GEMMs (more
+// than 64 rows) do it; the skinny ones stage the bf16 rows for the quantize pass.
+bool fp8_in_epilogue(const Ctx& x, int M) { return x.fp8 && M > 64 && x.m->gemm_impl != 1; }
+
+void set_fp8_epilogue(Ctx& x, EpiParams& e, bool expand) {
+  e.ks_pools = const_cast<float* const*>(x.ks_dev);
+  e.vs_pools = const_cast<float* const*>(x.vs_dev);
+  if (expand) {
+    e.exp_k = x.w.exp_k;
+    e.exp_v = x.w.exp_v;
+  }
+}
+
 int norm(Ctx& x, const float* src, const int* rows, int T, const float* gamma, bf16* u, float* xout) {
   Prof pr(x.m, x.s, "rmsnorm", 1, 0.0, (double)T * x.m->cfg.d * (xout ? 10 : 6));
   CK(launch_rmsnorm(src, rows, T, x.m->cfg.d, gamma, x.m->cfg.rms_eps, u, xout, x.s));
@@ -386,7 +441,8 @@ int norm(Ctx& x, const float* src, const int* rows, int T, const float* gamma, b
 // Attention output + O projection + MLP of layer j for rows [0, M) of (xres, q), reading
 // the layer's cache; `prefill` selects the varlen prompt kernel, else one query per row.
 int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, bf16* hb, bool prefill,
-               const int* qpos, int ntiles, const char* gname, double attn_flops, double attn_bytes) {
+               const int* qpos, int ntiles, const char* gname, double attn_flops, double attn_bytes,
+               bool attn_only = false) {
   swiftkv_model* m = x.m;
   const auto& c = m->cfg;
   const LayerW& L = m->layers[j];
@@ -413,41 +469,51 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
     return r;
   };
   auto launches = [&](const SplitPlan& sp) { return m->attn_impl == 0 || x.fp8 ? 1 + (int)sp.any_split : 1; };
-  // prompt tiles read the bf16 expansion of the layer's cache when the cache is FP8
+  // prompt tiles read the bf16 expansion (the e4m3 codes as bf16) of the layer's cache when
+  // the cache is FP8, with its scales applied in the attention kernel
   const bf16* tkp = x.fp8 ? x.w.exp_k : kp;
   const bf16* tvp = x.fp8 ? x.w.exp_v : vp;
+  const float* tks = x.fp8 ? static_cast<const float*>(x.kv->k_scale[cidx]) : nullptr;
+  const float* tvs = x.fp8 ? static_cast<const float*>(x.kv->v_scale[cidx]) : nullptr;
   {
   Prof pr(x.m, x.s, prefill ? "attn_prefill" : "attn_decode",
           prefill ? (ntiles > 0) + (x.nshort > 0 ? launches(x.sp_short) : 0) : launches(x.sp_rows), attn_flops,
           attn_bytes);
   if (prefill && x.tc_attn && m->attn_impl == 0)
-    e = launch_attention_prefill_tc2(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
+    e = launch_attention_prefill_tc2(qb, m->Nq, M, tkp, tvp, tks, tvs, x.kv->block_table, x.kv->max_pages_per_seq,
                                      x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
                                      m->Nq, m->num_sms, m->status, x.s);
   else if (prefill && x.tc_attn)
-    e = launch_attention_prefill_tc(qb, m->Nq, M, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq,
+    e = launch_attention_prefill_tc(qb, m->Nq, M, tkp, tvp, tks, tvs, x.kv->block_table, x.kv->max_pages_per_seq,
                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
                                     m->Nq, m->status, x.s);
   else if (prefill)
-    e = launch_attention_prefill(qb, m->Nq, tkp, tvp, x.kv->block_table, x.kv->max_pages_per_seq, x.kv->num_pages,
+    e = launch_attention_prefill(qb, m->Nq, tkp, tvp, tks, tvs, x.kv->block_table, x.kv->max_pages_per_seq,
+                                 x.kv->num_pages,
                                  x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab, m->Nq, x.s);
   else
     e = rows_attn(qpos, M, nullptr, nullptr, x.sp_rows);
   if (e == cudaSuccess && prefill && x.nshort > 0) e = rows_attn(x.w.positions, x.nshort, x.w.srow, x.w.sseq, x.sp_short);
   }
   if (e != cudaSuccess) return fail(SWIFTKV_ECUDA, "attention layer %d: %s", j, cudaGetErrorString(e));
+  if (attn_only) return SWIFTKV_OK;
+  const bool fused = prefill && x.fused;  // prompt rows on the fused-norm path
   EpiParams eo = epi_base(x, EPI_RESID, M, c.d);
   eo.ldo = c.d;
   eo.out_f32 = xres;
+  if (fused) fuse_output(eo, ub, L.g_mlp, x.w.ss_attn);
   RET(gemm(x, gname, ab, m->Nq, L.wo, m->Nq, eo, 2.0 * M * c.d * m->Nq));
-  RET(norm(x, xres, nullptr, M, L.g_mlp, ub, nullptr));
+  if (!fused) RET(norm(x, xres, nullptr, M, L.g_mlp, ub, nullptr));
   EpiParams eg = epi_base(x, EPI_SWIGLU, M, 2 * m->Fp);
   eg.ldo = m->Fp;
   eg.out_bf16 = hb;
+  if (fused) fuse_input(x, eg, x.w.ss_attn);
   RET(gemm(x, gname, ub, c.d, L.wgu, c.d, eg, 2.0 * M * 2 * c.ffn * c.d));
   EpiParams ed = epi_base(x, EPI_RESID, M, c.d);
   ed.ldo = c.d;
   ed.out_f32 = xres;
+  // the next norm: layer j + 1's input norm, or none before the wide KV GEMM (l = j + 1)
+  if (fused) fuse_output(ed, ub, j + 1 < m->l ? m->layers[j + 1].g_attn : nullptr, x.w.ss_mlp);
   RET(gemm(x, gname, hb, m->Fp, L.wd, m->Fp, ed, 2.0 * M * c.d * c.ffn));
   return SWIFTKV_OK;
 }
@@ -464,8 +530,9 @@ int quantize(Ctx& x, int M, const int* slots, int groups, int cache_base, int ld
   return SWIFTKV_OK;
 }
 
-// Q/K/V (full layer: cache_base = j) or Q only (skipped layer) projection with RoPE.
-int qkv(Ctx& x, int j, int M, const bf16* ub, bf16* qb, const int* pos, const int* slots, const char* gname) {
+// Epilogue of layer j's Q/K/V (full layer: cache_base = j) or Q only (skipped layer)
+// projection with RoPE.
+EpiParams qkv_epi(Ctx& x, int j, int M, bf16* qb, const int* pos, const int* slots) {
   swiftkv_model* m = x.m;
   const LayerW& L = m->layers[j];
   const bool full = j < m->l;
@@ -478,30 +545,126 @@ int qkv(Ctx& x, int j, int M, const bf16* ub, bf16* qb, const int* pos, const in
   e.slots = slots;
   e.cache_base = j;
   if (full && x.fp8) {
-    e.kv_stage = x.w.kv_stage;
-    e.kv_stage_ld = 2 * m->Nkv;
+    if (fp8_in_epilogue(x, M)) {
+      set_fp8_epilogue(x, e, x.expand);
+    } else {
+      e.kv_stage = x.w.kv_stage;
+      e.kv_stage_ld = 2 * m->Nkv;
+    }
   }
-  RET(gemm(x, gname, ub, m->cfg.d, L.wqkv, m->cfg.d, e, 2.0 * M * e.N * m->cfg.d));
-  if (full && x.fp8) RET(quantize(x, M, slots, 1, j, 2 * m->Nkv, x.expand));
+  return e;
+}
+
+int qkv(Ctx& x, int j, int M, const bf16* ub, bf16* qb, const int* pos, const int* slots, const char* gname,
+        bool fused = false) {
+  swiftkv_model* m = x.m;
+  const bool full = j < m->l;
+  EpiParams e = qkv_epi(x, j, M, qb, pos, slots);
+  if (fused) fuse_input(x, e, x.w.ss_mlp);
+  RET(gemm(x, gname, ub, m->cfg.d, m->layers[j].wqkv, m->cfg.d, e, 2.0 * M * e.N * m->cfg.d));
+  if (full && x.fp8 && !fp8_in_epilogue(x, M)) RET(quantize(x, M, slots, 1, j, 2 * m->Nkv, x.expand));
+  return SWIFTKV_OK;
+}
+
+// Rows after layer j's attention (in ab), one launch per step: O (+ residual into xres) ->
+// RMSNorm (gamma_mlp) -> gate/up (+ SwiGLU) -> down (+ residual).
+int mlp_rows(Ctx& x, int j, int M, float* xres, const bf16* ab, bf16* ub, bf16* hb, const char* gname) {
+  swiftkv_model* m = x.m;
+  const auto& c = m->cfg;
+  const LayerW& L = m->layers[j];
+  EpiParams eo = epi_base(x, EPI_RESID, M, c.d);
+  eo.ldo = c.d;
+  eo.out_f32 = xres;
+  RET(gemm(x, gname, ab, m->Nq, L.wo, m->Nq, eo, 2.0 * M * c.d * m->Nq));
+  RET(norm(x, xres, nullptr, M, L.g_mlp, ub, nullptr));
+  EpiParams eg = epi_base(x, EPI_SWIGLU, M, 2 * m->Fp);
+  eg.ldo = m->Fp;
+  eg.out_bf16 = hb;
+  RET(gemm(x, gname, ub, c.d, L.wgu, c.d, eg, 2.0 * M * 2 * c.ffn * c.d));
+  EpiParams ed = epi_base(x, EPI_RESID, M, c.d);
+  ed.ldo = c.d;
+  ed.out_f32 = xres;
+  RET(gemm(x, gname, hb, m->Fp, L.wd, m->Fp, ed, 2.0 * M * c.d * c.ffn));
+  return SWIFTKV_OK;
+}
+
+// Rows M <= 64 after layer j's attention (in ab), as one chained launch: O (+ residual into
+// xres) -> RMSNorm (gamma_mlp) -> gate/up (+ SwiGLU) -> down (+ residual) -> RMSNorm with
+// g_next (if g_next_set) -> the next GEMM (if next_W: A = ub, weight next_W, epilogue
+// next_ep). Returns SWIFTKV_EUNSUPPORTED, with nothing enqueued, where the chained kernel
+// does not apply; the caller then runs the same steps one launch each.
+int chain_rest(Ctx& x, int j, int M, float* xres, const bf16* ab, bf16* ub, bf16* hb, bool g_next_set,
+               const float* g_next, const bf16* next_W, const EpiParams* next_ep, const char* gname) {
+  swiftkv_model* m = x.m;
+  const auto& c = m->cfg;
+  const LayerW& L = m->layers[j];
+  if (m->rows_impl != 0 || M > 64) return SWIFTKV_EUNSUPPORTED;
+  ChainStep st[kChainMaxPhases];
+  memset(st, 0, sizeof st);
+  int n = 0;
+  double flops = 0, bytes = 0;
+  auto add_gemm = [&](const bf16* A, int lda, const bf16* W, int K, const EpiParams& ep) {
+    st[n].A = A;
+    st[n].lda = lda;
+    st[n].W = W;
+    st[n].K = K;
+    st[n].ep = ep;
+    ++n;
+    flops += 2.0 * M * ep.N * K;
+    bytes += (double)ep.N * K * 2 + (double)M * K * 2;
+  };
+  auto add_norm = [&](const float* gamma) {
+    st[n].norm = ChainNorm{xres, gamma, ub, M, c.d, c.d, c.d, c.rms_eps};
+    ++n;
+    bytes += (double)M * c.d * 6;
+  };
+  EpiParams eo = epi_base(x, EPI_RESID, M, c.d);
+  eo.ldo = c.d;
+  eo.out_f32 = xres;
+  add_gemm(ab, m->Nq, L.wo, m->Nq, eo);
+  add_norm(L.g_mlp);
+  EpiParams eg = epi_base(x, EPI_SWIGLU, M, 2 * m->Fp);
+  eg.ldo = m->Fp;
+  eg.out_bf16 = hb;
+  add_gemm(ub, c.d, L.wgu, c.d, eg);
+  EpiParams ed = epi_base(x, EPI_RESID, M, c.d);
+  ed.ldo = c.d;
+  ed.out_f32 = xres;
+  add_gemm(hb, m->Fp, L.wd, m->Fp, ed);
+  if (g_next_set) add_norm(g_next);
+  if (next_W) add_gemm(ub, c.d, next_W, c.d, *next_ep);
+  Prof pr(m, x.s, gname, 1, flops, bytes);
+  const cudaError_t e = launch_gemv_chain(st, n, m->num_sms, m->chain_count, &m->chain_base, m->status, x.s);
+  if (e != cudaSuccess) {
+    // nothing was enqueued (unsupported shape, or a cooperative launch this device cannot
+    // take): the caller runs the same steps one launch each
+    cudaGetLastError();
+    pr.cancel();
+    return SWIFTKV_EUNSUPPORTED;
+  }
   return SWIFTKV_OK;
 }
 
 // Boundary: one row-RMS of x_l (gains folded into W_KV) and the wide KV GEMM into the
-// skipped caches.
-int wide_kv(Ctx& x, int M, const float* xres, bf16* ub, const int* pos, const int* slots) {
+// skipped caches. On the fused path the RMS comes from the last down GEMM's sums of squares.
+int wide_kv(Ctx& x, int M, const float* xres, bf16* ub, const int* pos, const int* slots, bool fused = false) {
   swiftkv_model* m = x.m;
-  RET(norm(x, xres, nullptr, M, nullptr, ub, nullptr));
+  if (!fused) RET(norm(x, xres, nullptr, M, nullptr, ub, nullptr));
   EpiParams e = epi_base(x, EPI_WIDE_KV, M, m->Nwide);
+  if (fused) fuse_input(x, e, x.w.ss_mlp);
   e.bias = m->b_wide;
   e.positions = pos;
   e.slots = slots;
   e.cache_base = m->l;
-  if (x.fp8) {
+  const bool in_epi = fp8_in_epilogue(x, M);
+  if (x.fp8 && in_epi) {
+    set_fp8_epilogue(x, e, false);  // skipped caches are read only by the single-row attention
+  } else if (x.fp8) {
     e.kv_stage = x.w.kv_stage;
     e.kv_stage_ld = m->Nwide;
   }
   RET(gemm(x, "gemm_wide_kv", ub, m->cfg.d, m->w_wide, m->cfg.d, e, 2.0 * M * m->Nwide * m->cfg.d));
-  if (x.fp8) RET(quantize(x, M, slots, m->G, m->l, m->Nwide, false));
+  if (x.fp8 && !in_epi) RET(quantize(x, M, slots, m->G, m->l, m->Nwide, false));
   return SWIFTKV_OK;
 }
 
@@ -618,7 +781,8 @@ int swiftkv_model_create(const swiftkv_model_config* cfg, int l, int g, swiftkv_
     if (cfg->qkv_bias && (r = dalloc_t(m, &m->b_wide, m->Nwide))) return bail(r);
   }
   if ((r = dalloc_t(m, &m->embed, (size_t)cfg->vocab * d)) || (r = dalloc_t(m, &m->lm_head, (size_t)cfg->vocab * d)) ||
-      (r = dalloc_t(m, &m->g_final, d)) || (r = dalloc_t(m, &m->status, 1)))
+      (r = dalloc_t(m, &m->g_final, d)) || (r = dalloc_t(m, &m->status, 1)) ||
+      (r = dalloc_t(m, &m->chain_count, 1)))
     return bail(r);
   const int half = cfg->d_head / 2;
   if ((r = dalloc_t(m, &m->inv_freq, half)) || (r = dalloc_t(m, &m->rope_tab, (size_t)kRopeLen * half)))
@@ -637,7 +801,7 @@ int swiftkv_model_create(const swiftkv_model_config* cfg, int l, int g, swiftkv_
     }
   if (cudaMemcpy(m->inv_freq, inv.data(), half * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(m->rope_tab, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemset(m->status, 0, 4) != cudaSuccess)
+      cudaMemset(m->status, 0, 4) != cudaSuccess || cudaMemset(m->chain_count, 0, 4) != cudaSuccess)
     return bail(fail(SWIFTKV_ECUDA, "rope table upload"));
   *out = m;
   return SWIFTKV_OK;
@@ -743,6 +907,10 @@ int swiftkv_status(swiftkv_model* m, int clear) {
   int v = 0;
   CK(cudaMemcpy(&v, m->status, 4, cudaMemcpyDeviceToHost));
   if (clear) CK(cudaMemset(m->status, 0, 4));
+  if (clear && v != 0) {  // an expired wait may have left the chained launches' barrier count short
+    CK(cudaMemset(m->chain_count, 0, 4));
+    m->chain_base = 0;
+  }
   return v;
 }
 
@@ -750,6 +918,20 @@ int swiftkv_set_gemm_impl(swiftkv_model* m, int impl) {
   if (!m) return fail(SWIFTKV_EINVAL, "null model");
   if (impl < 0 || impl > 2) return fail(SWIFTKV_EINVAL, "gemm impl %d", impl);
   m->gemm_impl = impl;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_set_rows_impl(swiftkv_model* m, int impl) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  if (impl != 0 && impl != 1) return fail(SWIFTKV_EINVAL, "rows impl %d", impl);
+  m->rows_impl = impl;
+  return SWIFTKV_OK;
+}
+
+int swiftkv_set_norm_fusion(swiftkv_model* m, int on) {
+  if (!m) return fail(SWIFTKV_EINVAL, "null model");
+  if (on != 0 && on != 1) return fail(SWIFTKV_EINVAL, "norm fusion %d", on);
+  m->norm_fusion = on != 0;
   return SWIFTKV_OK;
 }
 
@@ -976,34 +1158,48 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
                          x.w.positions, x.w.slots, x.w.last_idx, x.w.last_pos, m->status, s));
   }
   const auto& c = m->cfg;
+  // more than 64 prompt rows run on the tcgen05 GEMMs, which take the RMSNorm in their epilogues
+  x.fused = m->norm_fusion && T > 64 && m->gemm_impl != 1;
   {
   Prof pr(m, s, "embed_rmsnorm", 1, 0.0, (double)T * c.d * 8);
-  CK(launch_embed_rmsnorm(tok, T, m->embed, c.vocab, c.d, m->layers[0].g_attn, c.rms_eps, x.w.x, x.w.u, s));
+  CK(launch_embed_rmsnorm(tok, T, m->embed, c.vocab, c.d, m->layers[0].g_attn, c.rms_eps, x.w.x, x.w.u,
+                          x.fused ? x.w.ss_mlp : nullptr, norm_tiles(c.d), s));
   }
   // layers 1..l in full for every prompt token
   for (int j = 0; j < m->l; ++j) {
-    if (j > 0) RET(norm(x, x.w.x, nullptr, T, m->layers[j].g_attn, x.w.u, nullptr));
+    if (j > 0 && !x.fused) RET(norm(x, x.w.x, nullptr, T, m->layers[j].g_attn, x.w.u, nullptr));
     if (x.n_deq > 0) {
       Prof pr(m, s, "kv_dequant", 1, 0.0,
               (double)x.n_deq * 2 * c.n_kv * kPageSize * (c.d_head * 3.0 + 4.0));
       CK(launch_kv_dequant_pages(x.w.deq_items, x.n_deq, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
                                  c.n_kv, c.d_head, static_cast<const uint8_t*>(kv->k_pool[j]),
-                                 static_cast<const uint8_t*>(kv->v_pool[j]), static_cast<const float*>(kv->k_scale[j]),
-                                 static_cast<const float*>(kv->v_scale[j]), x.w.exp_k, x.w.exp_v, s));
+                                 static_cast<const uint8_t*>(kv->v_pool[j]), x.w.exp_k, x.w.exp_v, s));
     }
-    RET(qkv(x, j, T, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_layers"));
+    RET(qkv(x, j, T, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_layers", x.fused));
     RET(layer_rest(x, j, T, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, true, nullptr, (int)tiles.size(),
                    "gemm_layers", attn_flops, attn_bytes));
   }
   // caches of every skipped layer / AcrossKV group from x_l
-  if (m->G > 0) RET(wide_kv(x, T, x.w.x, x.w.u, x.w.positions, x.w.slots));
+  if (m->G > 0) RET(wide_kv(x, T, x.w.x, x.w.u, x.w.positions, x.w.slots, x.fused));
   // last prompt token of each sequence: layers l+1..L
   RET(norm(x, x.w.x, x.w.last_idx, P, m->l < c.L ? m->layers[m->l].g_attn : m->g_final, x.w.ut, x.w.xt));
+  bool q_ready = false;  // the previous chained launch already computed this layer's Q
   for (int j = m->l; j < c.L; ++j) {
-    RET(qkv(x, j, P, x.w.ut, x.w.qt, x.w.last_pos, nullptr, "gemm_tail"));
+    if (!q_ready) RET(qkv(x, j, P, x.w.ut, x.w.qt, x.w.last_pos, nullptr, "gemm_tail"));
     RET(layer_rest(x, j, P, x.w.xt, x.w.qt, x.w.at, x.w.ut, x.w.ht, false, x.w.last_pos, 0, "gemm_tail",
-                   4.0 * c.n_q * c.d_head * tail_keys, tail_bytes));
-    RET(norm(x, x.w.xt, nullptr, P, j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final, x.w.ut, nullptr));
+                   4.0 * c.n_q * c.d_head * tail_keys, tail_bytes, true));
+    const float* g_next = j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final;
+    EpiParams eq;
+    if (j + 1 < c.L) eq = qkv_epi(x, j + 1, P, x.w.qt, x.w.last_pos, nullptr);
+    const int r = chain_rest(x, j, P, x.w.xt, x.w.at, x.w.ut, x.w.ht, true, g_next,
+                             j + 1 < c.L ? m->layers[j + 1].wqkv : nullptr, &eq, "gemm_tail");
+    q_ready = r == SWIFTKV_OK;
+    if (r == SWIFTKV_EUNSUPPORTED) {
+      RET(mlp_rows(x, j, P, x.w.xt, x.w.at, x.w.ut, x.w.ht, "gemm_tail"));
+      RET(norm(x, x.w.xt, nullptr, P, g_next, x.w.ut, nullptr));
+    } else {
+      RET(r);
+    }
   }
   EpiParams el = epi_base(x, EPI_STORE_F32, P, c.vocab);
   el.ldo = c.vocab;
@@ -1068,16 +1264,36 @@ int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   const auto& c = m->cfg;
   CK(launch_plan_decode(x.w.cu, B, tokens, c.vocab, kv->block_table, kv->max_pages_per_seq, kv->num_pages,
                         x.w.positions, x.w.slots, m->status, s));
-  CK(launch_embed_rmsnorm(tokens, B, m->embed, c.vocab, c.d, m->layers[0].g_attn, c.rms_eps, x.w.x, x.w.u, s));
+  CK(launch_embed_rmsnorm(tokens, B, m->embed, c.vocab, c.d, m->layers[0].g_attn, c.rms_eps, x.w.x, x.w.u, nullptr,
+                          0, s));
+  bool q_ready = false;  // the previous chained launch already computed this layer's Q/K/V
   for (int j = 0; j < c.L; ++j) {
     if (j == m->l && m->G > 0) {
       RET(wide_kv(x, B, x.w.x, x.w.u, x.w.positions, x.w.slots));
       RET(norm(x, x.w.x, nullptr, B, m->layers[j].g_attn, x.w.u, nullptr));
     }
-    RET(qkv(x, j, B, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_decode"));
+    if (!q_ready) RET(qkv(x, j, B, x.w.u, x.w.q, x.w.positions, x.w.slots, "gemm_decode"));
     RET(layer_rest(x, j, B, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, false, x.w.positions, 0, "gemm_decode",
-                   4.0 * c.n_q * c.d_head * dec_keys, dec_keys * kv_bytes_per_key(m, x.fp8) + 2.0 * B * m->Nq * 2));
-    RET(norm(x, x.w.x, nullptr, B, j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final, x.w.u, nullptr));
+                   4.0 * c.n_q * c.d_head * dec_keys, dec_keys * kv_bytes_per_key(m, x.fp8) + 2.0 * B * m->Nq * 2,
+                   true));
+    // the chained launch also runs the next layer's input norm and Q/K/V projection, except
+    // before the SwiftKV boundary (the wide KV GEMM normalises x_l itself)
+    const bool boundary_next = j + 1 == m->l && m->G > 0;
+    const bool next_qkv = j + 1 < c.L && !boundary_next;
+    const float* g_next = j + 1 < c.L ? m->layers[j + 1].g_attn : m->g_final;
+    EpiParams eq;
+    if (next_qkv) eq = qkv_epi(x, j + 1, B, x.w.q, x.w.positions, x.w.slots);
+    const int r = chain_rest(x, j, B, x.w.x, x.w.attn, x.w.u, x.w.h, !boundary_next, g_next,
+                             next_qkv ? m->layers[j + 1].wqkv : nullptr, &eq, "gemm_decode");
+    q_ready = r == SWIFTKV_OK && next_qkv;
+    if (r == SWIFTKV_EUNSUPPORTED) {
+      RET(mlp_rows(x, j, B, x.w.x, x.w.attn, x.w.u, x.w.h, "gemm_decode"));
+      RET(norm(x, x.w.x, nullptr, B, g_next, x.w.u, nullptr));
+    } else {
+      RET(r);
+      // K/V of the next full layer went to the staging rows: quantize them into the FP8 cache
+      if (q_ready && x.fp8 && j + 1 < m->l) RET(quantize(x, B, x.w.slots, 1, j + 1, 2 * m->Nkv, x.expand));
+    }
   }
   EpiParams el = epi_base(x, EPI_STORE_F32, B, c.vocab);
   el.ldo = c.vocab;

@@ -86,11 +86,17 @@ __device__ __forceinline__ void store_bf16x4(bf16* dst, float4 v) {
   *reinterpret_cast<uint2*>(dst) = pk;
 }
 
+// Embedding row of each token into the fp32 residual stream x, and the first layer's input:
+// without ss_part, u = bf16(RMSNorm(x) * gamma) (gamma NULL: 1); with ss_part (the fused-norm
+// path), u = bf16(gamma * x) and the row's sum of squares goes to ss_part[t][0] with zeros in
+// the other nparts - 1 slots, so a consumer summing the slots gets exactly the sum the unfused
+// path normalises by.
 __global__ void __launch_bounds__(RN_THREADS) embed_rmsnorm_kernel(const int* __restrict__ tokens,
                                                                    const bf16* __restrict__ embed, int vocab,
                                                                    int d, const float* __restrict__ gamma,
                                                                    float eps, float* __restrict__ x,
-                                                                   bf16* __restrict__ u) {
+                                                                   bf16* __restrict__ u, float* __restrict__ ss_part,
+                                                                   int nparts) {
   __shared__ float red[RN_THREADS / 32];
   const int t = blockIdx.x;
   int tok = tokens[t];
@@ -110,14 +116,23 @@ __global__ void __launch_bounds__(RN_THREADS) embed_rmsnorm_kernel(const int* __
       v[i] = make_float4(f0.x, f0.y, f1.x, f1.y);
       ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
       reinterpret_cast<float4*>(x + (size_t)t * d)[c] = v[i];
+      if (ss_part) {
+        const float4 g = gamma ? reinterpret_cast<const float4*>(gamma)[c] : make_float4(1.f, 1.f, 1.f, 1.f);
+        store_bf16x4(u + (size_t)t * d + 4 * c, make_float4(v[i].x * g.x, v[i].y * g.y, v[i].z * g.z, v[i].w * g.w));
+      }
     }
   }
-  const float r = rsqrtf(block_sum(ss, red) / d + eps);
+  const float total = block_sum(ss, red);
+  if (ss_part) {
+    for (int i = threadIdx.x; i < nparts; i += RN_THREADS) ss_part[(size_t)t * nparts + i] = i ? 0.f : total;
+    return;
+  }
+  const float r = rsqrtf(total / d + eps);
 #pragma unroll
   for (int i = 0; i < RN_MAXV; ++i) {
     int c = threadIdx.x + i * RN_THREADS;
     if (c < n4) {
-      float4 g = reinterpret_cast<const float4*>(gamma)[c];
+      const float4 g = gamma ? reinterpret_cast<const float4*>(gamma)[c] : make_float4(1.f, 1.f, 1.f, 1.f);
       float4 o = make_float4(v[i].x * r * g.x, v[i].y * r * g.y, v[i].z * r * g.z, v[i].w * r * g.w);
       store_bf16x4(u + (size_t)t * d + 4 * c, o);
     }
@@ -244,8 +259,9 @@ namespace {
 // One warp per staged (row m, group, K/V, head) vector of d_head bf16 values: per-vector
 // scale amax / 448, e4m3 codes of value / scale (float32 division, round to nearest even)
 // into the paged uint8 pool at the row's slot, the scale into the scale pool; with `sk`/`sv`
-// (groups == 1) the dequantized values also go, as bf16, into bf16 expansion pools of the
-// same layout for the prompt-tile attention.
+// (groups == 1) the codes also go, as bf16 (exact: e4m3 values are bf16 values), into bf16
+// expansion pools of the same layout for the prompt-tile attention, which applies the scales
+// itself in float32.
 template <int E>
 __global__ void kv_quantize_kernel(const bf16* __restrict__ stage, int ld, int M, const int* __restrict__ slots,
                                    int groups, int n_kv, int cache_base, uint8_t* const* k8, uint8_t* const* v8,
@@ -296,18 +312,17 @@ __global__ void kv_quantize_kernel(const bf16* __restrict__ stage, int ld, int M
     for (int i = 0; i < E; i += 2) {
       const uint32_t h = f16x2_from_e4m3x2(c2[i / 2]);
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-      *reinterpret_cast<__nv_bfloat162*>(ex + rowoff * DH + lane * E + i) =
-          __floats2bfloat162_rn(f.x * scale, f.y * scale);
+      *reinterpret_cast<__nv_bfloat162*>(ex + rowoff * DH + lane * E + i) = __floats2bfloat162_rn(f.x, f.y);
     }
   }
 }
 
-// Expands whole (page, all heads) blocks of one cache's uint8 pools into bf16 pools of the
-// same layout: item i = (sequence, page index) pairs; 16 codes per thread-step.
+// Expands whole (page, all heads) blocks of one cache's uint8 code pools into bf16 pools of
+// the same layout (exact: e4m3 values are bf16 values; the attention applies the scales):
+// item i = (sequence, page index) pairs; 16 codes per thread-step.
 __global__ void kv_dequant_pages_kernel(const int* __restrict__ items, const int* __restrict__ bt, int max_pages,
                                         int num_pages, int n_kv, int dh, const uint8_t* __restrict__ k8,
-                                        const uint8_t* __restrict__ v8, const float* __restrict__ ks,
-                                        const float* __restrict__ vs, bf16* sk, bf16* sv) {
+                                        const uint8_t* __restrict__ v8, bf16* sk, bf16* sv) {
   const int s = items[2 * blockIdx.x], pidx = items[2 * blockIdx.x + 1];
   const int page = bt[(size_t)s * max_pages + pidx];
   if (page < 0 || page >= num_pages) return;
@@ -316,7 +331,6 @@ __global__ void kv_dequant_pages_kernel(const int* __restrict__ items, const int
   for (int c = threadIdx.x; c < 2 * per_page / 16; c += blockDim.x) {
     const int kvsel = c >= per_page / 16;
     const int e = (c - kvsel * (per_page / 16)) * 16;  // element within the page
-    const float scale = (kvsel ? vs : ks)[(size_t)page * n_kv * kPageSize + e / dh];
     const uint4 raw = *reinterpret_cast<const uint4*>((kvsel ? v8 : k8) + base + e);
     const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
     uint32_t o[8];
@@ -326,7 +340,7 @@ __global__ void kv_dequant_pages_kernel(const int* __restrict__ items, const int
       for (int hh = 0; hh < 2; ++hh) {
         const uint32_t h = f16x2_from_e4m3x2((w[i] >> (16 * hh)) & 0xffffu);
         const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
-        __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(f.x, f.y);
         o[2 * i + hh] = *reinterpret_cast<uint32_t*>(&b2);
       }
     }
@@ -357,10 +371,10 @@ cudaError_t launch_kv_quantize(const bf16* stage, int ld, int M, const int* slot
 
 cudaError_t launch_kv_dequant_pages(const int* items, int num_items, const int* block_table, int max_pages,
                                     int num_pages, int n_kv, int d_head, const uint8_t* k8, const uint8_t* v8,
-                                    const float* ks, const float* vs, bf16* sk, bf16* sv, cudaStream_t stream) {
+                                    bf16* sk, bf16* sv, cudaStream_t stream) {
   if (num_items <= 0) return cudaSuccess;
   kv_dequant_pages_kernel<<<num_items, 256, 0, stream>>>(items, block_table, max_pages, num_pages, n_kv, d_head, k8,
-                                                          v8, ks, vs, sk, sv);
+                                                          v8, sk, sv);
   return cudaGetLastError();
 }
 
@@ -386,10 +400,10 @@ cudaError_t launch_plan_decode(const int* seq_lens, int B, const int* tokens, in
 }
 
 cudaError_t launch_embed_rmsnorm(const int* tokens, int T, const bf16* embed, int vocab, int d,
-                                 const float* gamma, float eps, float* x, bf16* u,
+                                 const float* gamma, float eps, float* x, bf16* u, float* ss_part, int nparts,
                                  cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  embed_rmsnorm_kernel<<<T, RN_THREADS, 0, stream>>>(tokens, embed, vocab, d, gamma, eps, x, u);
+  embed_rmsnorm_kernel<<<T, RN_THREADS, 0, stream>>>(tokens, embed, vocab, d, gamma, eps, x, u, ss_part, nparts);
   return cudaGetLastError();
 }
 

@@ -12,7 +12,8 @@ full model, a few GB on the device) and prints the per-kernel-class breakdown; i
 the small case for profiling the attention and norm kernels. `decode` prefills `batch`
 sequences of `ctx` tokens through a reduced-depth model with the Qwen2.5-14B layer shape
 (40 query heads, 8 KV heads, d_head 128) and times greedy decode steps from its bf16 or
-FP8 cache: the small case for the single-row attention and the skinny GEMMs.
+FP8 cache: the small case for the single-row attention and the skinny GEMMs (`--rows-impl 1`: one launch
+per GEMM and norm instead of the chained launch per layer).
 """
 from __future__ import annotations
 
@@ -104,6 +105,7 @@ def decode(args):
     shape = dataclasses.replace(synth.QWEN14B, L=args.layers, name=f"qwen2.5-14b-width-{args.layers}layers")
     batch = synth.prompt_batch(shape.vocab, args.batch, args.ctx, args.ctx, reserve_tokens=args.warmup + args.iters)
     m = api.load_synthetic(shape, args.l, args.g)
+    binding.check(binding.lib().swiftkv_set_rows_impl(m.handle, args.rows_impl))
     kv = api.KVCache(m, batch.num_pages, batch.block_table, dtype=args.kv)
     lg = api.prefill(m, torch.as_tensor(batch.tokens, device="cuda"), batch.cu_seqlens, kv)
     nxt = torch.argmax(lg, dim=-1).to(torch.int32)
@@ -112,6 +114,16 @@ def decode(args):
         _, nxt = api.decode_step(m, nxt, lens, kv)
         lens = [x + 1 for x in lens]
     torch.cuda.synchronize()
+    # whole steps without per-launch events, then the same number with them (breakdown)
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(args.iters):
+        _, nxt = api.decode_step(m, nxt, lens, kv)
+        lens = [x + 1 for x in lens]
+    e1.record(s)
+    torch.cuda.synchronize()
+    step_ms = e0.elapsed_time(e1) / args.iters
     binding.check(binding.lib().swiftkv_profile_begin(m.handle))
     for _ in range(args.iters):
         _, nxt = api.decode_step(m, nxt, lens, kv)
@@ -125,7 +137,7 @@ def decode(args):
         res[e.name.decode()] = {"ms_per_step": e.ms / args.iters, "calls": e.calls // args.iters,
                                 "gbs": e.bytes / (e.ms / 1e3) / 1e9 if e.bytes else None}
     print(json.dumps({"kernel": "decode", "batch": args.batch, "ctx": args.ctx, "kv": args.kv,
-                      "layers": args.layers, "classes": res}))
+                      "layers": args.layers, "rows_impl": args.rows_impl, "step_ms": step_ms, "classes": res}))
     assert m.status() == 0
 
 
@@ -155,6 +167,7 @@ def main():
     d.add_argument("--batch", type=int, default=24)
     d.add_argument("--ctx", type=int, default=1000)
     d.add_argument("--kv", choices=("bf16", "fp8"), default="bf16")
+    d.add_argument("--rows-impl", type=int, choices=(0, 1), default=0)
     d.add_argument("--iters", type=int, default=3)
     d.add_argument("--warmup", type=int, default=2)
     args = ap.parse_args()

@@ -10,6 +10,15 @@ from oracle import model as OM
 
 KV_REL_TOL = 1e-2      # per cache and K/V tensor: ||gpu - ref||_2 / ||ref||_2
 LOGIT_ABS_TOL = 5e-2   # last-token logits, max |gpu - ref|
+# Element-wise, per cache and K/V tensor: max |gpu - ref| / max |ref| (one wrong element or
+# row shows here even when it hides under the L2 norm).
+KV_MAXREL_TOL = 1e-2
+# The fused-RMSNorm mode (swiftkv_set_norm_fusion 1) rounds each GEMM input to bf16 at
+# gamma * x instead of gamma * x / rms, so about a quarter of the cache entries sit one bf16
+# ulp from the oracle's rounding already at the first layer. One ulp of a value just above a
+# power of two is 2^-7 of it, and after a few layers the largest entries may sit two ulps
+# apart: that mode's element-wise bound is two bf16 ulps of the largest value.
+FUSED_MAXREL_TOL = 2.0 ** -6
 
 # d_head = 128 shape with several 128-row GEMM tiles and attention tiles (tcgen05 attention)
 SMALL128 = synth.ModelShape("small-d128", L=6, d=512, n_q=4, n_kv=2, d_h=128, ffn=1000, vocab=2048,
@@ -33,6 +42,14 @@ def rel_l2(a, b) -> float:
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
 
 
+def max_rel(a, b) -> float:
+    """Element-wise error of a whole tensor: max |a - b| / max |b| (one bad element or row
+    shows here even when it hides under the L2 norm)."""
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return float(np.abs(a - b).max() / max(np.abs(b).max(), 1e-30))
+
+
 def run_gpu_prefill(shape, l, g, batch, gain_std=0.0, seed=0, model=None):
     import torch
     from swiftkv_prefill_skipping_gb300 import api
@@ -54,8 +71,9 @@ def oracle_prefill(shape, l, g, batch, prompts=None, gain_std=0.0, seed=0, cache
 
 
 def compare_prefill(kv, logits_gpu, batch, idx, caches, logits_ref, num_caches):
-    """Returns (worst KV relative error, worst logit abs error) over the prompts in idx."""
-    worst_kv, worst_lg = 0.0, 0.0
+    """Worst errors over the prompts in idx: (KV relative L2, KV element-wise max|d|/max|ref|,
+    logits max-abs), each cache's K and V tensors compared separately."""
+    worst_kv, worst_el, worst_lg = 0.0, 0.0, 0.0
     lg = logits_gpu.float().cpu().numpy()
     for i, s in enumerate(idx):
         n = int(batch.lens[s])
@@ -63,8 +81,9 @@ def compare_prefill(kv, logits_gpu, batch, idx, caches, logits_ref, num_caches):
             for which, t in (("k", 0), ("v", 1)):
                 got = kv.gather(c, s, n, which).float().cpu().numpy()
                 worst_kv = max(worst_kv, rel_l2(got, caches[i][c][t]))
+                worst_el = max(worst_el, max_rel(got, caches[i][c][t]))
         worst_lg = max(worst_lg, float(np.abs(lg[s] - logits_ref[i]).max()))
-    return worst_kv, worst_lg
+    return worst_kv, worst_el, worst_lg
 
 
 def untouched_rows_are_zero(kv, batch) -> bool:

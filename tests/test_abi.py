@@ -65,3 +65,13 @@ def test_no_cpu_fallback_in_product_path():
         if fn.endswith(".py"):
             src = open(os.path.join(pkg, fn)).read()
             assert "import oracle" not in src and "from oracle" not in src, fn
+
+
+def test_timeout_selftest_argument_checks_without_gpu():
+    """Limits outside [1 us, 100 ms] and a NULL status are refused before anything launches."""
+    lib = B.lib()
+    fake = C.c_void_p(256)   # never dereferenced: the arguments are rejected first
+    for bad in (0, 999, 100_000_001):
+        assert lib.swiftkv_selftest_wait_timeout(fake, None, bad, None) == -1
+    assert lib.swiftkv_selftest_wait_timeout(None, None, 1_000_000, None) == -1
+

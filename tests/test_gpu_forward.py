@@ -201,3 +201,46 @@ def test_gqa8_prefill_decode_and_long_tail():
         _, ref2 = OM.swiftkv_decode_step(cfg, w, caches[s], toks[s], l, g)
         assert float(np.abs(lg2[s] - ref2).max()) <= LOGIT_ABS_TOL, s
     assert m.status() == 0
+
+
+@pytest.mark.parametrize("shape", [SMALL128, MEDIUM])
+def test_rows_impl_chained_and_per_launch_agree(shape):
+    """The last-token tail and decode rows after each attention: one chained cooperative
+    launch per layer (default) and one launch per GEMM / RMSNorm. Both against the oracle
+    (prefill logits and three greedy decode steps), and against each other."""
+    import torch
+    from oracle import model as OM
+    from swiftkv_prefill_skipping_gb300 import api, binding
+    lens = [130, 7, 260]
+    l, g = 2, 1
+    batch = synth.prompt_batch(shape.vocab, len(lens), 0, 0, lens=lens, reserve_tokens=4)
+    w = oracle.synth_weights(shape, gain_std=0.1, cache_layers=True)
+    cfg = oracle.config_of(shape)
+    seq = [batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]] for s in range(len(lens))]
+    caches, refs = OM.swiftkv_prefill(cfg, w, seq, l, g)
+    out = {}
+    for impl in (0, 1):
+        m = api.load_synthetic(shape, l, g, gain_std=0.1)
+        binding.check(binding.lib().swiftkv_set_rows_impl(m.handle, impl))
+        kv = api.KVCache(m, batch.num_pages, batch.block_table)
+        lg = api.prefill(m, torch.as_tensor(batch.tokens, device="cuda"), batch.cu_seqlens, kv).cpu().numpy()
+        steps = [lg]
+        cur, cc, rr = list(lens), list(caches), list(refs)
+        for s in range(len(lens)):
+            assert float(np.abs(lg[s] - refs[s]).max()) <= LOGIT_ABS_TOL, (impl, "prefill", s)
+        for step in range(3):
+            toks = [OM.greedy(r) for r in rr]
+            dl, nxt = api.decode_step(m, torch.tensor(toks, dtype=torch.int32, device="cuda"), cur, kv)
+            dl = dl.cpu().numpy()
+            res = [OM.swiftkv_decode_step(cfg, w, cc[s], toks[s], l, g) for s in range(len(lens))]
+            cc, rr = [r[0] for r in res], [r[1] for r in res]
+            cur = [x + 1 for x in cur]
+            for s in range(len(lens)):
+                assert float(np.abs(dl[s] - rr[s]).max()) <= LOGIT_ABS_TOL, (impl, step, s)
+            steps.append(dl)
+        assert m.status() == 0
+        out[impl] = steps
+        m.free()
+    for a, b in zip(out[0], out[1]):
+        assert float(np.abs(a - b).max()) <= LOGIT_ABS_TOL
+    assert binding.lib().swiftkv_set_rows_impl(None, 0) == -1

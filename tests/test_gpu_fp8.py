@@ -5,16 +5,19 @@ Codes are an integer decision taken in float32 on both sides from the bfloat16 K
 so where the GPU's bf16 row equals the oracle's the codes and scale are identical. Cache 0
 (the first layer: inputs are embedding rows, the same on both sides) isolates the
 quantizer: >= 99 % identical codes, any other code within two e4m3 steps, scales within a
-bf16 ulp of the row's largest value. Deeper caches inherit the ~1e-2 relative K/V
-differences of float32 vs float64 accumulation, and one e4m3 step is 6-12 % of a value, so
-about one code in ten moves by a step there; those are bounded on the dequantized values
-(relative L2 <= 5e-2 per cache). Logits: the usual 5e-2."""
+bf16 ulp of the row's largest value. Deeper caches inherit the K/V differences of float32
+vs float64 accumulation, and one e4m3 step is 6-12 % of a value, so some codes move by a
+step there. The oracle measures that floor itself: the same prompts under the FP8 cache with
+the linear layers accumulated in float32 (the path's declared arithmetic) instead of float64.
+Each cache's dequantized values over the whole batch must satisfy relative L2 <=
+max(1e-2, 1.5 * floor), and the plain 1e-2 wherever the floor is at most half of it.
+Logits: the usual 5e-2."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from gpu_helpers import GQA8, LOGIT_ABS_TOL, SMALL128, SMALL_BIAS
+from gpu_helpers import GQA8, KV_REL_TOL, LOGIT_ABS_TOL, SMALL128, SMALL_BIAS
 from oracle import model as OM
 
 pytestmark = pytest.mark.gpu
@@ -33,24 +36,53 @@ def _setup(shape, l, g, lens, reserve=0, gain_std=0.0, spare_pages=2):
     return m, kv, batch, w, oracle.config_of(shape)
 
 
+def _rel(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def _fp32_floor(fn):
+    """Runs fn under the FP8 cache with float32 accumulation of the linear layers."""
+    with OM.kv_cache_fp8(), OM.accumulate_in(np.float32):
+        return fn()
+
+
 def _check_cache(m, kv, s, n, caches):
-    """GPU codes/scales of sequence s (n rows) against the oracle's fp8 cache values."""
+    """Codes and scales of sequence s (n rows) against the oracle's fp8 cache values: cache 0
+    (identical inputs on both sides) code by code. Returns, per cache and K/V, the GPU's and
+    the oracle's dequantized values for the batch-wide check of _check_batch."""
+    out = {}
     for c in range(m.num_caches):
         for which, t in (("k", 0), ("v", 1)):
             ref_codes, ref_scale = OM.fp8_quantize(caches[c][t])
             got_codes = kv.codes(c, s, n, which).cpu().numpy().astype(np.float64)
             got_scale = kv.scales(c, s, n, which).cpu().numpy()
-            got = got_codes * got_scale[..., None]
-            ref = OM.fp8_dequantize(ref_codes, ref_scale)
-            rel = np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30)
-            assert rel <= 5e-2, (c, which, rel)
+            out[(c, which)] = (got_codes * got_scale[..., None], OM.fp8_dequantize(ref_codes, ref_scale))
             if c == 0:
                 eq = got_codes == ref_codes
                 assert eq.mean() >= 0.99, (which, eq.mean())
                 step = np.exp2(np.floor(np.log2(np.maximum(np.abs(ref_codes), 2.0 ** -6))) - 3)
                 assert np.all(np.abs(got_codes - ref_codes)[~eq] <= 2 * step[~eq] + 1e-12), which
-                amax = np.abs(ref).max(axis=-1)
+                amax = np.abs(out[(c, which)][1]).max(axis=-1)
                 assert np.all(np.abs(got_scale - ref_scale) <= amax / 448.0 * 2.0 ** -7 + 1e-30), which
+    return out
+
+
+def _check_batch(m, kv, lens, caches, caches32):
+    """Every cache and K/V tensor over all of the batch's rows: relative L2 of the dequantized
+    values within the float32-accumulation floor (caches32: the same sequences evaluated by the
+    oracle with float32 accumulation). Taken over the whole batch because one e4m3 code moving
+    one step is several per cent of a value: a one-token sequence's 128 codes would turn a
+    single such move into ~1 % relative L2."""
+    per = [_check_cache(m, kv, s, n, caches[s]) for s, n in enumerate(lens)]
+    for c in range(m.num_caches):
+        for which, t in (("k", 0), ("v", 1)):
+            got = np.concatenate([p[(c, which)][0].ravel() for p in per])
+            ref = np.concatenate([p[(c, which)][1].ravel() for p in per])
+            r32 = np.concatenate([np.asarray(caches32[s][c][t], np.float64).ravel() for s in range(len(lens))])
+            rel, floor = _rel(got, ref), _rel(r32, ref)
+            assert rel <= max(KV_REL_TOL, 1.5 * floor), (c, which, rel, floor)
+            if floor <= 0.5 * KV_REL_TOL:
+                assert rel <= KV_REL_TOL, (c, which, rel, floor)
 
 
 @pytest.mark.parametrize("case", ["tiny_d64", "small_d128", "bias_gqa5", "gqa8"])
@@ -67,9 +99,10 @@ def test_fp8_prefill_codes_scales_and_logits(case):
     seq = [batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]] for s in range(len(lens))]
     with OM.kv_cache_fp8():
         caches, refs = OM.swiftkv_prefill(cfg, w, seq, l, g)
+    caches32, _ = _fp32_floor(lambda: OM.swiftkv_prefill(cfg, w, seq, l, g))
     for s in range(len(lens)):
         assert float(np.abs(lg[s] - refs[s]).max()) <= LOGIT_ABS_TOL, s
-        _check_cache(m, kv, s, lens[s], caches[s])
+    _check_batch(m, kv, lens, caches, caches32)
 
 
 def test_fp8_untouched_rows_stay_zero():
@@ -102,6 +135,7 @@ def test_fp8_decode_steps():
     seq = [batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]] for s in range(3)]
     with OM.kv_cache_fp8():
         caches, refs = OM.swiftkv_prefill(cfg, w, seq, l, g)
+    caches32, _ = _fp32_floor(lambda: OM.swiftkv_prefill(cfg, w, seq, l, g))
     cur = list(lens)
     for step in range(3):
         toks = [OM.greedy(r) for r in refs]
@@ -109,12 +143,13 @@ def test_fp8_decode_steps():
         lg = lg.cpu().numpy()
         with OM.kv_cache_fp8():
             out = [OM.swiftkv_decode_step(cfg, w, caches[s], toks[s], l, g) for s in range(3)]
+        out32 = _fp32_floor(lambda: [OM.swiftkv_decode_step(cfg, w, caches32[s], toks[s], l, g) for s in range(3)])
         caches, refs = [o[0] for o in out], [o[1] for o in out]
+        caches32 = [o[0] for o in out32]
         cur = [x + 1 for x in cur]
         for s in range(3):
             assert float(np.abs(lg[s] - refs[s]).max()) <= LOGIT_ABS_TOL, (step, s)
-    for s in range(3):
-        _check_cache(m, kv, s, cur[s], caches[s])
+    _check_batch(m, kv, cur, caches, caches32)
     assert m.status() == 0
 
 
@@ -131,6 +166,7 @@ def test_fp8_chunked_forward_and_mixed_batch():
             [(0, 100, 230), (2, 40, None)],
             [(0, 230, 300)]]
     ref = [None, None, None]
+    ref32 = [None, None, None]
     nxt = None
     with OM.kv_cache_fp8():
         for call in plan:
@@ -144,12 +180,13 @@ def test_fp8_chunked_forward_and_mixed_batch():
                              kv.view([s for s, _, _ in chunks])).cpu().numpy()
             for i, (s, a, t) in enumerate(chunks):
                 ref[s], lr = OM.swiftkv_forward_one(cfg, w, ref[s], t, l, g)
+                with OM.accumulate_in(np.float32):
+                    ref32[s], _ = OM.swiftkv_forward_one(cfg, w, ref32[s], t, l, g)
                 assert float(np.abs(lg[i] - lr).max()) <= LOGIT_ABS_TOL, (s, a)
                 if s == 2 and nxt is None:
                     nxt = OM.greedy(lr)
     assert m.status() == 0
-    for s, n in ((0, 300), (1, 150), (2, 41)):
-        _check_cache(m, kv, s, n, ref[s])
+    _check_batch(m, kv, [300, 150, 41], ref, ref32)
 
 
 def test_fp8_cache_is_half_the_bytes():

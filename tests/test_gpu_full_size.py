@@ -3,21 +3,25 @@
 For each workload the GPU prefills the whole packed batch. Checked:
   - bookkeeping over the whole batch, bit-exact: every (cache, page, row) that belongs
     to a prompt token was written, nothing else was;
-  - the shortest prompt of the batch through the oracle: all its caches and its
+  - the shortest and the longest prompt of the batch through the oracle: all their caches
+    (relative L2 and element-wise max |d| / max |ref|, K and V separately) and their
     last-token logits;
-  - the same prompt prefilled alone gives bit-identical caches and logits (packing
+  - the shortest prompt prefilled alone gives bit-identical caches and logits (packing
     independence, a property that holds at any size).
 
-Tolerance at full depth. Rounding to bfloat16 at every linear-layer input amplifies any
-difference between two evaluations: a perturbation far below one bf16 ulp flips a few
-roundings, the flips perturb the next GEMM by ~sqrt(perturbation * ulp), and within a
-layer or two two correct evaluations differ at the bf16 floor; each further layer adds
-to it. The oracle measures this floor itself: the same prompt evaluated at the GPU path's
-declared precision (linear layers accumulated in float32, softmax weights rounded to fp16
-before they meet V) instead of float64. At 16+ random-init layers that floor already
-exceeds 1e-2 (KV, relative L2) and 5e-2 (logits, max-abs), so here each cache must satisfy
-err <= max(1e-2, 1.5 * floor) and the logits err <= max(5e-2, 1.5 * floor). The stated tolerances apply unchanged at the shallow
-shapes of test_gpu_parity.py. Llama-3.1-70B (141 GB of weights) runs with SWIFTKV_TEST_70B=1.
+Tolerance at full depth. The path's declared arithmetic is bfloat16 operands with float32
+accumulation. Rounding to bfloat16 at every linear-layer input amplifies any difference
+between two evaluations: a perturbation far below one bf16 ulp flips a few roundings, the
+flips perturb the next GEMM by ~sqrt(perturbation * ulp), and within a layer or two two
+correct evaluations differ at the bf16 floor; each further layer adds to it. The oracle
+measures this floor itself: the same prompt evaluated with the linear layers accumulated in
+float32 (nothing else changed) instead of float64. At 16+ random-init layers that floor
+already exceeds 1e-2 (KV) and 5e-2 (logits), so the stated limits cannot bind the deep
+caches of any float32-accumulating implementation. Each cache and the logits must satisfy
+err <= max(limit, 1.5 * floor), and wherever the floor is at most half the limit (the first
+layers) the plain limit applies (limits: 1e-2 for the KV, relative L2 and element-wise
+max |d| / max |ref|; 5e-2 max-abs for the logits). The stated tolerances apply unchanged at the shallow shapes
+of test_gpu_parity.py. Llama-3.1-70B (141 GB of weights) runs with SWIFTKV_TEST_70B=1.
 """
 import os
 
@@ -26,7 +30,7 @@ import pytest
 
 import oracle
 import synth
-from gpu_helpers import KV_REL_TOL, LOGIT_ABS_TOL, compare_prefill, rel_l2, untouched_rows_are_zero
+from gpu_helpers import KV_MAXREL_TOL, KV_REL_TOL, LOGIT_ABS_TOL, max_rel, rel_l2, untouched_rows_are_zero
 
 pytestmark = pytest.mark.gpu
 
@@ -59,26 +63,15 @@ def _run_workload(name, decode_steps=0):
     assert m.status() == 0
     assert untouched_rows_are_zero(kv, batch)
 
+    cfg = oracle.config_of(w.shape)
+    wts = _oracle_weights(w.shape)
+    lg_all = logits.float().cpu().numpy()
+    checked = {s: _check_prompt(name, w, cfg, wts, m, kv, batch, lg_all, s)
+               for s in sorted({int(np.argmin(batch.lens)), int(np.argmax(batch.lens))})}
+
     s = int(np.argmin(batch.lens))
     n = int(batch.lens[s])
     toks = batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]]
-    cfg = oracle.config_of(w.shape)
-    wts = _oracle_weights(w.shape)
-    caches, ref = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
-    with OM.accumulate_in(np.float32, OM.fp16):
-        caches32, ref32 = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
-    lg = logits[s].float().cpu().numpy()
-    lg_err, lg_floor = float(np.abs(lg - ref).max()), float(np.abs(ref32 - ref).max())
-    report = {"logits": (lg_err, lg_floor)}
-    for c in range(m.num_caches):
-        for which, t in (("k", 0), ("v", 1)):
-            got = kv.gather(c, s, n, which).float().cpu().numpy()
-            err, floor = rel_l2(got, caches[c][t]), rel_l2(caches32[c][t], caches[c][t])
-            report[f"{which}{c}"] = (err, floor)
-            assert err <= max(KV_REL_TOL, 1.5 * floor), (name, which, c, err, floor)
-    assert lg_err <= max(LOGIT_ABS_TOL, 1.5 * lg_floor), (name, lg_err, lg_floor)
-    print(name, {k: (round(a, 5), round(b, 5)) for k, (a, b) in report.items()})
-
     alone = synth.Batch(lens=np.array([n], np.int32), cu_seqlens=np.array([0, n], np.int32), tokens=toks,
                         block_table=batch.block_table[s:s + 1], num_pages=batch.num_pages)
     kv1 = api.KVCache(m, batch.num_pages, alone.block_table)
@@ -90,11 +83,11 @@ def _run_workload(name, decode_steps=0):
         assert torch.equal(kv1.gather(c, 0, n, "v"), kv.gather(c, s, n, "v"))
 
     # decode from the SwiftKV cache: feed the oracle's greedy tokens to both sides
-    cache, lg_ref, cache32 = caches, ref, caches32
+    cache, cache32, lg_ref = checked[s]
     for step in range(decode_steps):
         nxt = OM.greedy(lg_ref)
         cache, lg_ref = OM.swiftkv_decode_step(cfg, wts, cache, nxt, w.l, w.g)
-        with OM.accumulate_in(np.float32, OM.fp16):
+        with OM.accumulate_in(np.float32):
             cache32, lg32 = OM.swiftkv_decode_step(cfg, wts, cache32, nxt, w.l, w.g)
         toks_b = torch.zeros(len(batch.lens), dtype=torch.int32, device="cuda")
         toks_b[s] = nxt
@@ -102,13 +95,47 @@ def _run_workload(name, decode_steps=0):
         lg_b, _ = api.decode_step(m, toks_b, lens_b, kv)
         torch.cuda.synchronize()
         err, floor = float(np.abs(lg_b[s].cpu().numpy() - lg_ref).max()), float(np.abs(lg32 - lg_ref).max())
-        assert err <= max(LOGIT_ABS_TOL, 1.5 * floor), (name, step, err, floor)
+        _bound(err, floor, LOGIT_ABS_TOL, (name, "decode logits", step))
         for c in range(m.num_caches):
-            e = rel_l2(kv.gather(c, s, n + step + 1).float().cpu().numpy(), cache[c][0])
-            f = rel_l2(cache32[c][0], cache[c][0])
-            assert e <= max(KV_REL_TOL, 1.5 * f), (name, step, c, e, f)
+            for which, t in (("k", 0), ("v", 1)):
+                got = kv.gather(c, s, n + step + 1, which).float().cpu().numpy()
+                _bound(rel_l2(got, cache[c][t]), rel_l2(cache32[c][t], cache[c][t]), KV_REL_TOL,
+                       (name, "decode", step, which, c))
     assert m.status() == 0
     m.free()
+
+
+def _bound(err, floor, limit, what):
+    """err <= max(limit, 1.5 * floor); the plain limit wherever the floor leaves it room."""
+    assert err <= max(limit, 1.5 * floor), (what, err, floor)
+    if floor <= 0.5 * limit:
+        assert err <= limit, (what, err, floor)
+
+
+def _check_prompt(name, w, cfg, wts, m, kv, batch, lg_all, s):
+    """Prompt s of the batch: every cache (K and V; relative L2 and element-wise) and its
+    last-token logits against the oracle, bounded by the float32-accumulation floor."""
+    from oracle import model as OM
+    n = int(batch.lens[s])
+    toks = batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]]
+    caches, ref = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
+    with OM.accumulate_in(np.float32):
+        caches32, ref32 = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
+    lg_err, lg_floor = float(np.abs(lg_all[s] - ref).max()), float(np.abs(ref32 - ref).max())
+    _bound(lg_err, lg_floor, LOGIT_ABS_TOL, (name, n, "logits"))
+    worst = {"l2": (0.0, 0.0, None), "max": (0.0, 0.0, None)}
+    for c in range(m.num_caches):
+        for which, t in (("k", 0), ("v", 1)):
+            got = kv.gather(c, s, n, which).float().cpu().numpy()
+            for kind, f, lim in (("l2", rel_l2, KV_REL_TOL), ("max", max_rel, KV_MAXREL_TOL)):
+                err, floor = f(got, caches[c][t]), f(caches32[c][t], caches[c][t])
+                _bound(err, floor, lim, (name, n, kind, which, c))
+                if err > worst[kind][0]:
+                    worst[kind] = (err, floor, f"{which}{c}")
+    print(f"{name} n={n}: logits {lg_err:.4f} (floor {lg_floor:.4f}); worst KV rel-L2 "
+          f"{worst['l2'][0]:.4f} (floor {worst['l2'][1]:.4f}, {worst['l2'][2]}); worst KV max-rel "
+          f"{worst['max'][0]:.4f} (floor {worst['max'][1]:.4f}, {worst['max'][2]})")
+    return caches, caches32, ref
 
 
 def test_llama8b_l16_full_workload():

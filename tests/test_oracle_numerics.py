@@ -137,26 +137,49 @@ def test_accumulate_in_float32_switch():
     assert np.array_equal(M.linear(x, w), exact)      # switch restored
 
 
-def test_precision_mode_rounds_softmax_weights_before_v():
-    """Inside accumulate_in(float32, fp16) attention uses fp16-rounded unnormalised weights
-    against V and the exact sum as denominator; brute force on a tiny case."""
+def test_accumulate_in_float32_covers_attention_and_rmsnorm():
+    """Inside the switch the attention's scores, softmax sum and weighted sum of V and the
+    RMSNorm mean of squares are float32 accumulations: against brute-force float32 loops on
+    a tiny case; outside it the float64 definition is untouched."""
     n_q, d_h = 2, 4
-    q = rng.standard_normal((3, n_q, d_h))
-    k = rng.standard_normal((3, 1, d_h))
-    v = rng.standard_normal((3, 1, d_h))
+    q = M.bf16(rng.standard_normal((3, n_q, d_h)))
+    k = M.bf16(rng.standard_normal((3, 1, d_h)))
+    v = M.bf16(rng.standard_normal((3, 1, d_h)))
     pos = np.arange(3)
-    with M.accumulate_in(np.float32, M.fp16):
+    exact = M.causal_gqa_attention(q, k, v, pos, pos)
+    with M.accumulate_in(np.float32):
         got = M.causal_gqa_attention(q, k, v, pos, pos)
+    f32 = np.float32
     for h in range(n_q):
         for i in range(3):
-            s = [float(q[i, h] @ k[t, 0]) / math.sqrt(d_h) for t in range(i + 1)]
-            e = [math.exp(a - max(s)) for a in s]
-            num = sum(float(np.float16(e[t])) * v[t, 0] for t in range(i + 1))
-            np.testing.assert_allclose(got[i, h], num / sum(e), rtol=1e-12)
-    exact = M.causal_gqa_attention(q, k, v, pos, pos)
+            s = []
+            for t in range(i + 1):
+                acc = f32(0)
+                for e in range(d_h):
+                    acc = f32(acc + f32(q[i, h, e]) * f32(k[t, 0, e]))
+                s.append(float(acc) / math.sqrt(d_h))
+            w = [math.exp(a - max(s)) for a in s]
+            den = f32(0)
+            for t in range(i + 1):
+                den = f32(den + f32(w[t]))
+            for e in range(d_h):
+                num = f32(0)
+                for t in range(i + 1):
+                    num = f32(num + f32(w[t]) * f32(v[t, 0, e]))
+                np.testing.assert_allclose(got[i, h, e], float(num) / float(den), rtol=2e-6, atol=1e-7)
     assert not np.array_equal(got, exact)
-    np.testing.assert_allclose(got, exact, rtol=2e-3, atol=2e-3)
-    assert M.fp16(1 + 2 ** -11) == 1.0 and M.fp16(1 + 3 * 2 ** -11) == 1 + 2 ** -9   # ties to even
+    np.testing.assert_allclose(got, exact, rtol=1e-5, atol=1e-6)
+    assert np.array_equal(M.causal_gqa_attention(q, k, v, pos, pos), exact)   # switch restored
+
+    x = rng.standard_normal((4, 64)) * 0.3
+    g = 1.0 + 0.1 * rng.standard_normal(64)
+    ref = M.rms_norm(x, g, 1e-5)
+    with M.accumulate_in(np.float32):
+        r32 = M.rms_norm(x, g, 1e-5)
+    ms32 = np.array([float(np.mean((row * row).astype(np.float32), dtype=np.float32)) for row in x])
+    np.testing.assert_allclose(r32, x / np.sqrt(ms32[:, None] + 1e-5) * g, rtol=1e-12)
+    np.testing.assert_allclose(r32, ref, rtol=1e-6)
+    assert np.array_equal(M.rms_norm(x, g, 1e-5), ref)
 
 
 def test_e4m3_matches_torch_float8_cast():
