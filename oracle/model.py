@@ -43,30 +43,37 @@ def bf16(x) -> np.ndarray:
 
 
 # Precision mode. float64 everywhere is the definition. Tests evaluate the same model with
-# every accumulation in float32 - the linear layers' dot products, the attention scores, the
-# softmax normaliser and the weighted sum of V, the RMSNorm mean of squares - the GPU path's
-# declared arithmetic (bfloat16 operands, float32 accumulation), to measure the rounding floor
-# any implementation with that precision faces against the definition. Pointwise functions
-# (exp, silu, RoPE angles) and the residual stream stay float64; nothing is rounded to a
-# format narrower than float32 beyond the model's own bfloat16 points.
+# everything except the model's own bfloat16 rounding points in float32 - accumulations (the
+# linear layers' dot products, the attention scores, the softmax normaliser and weighted sum
+# of V, the RMSNorm mean of squares) and every other operation (norm scaling, RoPE, SiLU and
+# the SwiGLU product, softmax exponentials, bias and residual adds) - the GPU path's declared
+# arithmetic (bfloat16 operands, float32 compute and accumulation), to measure the rounding
+# floor any implementation of that precision faces against the definition. Nothing is rounded
+# to a format narrower than float32 beyond the bfloat16 points the model itself has.
 _LINEAR_ACC = [F64]
+
+
+def _mode():
+    """The precision mode's type (float64: the definition)."""
+    return _LINEAR_ACC[-1]
 
 
 def rms_norm(x: np.ndarray, gamma: np.ndarray, eps: float) -> np.ndarray:
     """RMSNorm over the last axis: x / sqrt(mean(x^2) + eps) * gamma."""
     x = np.asarray(x, dtype=F64)
-    acc = _LINEAR_ACC[-1]
-    if acc is F64:
-        ms = np.mean(x * x, axis=-1, keepdims=True)
-    else:  # squares and their sum accumulated in the precision mode's type
-        ms = np.mean((x * x).astype(acc), axis=-1, keepdims=True, dtype=acc).astype(F64)
-    return x / np.sqrt(ms + eps) * np.asarray(gamma, F64)
+    t = _mode()
+    if t is F64:
+        return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * np.asarray(gamma, F64)
+    xt = x.astype(t)
+    ms = np.mean(xt * xt, axis=-1, keepdims=True, dtype=t)
+    r = (t(1) / np.sqrt(ms + t(eps))).astype(t)
+    return (xt * r * np.asarray(gamma).astype(t)).astype(F64)
 
 
-class accumulate_in:
-    """Context manager: run every accumulation (linear layers, attention scores, softmax sum
-    and weighted sum of V, RMSNorm mean of squares) in `dtype`; inputs that are bfloat16
-    values stay exact; everything else unchanged."""
+class compute_in:
+    """Context manager: evaluate every quantity that the model does not round to bfloat16
+    itself (accumulations, norm scaling, RoPE, SiLU, softmax, bias and residual adds) in
+    `dtype`; values that are bfloat16 stay exact."""
 
     def __init__(self, dtype):
         self.dtype = dtype
@@ -84,7 +91,7 @@ def linear(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None,
            block: int = 8192) -> np.ndarray:
     """x @ w.T (+ b), w in nn.Linear layout [out][in]; w may be stored as float32
     (bfloat16 values) and is widened to float64 one block of output rows at a time."""
-    acc = _LINEAR_ACC[-1]
+    acc = _mode()
     x = np.asarray(x, dtype=F64)
     xa = x.astype(acc)
     n_out = w.shape[0]
@@ -92,8 +99,19 @@ def linear(x: np.ndarray, w: np.ndarray, b: Optional[np.ndarray] = None,
     for i in range(0, n_out, block):
         out[..., i:i + block] = xa @ np.asarray(w[i:i + block], dtype=acc).T
     if b is not None:
-        out += np.asarray(b, F64)
+        if acc is F64:
+            out += np.asarray(b, F64)
+        else:
+            out = (out.astype(acc) + np.asarray(b).astype(acc)).astype(F64)
     return out
+
+
+def residual_add(x: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """The residual stream's update x + y (in the precision mode's type)."""
+    t = _mode()
+    if t is F64:
+        return np.asarray(x, F64) + np.asarray(y, F64)
+    return (np.asarray(x).astype(t) + np.asarray(y).astype(t)).astype(F64)
 
 
 def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
@@ -108,12 +126,27 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     ang = np.asarray(pos, dtype=F64)[:, None] * inv_freq[None, :]
     c = np.cos(ang)[:, None, :]
     s = np.sin(ang)[:, None, :]
+    t = _mode()
+    if t is not F64:  # the rotation in the precision mode's type (angles in float64)
+        c, s, x = c.astype(t), s.astype(t), x.astype(t)
     x1, x2 = x[..., :half], x[..., half:]
-    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1)
+    return np.concatenate([x1 * c - x2 * s, x2 * c + x1 * s], axis=-1).astype(F64)
 
 
 def silu(x: np.ndarray) -> np.ndarray:
+    t = _mode()
+    if t is not F64:
+        xt = np.asarray(x).astype(t)
+        return (xt / (t(1) + np.exp(-xt))).astype(F64)
     return x / (1.0 + np.exp(-x))
+
+
+def swiglu(g: np.ndarray, u: np.ndarray) -> np.ndarray:
+    """silu(g) * u (the product in the precision mode's type)."""
+    t = _mode()
+    if t is F64:
+        return silu(g) * u
+    return (silu(g).astype(t) * np.asarray(u).astype(t)).astype(F64)
 
 
 def causal_gqa_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.ndarray,
@@ -126,23 +159,22 @@ def causal_gqa_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, q_pos: np.
     allowed = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]
     out = np.empty(q.shape, dtype=F64)
     scale = 1.0 / np.sqrt(F64(d_h))
-    acc = _LINEAR_ACC[-1]
+    t = _mode()
     for h in range(n_q):
         kv = h // grp
-        if acc is F64:
+        if t is F64:
             s = (q[:, h, :] @ k[:, kv, :].T) * scale
-        else:
-            s = (q[:, h, :].astype(acc) @ k[:, kv, :].T.astype(acc)).astype(F64) * scale
-        s = np.where(allowed, s, -np.inf)
-        s = s - s.max(axis=1, keepdims=True)
-        p = np.exp(s)
-        if acc is F64:
+            s = np.where(allowed, s, -np.inf)
+            s = s - s.max(axis=1, keepdims=True)
+            p = np.exp(s)
             p = p / p.sum(axis=1, keepdims=True)
             out[:, h, :] = p @ v[:, kv, :]
-        else:  # unnormalised weights summed and applied to V in the mode's type, then divided
-            pa = p.astype(acc)
-            denom = pa.sum(axis=1, keepdims=True, dtype=acc).astype(F64)
-            out[:, h, :] = (pa @ v[:, kv, :].astype(acc)).astype(F64) / denom
+        else:  # everything in the mode's type; unnormalised weights applied to V, then divided
+            s = (q[:, h, :].astype(t) @ k[:, kv, :].T.astype(t)) * t(scale)
+            s = np.where(allowed, s, t(-np.inf))
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            denom = p.sum(axis=1, keepdims=True, dtype=t)
+            out[:, h, :] = ((p @ v[:, kv, :].astype(t)) / denom).astype(F64)
     return out
 
 
@@ -295,14 +327,14 @@ def attn_out(cfg: Config, lw: Layer, x: np.ndarray, q: np.ndarray, kv: KV, q_pos
     """Residual update of the attention block: x + W_O attention(q, K, V)."""
     a = causal_gqa_attention(q, kv[0], kv[1], q_pos, k_pos)
     a = bf16(a.reshape(a.shape[0], cfg.n_q * cfg.d_h))
-    return x + linear(a, lw.wo)
+    return residual_add(x, linear(a, lw.wo))
 
 
 def mlp(cfg: Config, lw: Layer, x: np.ndarray) -> np.ndarray:
     """Residual update of the SwiGLU MLP: x + W_down (silu(W_gate u) * (W_up u))."""
     u = bf16(rms_norm(x, lw.gamma_mlp, cfg.rms_eps))
-    h = bf16(silu(linear(u, lw.wg)) * linear(u, lw.wu))
-    return x + linear(h, lw.wd)
+    h = bf16(swiglu(linear(u, lw.wg), linear(u, lw.wu)))
+    return residual_add(x, linear(h, lw.wd))
 
 
 def lm_head(cfg: Config, w: Weights, x: np.ndarray) -> np.ndarray:

@@ -5,7 +5,7 @@
 //   memory with cp.async; each (page, head) block of 16 keys is 16*d_head*2
 //   contiguous bytes. S = Q K^T and O += P V run on mma.sync bf16 tensor cores with fp32
 //   accumulation; P V takes V in bf16 as cached and P as bf16 high + low parts (two MMAs,
-//   about 15 significant bits of P); softmax is online (running max / sum in the log2
+//   about 17 significant bits of P); softmax is online (running max / sum in the log2
 //   domain). FP8 cache: the pools hold the e4m3 codes as (exact) bf16 values, and each score
 //   is multiplied by its key's scale and each P by its value's scale (float32).
 //   Query tiles arrive longest-first (heaviest causal tiles scheduled first).

@@ -18,7 +18,7 @@
 //              blocks that cross the diagonal or the prompt end), online softmax in the log2
 //              domain with a running max allowed to lag by up to 2^8 (O, accumulated across
 //              blocks in TMEM by the MMA, is rescaled in place only when it moves further),
-//              P as bf16 high + low parts (about 15 significant bits) by tcgen05.st over
+//              P as bf16 high + low parts (about 17 significant bits) by tcgen05.st over
 //              the S columns it came from; finally O / l from TMEM to global memory
 // FP8 cache: the pools hold the e4m3 codes as (exact) bf16 values; the block's key and value
 // scales come with its K/V, each score is multiplied by its key's scale and each P by its

@@ -20,7 +20,7 @@
 //               (tcgen05.ld of its S row, causal/length mask only on blocks that cross the
 //               diagonal or the chunk end, online softmax in the log2 domain with a running
 //               max allowed to lag by up to 2^8 -- O is rescaled in TMEM only past that --, P
-//               split into bf16 high + low parts (about 15 significant bits) and stored by
+//               split into bf16 high + low parts (about 17 significant bits) and stored by
 //               tcgen05.st over the S columns it came from), then O / l from TMEM to global
 //               memory.
 // While one tile's softmax warps work, the tensor core runs the other tile's MMAs, and each

@@ -22,7 +22,7 @@ __device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
 }
 
 // Softmax weights of one 64-key block as bfloat16 high and low parts (split_pair_bf16), for a
-// P V product on bf16 tensor cores that keeps P to about 15 significant bits: w[c] packs the
+// P V product on bf16 tensor cores that keeps P to about 17 significant bits: w[c] packs the
 // high parts of p[2c] (low half) and p[2c + 1], w[32 + c] their low parts.
 __device__ __forceinline__ void split_p_bf16(const float* p, uint32_t* w) {
 #pragma unroll

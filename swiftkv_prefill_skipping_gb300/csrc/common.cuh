@@ -395,11 +395,13 @@ __device__ __forceinline__ void kv_chunk_prep(const EpiParams& p, int m, int n_l
 }
 
 // Codes, scale and expansion of the head whose pair block starts at column n0 for row m; pk
-// holds its 2 * half values as bf16 pairs in dimension order, amax their largest magnitude.
+// holds its DH values as bf16 pairs in dimension order, amax their largest magnitude.
+template <int DH>
 __device__ __forceinline__ void store_head_fp8(const EpiParams& p, int m, int n0, const uint32_t* pk, float amax) {
   const int slot = p.slots[m];
   if (slot < 0) return;
-  const int dh = p.d_head, kvc = p.n_kv * dh;
+  constexpr int dh = DH;
+  const int kvc = p.n_kv * dh;
   int c, cache;
   if (p.kind == EPI_QKV) {
     c = n0 - p.q_cols;
@@ -415,6 +417,7 @@ __device__ __forceinline__ void store_head_fp8(const EpiParams& p, int m, int n0
   const float scale = amax / 448.f;
   uint8_t* dst = reinterpret_cast<uint8_t* const*>(is_k ? p.k_pools : p.v_pools)[cache] + rowoff * dh;
   bf16* ex = is_k ? p.exp_k : p.exp_v;
+#pragma unroll
   for (int q = 0; q < dh / 16; ++q) {  // 16 dimensions per 16-byte store
     uint32_t w[4], e[8];
 #pragma unroll
@@ -513,13 +516,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // Two softmax weights p0, p1 (>= 0, finite) as bfloat16 high and low parts, packed bf16x2
-// with p0's part in the low half: the high part is the float32 encoding with its low 16 bits
-// cleared, the low part the remainder (exact in float32) rounded to the nearest bf16, so
-// hi + lo equals p to within 2^-15 |p|.
+// with p0's part in the low half: the high part is p rounded to the nearest bf16, the low part
+// the remainder (exact in float32, at most half a bf16 ulp of p) rounded to the nearest bf16,
+// so hi + lo equals p to within 2^-18 |p|.
 __device__ __forceinline__ void split_pair_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
-  const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-  hi = __byte_perm(b0, b1, 0x7632);
-  lo = pack_bf16(p0 - __uint_as_float(b0 & 0xffff0000u), p1 - __uint_as_float(b1 & 0xffff0000u));
+  hi = pack_bf16(p0, p1);
+  lo = pack_bf16(p0 - __uint_as_float(hi << 16), p1 - __uint_as_float(hi & 0xffff0000u));
 }
 
 }  // namespace skv

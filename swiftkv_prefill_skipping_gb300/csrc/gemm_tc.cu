@@ -53,6 +53,31 @@ constexpr uint32_t IDESC = tc::make_idesc(BM, BN, false, false);
 // 16 MB at K = 4096) that stays resident in L2 while the group sweeps every weight tile.
 constexpr int GROUP_M = 16;
 
+// FP8 cache, one K or V head (2 * H columns from TMEM column tcol) of row `row`: bias and RoPE,
+// the bf16 values the cache would hold, their max, then codes, scale and expansion. The TMEM
+// loads are warp-collective, so every lane runs them whether or not its row exists.
+template <int H>
+__device__ __forceinline__ void fp8_head_epilogue(const EpiParams& ep, int row, int M, int ncol, uint32_t tcol) {
+  uint32_t pk[H];
+  float amax = 0.f;
+#pragma unroll
+  for (int c = 0; c < H; c += 32) {
+    float lo[32], hi[32];
+    tmem_ld32(tcol + c, lo);
+    tmem_ld32(tcol + H + c, hi);
+    if (row < M) kv_chunk_prep(ep, row, ncol + c, ncol + H + c, lo, hi);
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const uint32_t pl = pack_bf16_(lo[i], lo[i + 1]), ph = pack_bf16_(hi[i], hi[i + 1]);
+      pk[(c + i) >> 1] = pl;
+      pk[(H + c + i) >> 1] = ph;
+      amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(pl << 16))), fabsf(__uint_as_float(pl & 0xffff0000u)));
+      amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(ph << 16))), fabsf(__uint_as_float(ph & 0xffff0000u)));
+    }
+  }
+  if (row < M) store_head_fp8<2 * H>(ep, row, ncol, pk, amax);
+}
+
 __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int& mt, int& nt) {
   const int per_group = GROUP_M * n_tiles;
   const int g = t / per_group;
@@ -183,25 +208,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_kernel(const __grid_consta
       for (int b0 = 0; b0 < BN; b0 += 2 * half) {
         const int ncol = nt * BN + b0;
         if (ncol >= N) break;
-        if (fp8_head_block(ep, ncol)) {
-          // one K or V head of an FP8 cache: bf16 values, their max, codes and scale
-          uint32_t pk[64];
-          float amax = 0.f;
-          for (int c = 0; c < half; c += 32) {
-            float lo[32], hi[32];
-            tmem_ld32(tb + b0 + c, lo);
-            tmem_ld32(tb + b0 + half + c, hi);
-            if (row < M) kv_chunk_prep(ep, row, ncol + c, ncol + half + c, lo, hi);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const uint32_t pl = pack_bf16_(lo[i], lo[i + 1]), ph = pack_bf16_(hi[i], hi[i + 1]);
-              pk[(c + i) >> 1] = pl;
-              pk[(half + c + i) >> 1] = ph;
-              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(pl << 16))), fabsf(__uint_as_float(pl & 0xffff0000u)));
-              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(ph << 16))), fabsf(__uint_as_float(ph & 0xffff0000u)));
-            }
-          }
-          if (row < M) store_head_fp8(ep, row, ncol, pk, amax);
+        if (fp8_head_block(ep, ncol)) {  // one K or V head of an FP8 cache
+          if (half == 64) fp8_head_epilogue<64>(ep, row, M, ncol, tb + b0);
+          else fp8_head_epilogue<32>(ep, row, M, ncol, tb + b0);
           continue;
         }
         for (int c = 0; c < half; c += 32) {
@@ -399,25 +408,9 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_pair_kernel(const __grid_c
       for (int b0 = 0; b0 < BN; b0 += 2 * half) {
         const int ncol = nt * BN + b0;
         if (ncol >= N) break;
-        if (fp8_head_block(ep, ncol)) {
-          // one K or V head of an FP8 cache: bf16 values, their max, codes and scale
-          uint32_t pk[64];
-          float amax = 0.f;
-          for (int c = 0; c < half; c += 32) {
-            float lo[32], hi[32];
-            tmem_ld32(tb + b0 + c, lo);
-            tmem_ld32(tb + b0 + half + c, hi);
-            if (row < M) kv_chunk_prep(ep, row, ncol + c, ncol + half + c, lo, hi);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const uint32_t pl = pack_bf16_(lo[i], lo[i + 1]), ph = pack_bf16_(hi[i], hi[i + 1]);
-              pk[(c + i) >> 1] = pl;
-              pk[(half + c + i) >> 1] = ph;
-              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(pl << 16))), fabsf(__uint_as_float(pl & 0xffff0000u)));
-              amax = fmaxf(fmaxf(amax, fabsf(__uint_as_float(ph << 16))), fabsf(__uint_as_float(ph & 0xffff0000u)));
-            }
-          }
-          if (row < M) store_head_fp8(ep, row, ncol, pk, amax);
+        if (fp8_head_block(ep, ncol)) {  // one K or V head of an FP8 cache
+          if (half == 64) fp8_head_epilogue<64>(ep, row, M, ncol, tb + b0);
+          else fp8_head_epilogue<32>(ep, row, M, ncol, tb + b0);
           continue;
         }
         for (int c = 0; c < half; c += 32) {

@@ -42,7 +42,7 @@ def _rel(a, b):
 
 def _fp32_floor(fn):
     """Runs fn under the FP8 cache with float32 accumulation of the linear layers."""
-    with OM.kv_cache_fp8(), OM.accumulate_in(np.float32):
+    with OM.kv_cache_fp8(), OM.compute_in(np.float32):
         return fn()
 
 
@@ -180,7 +180,7 @@ def test_fp8_chunked_forward_and_mixed_batch():
                              kv.view([s for s, _, _ in chunks])).cpu().numpy()
             for i, (s, a, t) in enumerate(chunks):
                 ref[s], lr = OM.swiftkv_forward_one(cfg, w, ref[s], t, l, g)
-                with OM.accumulate_in(np.float32):
+                with OM.compute_in(np.float32):
                     ref32[s], _ = OM.swiftkv_forward_one(cfg, w, ref32[s], t, l, g)
                 assert float(np.abs(lg[i] - lr).max()) <= LOGIT_ABS_TOL, (s, a)
                 if s == 2 and nxt is None:

@@ -87,7 +87,7 @@ def _run_workload(name, decode_steps=0):
     for step in range(decode_steps):
         nxt = OM.greedy(lg_ref)
         cache, lg_ref = OM.swiftkv_decode_step(cfg, wts, cache, nxt, w.l, w.g)
-        with OM.accumulate_in(np.float32):
+        with OM.compute_in(np.float32):
             cache32, lg32 = OM.swiftkv_decode_step(cfg, wts, cache32, nxt, w.l, w.g)
         toks_b = torch.zeros(len(batch.lens), dtype=torch.int32, device="cuda")
         toks_b[s] = nxt
@@ -119,7 +119,7 @@ def _check_prompt(name, w, cfg, wts, m, kv, batch, lg_all, s):
     n = int(batch.lens[s])
     toks = batch.tokens[batch.cu_seqlens[s]:batch.cu_seqlens[s + 1]]
     caches, ref = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
-    with OM.accumulate_in(np.float32):
+    with OM.compute_in(np.float32):
         caches32, ref32 = OM.swiftkv_prefill_one(cfg, wts, toks, w.l, w.g)
     lg_err, lg_floor = float(np.abs(lg_all[s] - ref).max()), float(np.abs(ref32 - ref).max())
     _bound(lg_err, lg_floor, LOGIT_ABS_TOL, (name, n, "logits"))

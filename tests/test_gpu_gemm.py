@@ -109,3 +109,20 @@ def test_tma_gemv_rows_do_not_depend_on_batch_size(N, K):
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert all(torch.equal(outs[0], o) for o in outs[1:])
+
+
+def test_skinny_kernels_on_each_visible_device():
+    """Kernels that raise their shared-memory limit do it once per device: the split-K
+    skinny GEMM with more than 16 rows (55-74 KB of shared memory) and the persistent tcgen05
+    GEMM run on every visible GPU in turn, twice each, in one process."""
+    import torch
+    n = torch.cuda.device_count()
+    if n < 2:
+        pytest.skip("one GPU visible")
+    for rnd in range(2):
+        for dev in range(n):
+            with torch.cuda.device(dev):
+                for impl, (M, N, K) in ((2, (40, 1024, 512)), (0, (300, 512, 256))):
+                    Cm, ref = _run(impl, M, N, K, seed=rnd)
+                    err = (Cm - ref).abs().max().item() / ref.abs().max().item()
+                    assert err < 2e-5, (dev, impl, err)

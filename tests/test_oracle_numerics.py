@@ -123,33 +123,36 @@ def test_silu_special_values():
     np.testing.assert_allclose(M.silu(x.numpy()), torch.nn.functional.silu(x).numpy(), rtol=1e-14)
 
 
-def test_accumulate_in_float32_switch():
-    """The precision switch used to measure the float32-accumulation floor: inside it the
-    linear layer equals a float32 matmul of the same (bfloat16-valued) operands."""
+def test_compute_in_float32_linear():
+    """The precision switch used to measure the float32 floor: inside it the linear layer is a
+    float32 matmul of the same (bfloat16-valued) operands, its bias added in float32."""
     x = M.bf16(rng.standard_normal((5, 64)))
     w = M.bf16(rng.standard_normal((7, 64))).astype(np.float32)
-    exact = M.linear(x, w)
-    with M.accumulate_in(np.float32):
-        f32 = M.linear(x, w)
-    assert np.array_equal(f32, (x.astype(np.float32) @ w.T).astype(np.float64))
+    b = rng.standard_normal(7) * 0.1
+    exact = M.linear(x, w, b)
+    with M.compute_in(np.float32):
+        f32 = M.linear(x, w, b)
+    want = ((x.astype(np.float32) @ w.T) + b.astype(np.float32)).astype(np.float64)
+    assert np.array_equal(f32, want)
     assert not np.array_equal(f32, exact)
     np.testing.assert_allclose(f32, exact, rtol=1e-5, atol=1e-5)
-    assert np.array_equal(M.linear(x, w), exact)      # switch restored
+    assert np.array_equal(M.linear(x, w, b), exact)      # switch restored
 
 
-def test_accumulate_in_float32_covers_attention_and_rmsnorm():
-    """Inside the switch the attention's scores, softmax sum and weighted sum of V and the
-    RMSNorm mean of squares are float32 accumulations: against brute-force float32 loops on
-    a tiny case; outside it the float64 definition is untouched."""
+def test_compute_in_float32_attention():
+    """Inside the switch the attention is a float32 evaluation: scores, scaling, max, exp,
+    normaliser and weighted sum of V, each in float32 (brute-force loops on a tiny case);
+    outside it the float64 definition is untouched."""
     n_q, d_h = 2, 4
     q = M.bf16(rng.standard_normal((3, n_q, d_h)))
     k = M.bf16(rng.standard_normal((3, 1, d_h)))
     v = M.bf16(rng.standard_normal((3, 1, d_h)))
     pos = np.arange(3)
     exact = M.causal_gqa_attention(q, k, v, pos, pos)
-    with M.accumulate_in(np.float32):
+    with M.compute_in(np.float32):
         got = M.causal_gqa_attention(q, k, v, pos, pos)
     f32 = np.float32
+    sc = f32(1.0 / math.sqrt(d_h))
     for h in range(n_q):
         for i in range(3):
             s = []
@@ -157,29 +160,51 @@ def test_accumulate_in_float32_covers_attention_and_rmsnorm():
                 acc = f32(0)
                 for e in range(d_h):
                     acc = f32(acc + f32(q[i, h, e]) * f32(k[t, 0, e]))
-                s.append(float(acc) / math.sqrt(d_h))
-            w = [math.exp(a - max(s)) for a in s]
+                s.append(f32(acc * sc))
+            mx = max(s)
+            w = [np.exp(f32(a - mx)) for a in s]
             den = f32(0)
             for t in range(i + 1):
-                den = f32(den + f32(w[t]))
+                den = f32(den + w[t])
             for e in range(d_h):
                 num = f32(0)
                 for t in range(i + 1):
-                    num = f32(num + f32(w[t]) * f32(v[t, 0, e]))
-                np.testing.assert_allclose(got[i, h, e], float(num) / float(den), rtol=2e-6, atol=1e-7)
+                    num = f32(num + w[t] * f32(v[t, 0, e]))
+                np.testing.assert_allclose(got[i, h, e], float(f32(num / den)), rtol=2e-6, atol=1e-7)
     assert not np.array_equal(got, exact)
     np.testing.assert_allclose(got, exact, rtol=1e-5, atol=1e-6)
     assert np.array_equal(M.causal_gqa_attention(q, k, v, pos, pos), exact)   # switch restored
 
+
+def test_compute_in_float32_pointwise_ops():
+    """RMSNorm (mean of squares, reciprocal root, scaling), RoPE (float64 angles, float32
+    rotation), SiLU, the SwiGLU product and the residual add, each against a direct float32
+    evaluation, and untouched outside the switch."""
+    f32 = np.float32
     x = rng.standard_normal((4, 64)) * 0.3
     g = 1.0 + 0.1 * rng.standard_normal(64)
     ref = M.rms_norm(x, g, 1e-5)
-    with M.accumulate_in(np.float32):
+    with M.compute_in(np.float32):
         r32 = M.rms_norm(x, g, 1e-5)
-    ms32 = np.array([float(np.mean((row * row).astype(np.float32), dtype=np.float32)) for row in x])
-    np.testing.assert_allclose(r32, x / np.sqrt(ms32[:, None] + 1e-5) * g, rtol=1e-12)
+        xs = rng.standard_normal((3, 2, 8))
+        ro = M.rope(xs, np.array([0, 5, 1000]), 10000.0)
+        sl = M.silu(x)
+        sw = M.swiglu(x, x[::-1])
+        ra = M.residual_add(x, x * 1e-3)
+    xt = x.astype(f32)
+    ms = np.mean(xt * xt, axis=-1, keepdims=True, dtype=f32)
+    np.testing.assert_array_equal(r32, (xt * (f32(1) / np.sqrt(ms + f32(1e-5))) * g.astype(f32)).astype(np.float64))
     np.testing.assert_allclose(r32, ref, rtol=1e-6)
     assert np.array_equal(M.rms_norm(x, g, 1e-5), ref)
+    inv = np.power(10000.0, -2.0 * np.arange(4) / 8)
+    ang = np.array([0, 5, 1000])[:, None] * inv[None, :]
+    c, s_ = np.cos(ang).astype(f32)[:, None, :], np.sin(ang).astype(f32)[:, None, :]
+    a1, a2 = xs[..., :4].astype(f32), xs[..., 4:].astype(f32)
+    np.testing.assert_array_equal(ro, np.concatenate([a1 * c - a2 * s_, a2 * c + a1 * s_], axis=-1).astype(np.float64))
+    np.testing.assert_array_equal(sl, (xt / (f32(1) + np.exp(-xt))).astype(np.float64))
+    np.testing.assert_array_equal(sw, ((xt / (f32(1) + np.exp(-xt))) * x[::-1].astype(f32)).astype(np.float64))
+    np.testing.assert_array_equal(ra, (xt + (x * 1e-3).astype(f32)).astype(np.float64))
+    assert np.array_equal(M.silu(x), x / (1.0 + np.exp(-x)))
 
 
 def test_e4m3_matches_torch_float8_cast():
