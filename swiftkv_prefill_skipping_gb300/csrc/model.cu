@@ -7,8 +7,11 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <memory>
 #include <string>
 #include <vector>
+
+#include <nvtx3/nvToolsExt.h>
 
 #include "launch.h"
 #include "swiftkv.h"
@@ -65,6 +68,15 @@ struct Workspace {
 };
 
 constexpr int kShortChunk = 4;  // chunks up to this many rows take the single-row attention kernel
+
+// NVTX range over a host-side phase of a call (plan, layers 1..l, wide KV, tail, LM head,
+// decode): visible in a profiler timeline, a no-op without one.
+struct PhaseRange {
+  explicit PhaseRange(const char* name) { nvtxRangePushA(name); }
+  ~PhaseRange() { nvtxRangePop(); }
+  PhaseRange(const PhaseRange&) = delete;
+  PhaseRange& operator=(const PhaseRange&) = delete;
+};
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -1133,6 +1145,7 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   const double attn_bytes = tail_keys * kv_key_bytes + 2.0 * T * m->Nq * 2;
   const double tail_bytes = tail_keys * kv_key_bytes + 2.0 * P * m->Nq * 2;
   {
+  PhaseRange nv("swiftkv plan");
   Prof pr(m, s, "plan", 1 + (P + 1 + kBlobInts - 1) / kBlobInts + ((int)tiles.size() + kBlobInts - 1) / kBlobInts +
           (4 * m->C + kBlobInts - 1) / kBlobInts + (ctx ? (P + kBlobInts - 1) / kBlobInts : 0) +
           2 * (((int)srow.size() + kBlobInts - 1) / kBlobInts) +
@@ -1166,6 +1179,7 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
                           x.fused ? x.w.ss_mlp : nullptr, norm_tiles(c.d), s));
   }
   // layers 1..l in full for every prompt token
+  std::unique_ptr<PhaseRange> nv_layers(new PhaseRange("swiftkv layers 1..l"));
   for (int j = 0; j < m->l; ++j) {
     if (j > 0 && !x.fused) RET(norm(x, x.w.x, nullptr, T, m->layers[j].g_attn, x.w.u, nullptr));
     if (x.n_deq > 0) {
@@ -1179,8 +1193,13 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
     RET(layer_rest(x, j, T, x.w.x, x.w.q, x.w.attn, x.w.u, x.w.h, true, nullptr, (int)tiles.size(),
                    "gemm_layers", attn_flops, attn_bytes));
   }
+  nv_layers.reset();
   // caches of every skipped layer / AcrossKV group from x_l
-  if (m->G > 0) RET(wide_kv(x, T, x.w.x, x.w.u, x.w.positions, x.w.slots, x.fused));
+  if (m->G > 0) {
+    PhaseRange nv("swiftkv wide KV");
+    RET(wide_kv(x, T, x.w.x, x.w.u, x.w.positions, x.w.slots, x.fused));
+  }
+  std::unique_ptr<PhaseRange> nv_tail(new PhaseRange("swiftkv last-token tail"));
   // last prompt token of each sequence: layers l+1..L
   RET(norm(x, x.w.x, x.w.last_idx, P, m->l < c.L ? m->layers[m->l].g_attn : m->g_final, x.w.ut, x.w.xt));
   bool q_ready = false;  // the previous chained launch already computed this layer's Q
@@ -1201,6 +1220,8 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
       RET(r);
     }
   }
+  nv_tail.reset();
+  PhaseRange nv_lm("swiftkv LM head");
   EpiParams el = epi_base(x, EPI_STORE_F32, P, c.vocab);
   el.ldo = c.vocab;
   el.out_f32 = host_io ? x.w.logits : logits;
@@ -1243,6 +1264,7 @@ int swiftkv_decode_step(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   }
   cudaStream_t s = (cudaStream_t)stream;
   CK(cudaSetDevice(m->device));
+  PhaseRange nv("swiftkv decode step");
   Ctx x;
   x.m = m;
   x.s = s;
