@@ -8,7 +8,9 @@
 // TMEM, barriers and the K/V ring carried from item to item, so the next item's Q and K/V
 // loads and first S MMAs run while the softmax warps write the current item's output. 11 warps:
 //   warp 0      TMA: both Q tiles once (two 64-column halves each, 128B swizzle), then per
-//               64-key block the K and V rows of its four 16-token pages into a 4-stage ring
+//               64-key block the K and V rows of its four 16-token pages into a 4-stage ring;
+//               a block's page ids are read from the block table one block ahead of its
+//               copies, and the next item's Q is requested into L2 while the current item runs
 //   warps 1, 2  MMA issue for tile A and tile B (warp 1 also allocates all 512 TMEM columns):
 //               one lane issues, per block, S = Q K^T (M=128, N=64, K=128; double-buffered)
 //               ahead of O += P V (M=128, N=128, K=64, bf16 operands: P read from TMEM, where
@@ -172,9 +174,23 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
 
   if (warp == 0) {
     if (lane == 0) {
+      // Page ids of block j of item X, read from the block table one block ahead of that
+      // block's copies, so the reads' latency hides behind the copies of the block before
+      auto block_pages = [&](const Item& X, int j, int* pg) {
+#pragma unroll
+        for (int p = 0; p < BKV / kPageSize; ++p) {
+          const int key = j * BKV + p * kPageSize;
+          pg[p] = key < X.nk ? bt[(size_t)X.s * max_pages + (key >> 4)] : -1;
+        }
+      };
       int kv_i = 0;  // K/V blocks loaded so far (all items): ring stage and phase
       bool ok = true;
-      for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
+      bool have = item_at(0, tiles, n_items, n_q, cu, ctx, I);
+      int pg[BKV / kPageSize], pgn[BKV / kPageSize];
+#pragma unroll
+      for (int p = 0; p < BKV / kPageSize; ++p) pg[p] = pgn[p] = -1;
+      if (have) block_pages(I, 0, pg);
+      for (int it = 0; ok && have; ++it) {
         const int kvh = I.h / group;
         // Q of this item overwrites the previous item's, once its last S MMA has completed
         if (it > 0 && !mbar_wait(bar(ctl->q_empty), (uint32_t)((it - 1) & 1), abort_flag)) break;
@@ -187,9 +203,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
           tma_load_2d(sQ + t * Q_BYTES, &tmQ, I.h * D, row, bar(ctl->q_full));
           tma_load_2d(sQ + t * Q_BYTES + Q_BYTES / 2, &tmQ, I.h * D + 64, row, bar(ctl->q_full));
         }
+        Item N;
+        const bool have_next = item_at(it + 1, tiles, n_items, n_q, cu, ctx, N);
         for (int j = 0; j < I.nblk; ++j, ++kv_i) {
           const int stage = kv_i % KV_STAGES;
           const uint32_t phase = (uint32_t)((kv_i / KV_STAGES) & 1);
+          if (j + 1 < I.nblk) {
+            block_pages(I, j + 1, pgn);
+          } else if (have_next) {
+            block_pages(N, 0, pgn);
+          }
           if (!mbar_wait(bar(ctl->kv_empty[stage]), phase ^ 1, abort_flag)) {
             ok = false;
             break;
@@ -198,25 +221,37 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
           ctl->pending[stage] = (int)phase;
           const uint32_t sk = sKV + stage * STAGE_BYTES, sv = sk + K_BYTES;
 #pragma unroll
-          for (int pg = 0; pg < BKV / kPageSize; ++pg) {
-            const int key = j * BKV + pg * kPageSize;
-            int page = key < I.nk ? bt[(size_t)I.s * max_pages + (key >> 4)] : -1;
+          for (int p = 0; p < BKV / kPageSize; ++p) {
+            const int page = pg[p];
             const bool valid = page >= 0 && page < num_pages;
             // a page outside the pool reads rows past the tensor's end: TMA fills zeros
             const int row = valid ? (page * n_kv + kvh) * kPageSize : pool_rows;
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-              tma_load_2d(sk + hf * KV_HALF + pg * 2048, &tmK, hf * 64, row, bar(ctl->kv_full[stage]));
-              tma_load_2d(sv + hf * KV_HALF + pg * 2048, &tmV, hf * 64, row, bar(ctl->kv_full[stage]));
+              tma_load_2d(sk + hf * KV_HALF + p * 2048, &tmK, hf * 64, row, bar(ctl->kv_full[stage]));
+              tma_load_2d(sv + hf * KV_HALF + p * 2048, &tmV, hf * 64, row, bar(ctl->kv_full[stage]));
             }
             if (fp8) {  // the page's 16 key and 16 value scales (page 0's for a page outside the pool)
               const size_t srow = valid ? (size_t)row : (size_t)kvh * kPageSize;
-              const uint32_t ss = sScale + stage * SCALE_BYTES + pg * kPageSize * 4;
+              const uint32_t ss = sScale + stage * SCALE_BYTES + p * kPageSize * 4;
               bulk_load(ss, kscale + srow, kPageSize * 4, bar(ctl->kv_full[stage]));
               bulk_load(ss + BKV * 4, vscale + srow, kPageSize * 4, bar(ctl->kv_full[stage]));
             }
           }
+#pragma unroll
+          for (int p = 0; p < BKV / kPageSize; ++p) pg[p] = pgn[p];
+          // the next item's Q into L2 while this item runs, so its load after q_empty is short
+          // (after the second block, by when the next item's descriptor reads have returned)
+          if (j == min(1, I.nblk - 1) && have_next) {
+            for (int t = 0; t < (N.has_b ? 2 : 1); ++t) {
+              const int row = N.seq0 + (t ? N.q0b : N.q0a);
+              tma_prefetch_l2_2d(&tmQ, N.h * D, row);
+              tma_prefetch_l2_2d(&tmQ, N.h * D + 64, row);
+            }
+          }
         }
+        I = N;
+        have = have_next;
       }
     }
   } else if (warp == 1 || warp == 2) {
