@@ -19,6 +19,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tc_common.cuh"
@@ -279,10 +281,42 @@ struct CtrlPair {
 constexpr int P_SMEM_BYTES = 1024 + P_STAGES * P_STAGE_BYTES + (int)sizeof(CtrlPair);
 constexpr uint32_t IDESC_PAIR = tc::make_idesc(2 * BM, BN, false, false);
 
+// Unit order of the 2-SM kernel, `order` = group << 1 | by_n. by_n = 0: groups of `group`
+// 256-row units, the row index running fastest, each group sweeping every weight tile while
+// its activation panels stay in L2. by_n = 1: groups of `group` weight tiles, the weight index
+// running fastest, each group sweeping every 256-row unit while its weight panels stay in L2.
+__device__ __forceinline__ void unit_coords(int u, int m_units, int n_tiles, int order, int& mu, int& nt) {
+  const int group = order >> 1;
+  if (!(order & 1)) {
+    const int per = group * n_tiles, g = u / per, r = u - g * per;
+    const int gm = min(group, m_units - g * group);
+    mu = g * group + r % gm;
+    nt = r / gm;
+  } else {
+    const int per = group * m_units, g = u / per, r = u - g * per;
+    const int gn = min(group, n_tiles - g * group);
+    nt = g * group + r % gn;
+    mu = r / gn;
+  }
+}
+
+// Unit order per GEMM shape, chosen from DRAM traffic measured (ncu, one layer of the
+// Llama-3.1-8B shape, 11 703 rows) over group kinds and sizes: reads per launch went from
+// 455 to 356 MB for O (N = 4096) and from 2 246 to 1 666 MB for down (K = 14 336); row groups
+// of 16 stayed best for QKV and gate/up, where larger and smaller groups both read more.
+//   K > 8192 (panels over 4 MB): groups of 8 weight tiles, activation panels swept per group;
+//   otherwise, at most 16 weight tiles: one group of all of them;
+//   otherwise: groups of 256-row units holding about 32 MB of activation panels (4 to 16).
+static int pair_order(int m_units, int n_tiles, int K) {
+  if (K > 8192) return (std::min(8, n_tiles) << 1) | 1;
+  if (n_tiles <= 16) return (n_tiles << 1) | 1;
+  const int g = std::min(16, std::max(4, (int)(32e6 / (512.0 * K))));
+  return std::min(g, m_units) << 1;
+}
 
 __global__ void __launch_bounds__(THREADS, 1) gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                                                                   const __grid_constant__ CUtensorMap tmB,
-                                                                  EpiParams ep, int K, int* status) {
+                                                                  EpiParams ep, int K, int order, int* status) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -338,7 +372,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_pair_kernel(const __grid_c
       uint32_t phase = 0;
       for (int u = first_unit; u < num_units && !*abort_flag; u += unit_stride) {
         int mu, nt;
-        tile_coords(u, m_units, n_tiles, mu, nt);
+        unit_coords(u, m_units, n_tiles, order, mu, nt);
         const int mt = mu * 2 + crank;
         for (int kb = 0; kb < kblocks; ++kb) {
           if (!mbar_wait(empty(stage), phase ^ 1, abort_flag)) break;
@@ -397,7 +431,7 @@ __global__ void __launch_bounds__(THREADS, 1) gemm_tc_pair_kernel(const __grid_c
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       int mu, nt;
-      tile_coords(u, m_units, n_tiles, mu, nt);
+      unit_coords(u, m_units, n_tiles, order, mu, nt);
       const int mt = mu * 2 + crank;
       if (!mbar_wait(tfull(acc), aph, abort_flag)) break;
       tc_fence_after();
@@ -484,7 +518,9 @@ static cudaError_t launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, 
     if (e != cudaSuccess) return e;
   }
   const int m_units = ((ep.M + BM - 1) / BM + 1) / 2;
-  const int units = m_units * ((ep.N + BN - 1) / BN);
+  const int n_tiles = (ep.N + BN - 1) / BN;
+  const int units = m_units * n_tiles;
+  const int order = pair_order(m_units, n_tiles, K);
   const int clusters = units < num_sms / 2 ? units : num_sms / 2;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(clusters * 2);
@@ -498,7 +534,7 @@ static cudaError_t launch_tc_pair(const CUtensorMap& ta, const CUtensorMap& tb, 
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, ta, tb, ep, K, status);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_pair_kernel, ta, tb, ep, K, order, status);
 }
 
 cudaError_t launch_gemm_tc(const bf16* A, int lda, const bf16* B, int K, const EpiParams& ep, int num_sms,
