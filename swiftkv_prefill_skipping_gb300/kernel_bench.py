@@ -103,7 +103,8 @@ def decode(args):
     import synth
     from swiftkv_prefill_skipping_gb300 import api, binding
     shape = dataclasses.replace(synth.QWEN14B, L=args.layers, name=f"qwen2.5-14b-width-{args.layers}layers")
-    batch = synth.prompt_batch(shape.vocab, args.batch, args.ctx, args.ctx, reserve_tokens=args.warmup + args.iters)
+    batch = synth.prompt_batch(shape.vocab, args.batch, args.ctx, args.ctx,
+                               reserve_tokens=args.warmup + 2 * args.iters)  # timed and profiled passes
     m = api.load_synthetic(shape, args.l, args.g)
     binding.check(binding.lib().swiftkv_set_rows_impl(m.handle, args.rows_impl))
     kv = api.KVCache(m, batch.num_pages, batch.block_table, dtype=args.kv)
