@@ -136,7 +136,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) gemv_chain_kernel(const __grid_
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       // A slices not yet requested: (stage, phase, k step), in issue order
-      int pq_stage[CH_MAX_STAGES], pq_phase[CH_MAX_STAGES], pq_kt[CH_MAX_STAGES];
+      int pq_stage[CH_MAX_STAGES] = {}, pq_phase[CH_MAX_STAGES] = {}, pq_kt[CH_MAX_STAGES] = {};
       int pq_head = 0, pq_n = 0;
       int ready = -1;  // highest phase whose inputs are complete
       auto load_a = [&](int st, int p, int kt) {
