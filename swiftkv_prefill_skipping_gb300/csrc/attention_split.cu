@@ -7,9 +7,9 @@
 // own length only, so no row's arithmetic depends on the batch. One CTA of 4 warps per SM; each warp walks its
 // own items (v = global warp, + all warps, ...) one 16-key page at a time. Each (page, KV
 // head) block is 16*d_head*2 contiguous bytes in the pool; the warp stages K and V (and,
-// with an item's first page, its G query rows) with cp.async into a 2-slot ring of
+// with an item's first page, its G query rows) with cp.async into a 3-slot ring of
 // XOR-swizzled shared-memory tiles that runs ahead across item boundaries, so HBM reads
-// stay in flight while it computes (8 warps per SM). The G = n_q/n_kv <= 8 query heads of
+// stay in flight while it computes (7 warps per SM). The G = n_q/n_kv <= 8 query heads of
 // the group are rows of an mma.sync m16n8k16 A operand (the other rows are zero), so one
 // read of each K/V row serves the whole group: S = Q K^T (bf16, fp32 accumulate), online
 // softmax in the log2 domain (O rescaled only when a row's running max moves), O += P V
@@ -30,8 +30,8 @@ namespace skv {
 
 namespace {
 
-constexpr int SW = 8;        // warps per CTA (one CTA per SM)
-constexpr int SSTAGES = 2;   // ring slots per warp
+constexpr int SW = 7;        // warps per CTA (one CTA per SM; 3 ring slots of 10 KB each fit 7)
+constexpr int SSTAGES = 3;   // ring slots per warp
 constexpr int SMAXG = 8;     // query heads per KV head (rows 0..7 of the mma A operand)
 
 template <int D>
