@@ -1,9 +1,13 @@
 // Varlen causal GQA flash attention on tcgen05 (sm_103a), d_head = 128, two 128-row query
 // tiles per CTA sharing every K/V block, reading K/V straight out of the paged cache.
 //
-// Work item = query rows [256p, 256p + 256) of one prompt chunk x one query head: tile A the
-// first 128 rows, tile B the next 128 (absent past the chunk's end). A chunk may follow ctx
-// cached tokens: its rows sit at positions ctx.. and see keys [0, ctx + row]. Persistent: one
+// Work item: two 128-row query tiles that share every K/V block. With an even number of query
+// heads per KV head (head_pairs), tile A and tile B are the same 128 rows [128p, 128p + 128) of
+// one prompt chunk for two query heads of one KV head, so both need the same key blocks and
+// finish together; otherwise tile A is rows [256p, 256p + 128) of one query head and tile B the
+// next 128 rows (absent past the chunk's end), and tile A needs up to two fewer key blocks.
+// A chunk may follow ctx cached tokens: its rows sit at positions ctx.. and see keys
+// [0, ctx + row]. Persistent: one
 // CTA per SM walks its share of the items (heaviest first, alternate rounds reversed) with
 // TMEM, barriers and the K/V ring carried from item to item, so the next item's Q and K/V
 // loads and first S MMAs run while the softmax warps write the current item's output. 11 warps:
@@ -82,22 +86,27 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 constexpr uint32_t IDESC_S = make_idesc(BQ, BKV, false, false);  // Q (K-major) x K (K-major)
 constexpr uint32_t IDESC_O = make_idesc(BQ, D, false, true);  // P (TMEM) x V (MN-major), bf16
 
-// One work item: query rows [256p, 256p + 256) of one chunk x one query head.
+// One work item: tile A (query head h, rows q0a..) and tile B (head hb, rows q0b..) of one chunk.
 struct Item {
-  int s, h, seq0, n, c0, nk, q0a, q0b, nblk_a, nblk_b, nblk;
+  int s, h, hb, seq0, n, c0, nk, q0a, q0b, nblk_a, nblk_b, nblk;
   bool has_b;
 };
 
-// This CTA's it-th item. Items are (tile, head) pairs, tile-major over the tile list (which is
-// sorted heaviest first); CTA c takes item c of every round of gridDim.x items, counted from
-// the other end in odd rounds, so every CTA gets a similar total. False past the last item.
+// This CTA's it-th item. Items are (tile, head) or (tile, head pair) pairs, tile-major over the
+// tile list (sorted heaviest first), so consecutive items share their K/V rows in L2; CTA c
+// takes item c of every round of gridDim.x items, counted from the other end in odd rounds, so
+// every CTA gets a similar total. False past the last item.
 __device__ __forceinline__ bool item_at(int it, const int* __restrict__ tiles, int n_items, int n_q,
-                                        const int* __restrict__ cu, const int* __restrict__ ctx, Item& I) {
+                                        const int* __restrict__ cu, const int* __restrict__ ctx, Item& I,
+                                        bool head_pairs) {
   const int G = gridDim.x, c = blockIdx.x;
   const long long w = (long long)it * G + ((it & 1) ? (G - 1 - c) : c);
   if (w >= n_items) return false;
-  const int tile = tiles[w / n_q];
-  I.h = (int)(w % n_q);
+  // head_pairs: items are (128-row tile, two query heads of one KV head), both tiles on the
+  // same rows; else (256-row tile pair, one query head)
+  const int per = head_pairs ? n_q / 2 : n_q;
+  const int tile = tiles[w / per];
+  const int k = (int)(w % per);
   I.s = tile >> 16;
   const int qp = tile & 0xffff;
   I.seq0 = cu[I.s];
@@ -105,9 +114,17 @@ __device__ __forceinline__ bool item_at(int it, const int* __restrict__ tiles, i
   // the chunk's rows sit at positions c0.. after c0 cached keys; keys [0, nk) are visible
   I.c0 = ctx ? ctx[I.s] : 0;
   I.nk = I.c0 + I.n;
-  I.q0a = qp * 2 * BQ;
-  I.q0b = I.q0a + BQ;
-  I.has_b = I.q0b < I.n;
+  if (head_pairs) {
+    I.h = 2 * k;
+    I.hb = 2 * k + 1;
+    I.q0a = I.q0b = qp * BQ;
+    I.has_b = true;
+  } else {
+    I.h = I.hb = k;
+    I.q0a = qp * 2 * BQ;
+    I.q0b = I.q0a + BQ;
+    I.has_b = I.q0b < I.n;
+  }
   I.nblk_a = (min(I.nk, I.c0 + I.q0a + BQ) + BKV - 1) / BKV;
   I.nblk_b = I.has_b ? (min(I.nk, I.c0 + I.q0b + BQ) + BKV - 1) / BKV : 0;
   I.nblk = I.has_b ? I.nblk_b : I.nblk_a;  // blocks loaded (tile B's range covers tile A's)
@@ -119,7 +136,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
     const __grid_constant__ CUtensorMap tmV, const float* __restrict__ kscale, const float* __restrict__ vscale,
     const int* __restrict__ bt, int max_pages, int num_pages, const int* __restrict__ cu,
     const int* __restrict__ ctx, const int* __restrict__ tiles, int n_items, int n_q, int n_kv,
-    bf16* __restrict__ out, int ldo, float scale_log2, int* status) {
+    bf16* __restrict__ out, int ldo, float scale_log2, int* status, bool head_pairs) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   unsigned char* smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -185,7 +202,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
       };
       int kv_i = 0;  // K/V blocks loaded so far (all items): ring stage and phase
       bool ok = true;
-      bool have = item_at(0, tiles, n_items, n_q, cu, ctx, I);
+      bool have = item_at(0, tiles, n_items, n_q, cu, ctx, I, head_pairs);
       int pg[BKV / kPageSize], pgn[BKV / kPageSize];
 #pragma unroll
       for (int p = 0; p < BKV / kPageSize; ++p) pg[p] = pgn[p] = -1;
@@ -200,11 +217,12 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
         ctl->pending[KV_STAGES] = it & 1;
         for (int t = 0; t < (I.has_b ? 2 : 1); ++t) {
           const int row = I.seq0 + (t ? I.q0b : I.q0a);
-          tma_load_2d(sQ + t * Q_BYTES, &tmQ, I.h * D, row, bar(ctl->q_full));
-          tma_load_2d(sQ + t * Q_BYTES + Q_BYTES / 2, &tmQ, I.h * D + 64, row, bar(ctl->q_full));
+          const int hq = t ? I.hb : I.h;
+          tma_load_2d(sQ + t * Q_BYTES, &tmQ, hq * D, row, bar(ctl->q_full));
+          tma_load_2d(sQ + t * Q_BYTES + Q_BYTES / 2, &tmQ, hq * D + 64, row, bar(ctl->q_full));
         }
         Item N;
-        const bool have_next = item_at(it + 1, tiles, n_items, n_q, cu, ctx, N);
+        const bool have_next = item_at(it + 1, tiles, n_items, n_q, cu, ctx, N, head_pairs);
         for (int j = 0; j < I.nblk; ++j, ++kv_i) {
           const int stage = kv_i % KV_STAGES;
           const uint32_t phase = (uint32_t)((kv_i / KV_STAGES) & 1);
@@ -245,8 +263,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
           if (j == min(1, I.nblk - 1) && have_next) {
             for (int t = 0; t < (N.has_b ? 2 : 1); ++t) {
               const int row = N.seq0 + (t ? N.q0b : N.q0a);
-              tma_prefetch_l2_2d(&tmQ, N.h * D, row);
-              tma_prefetch_l2_2d(&tmQ, N.h * D + 64, row);
+              const int hq = t ? N.hb : N.h;
+              tma_prefetch_l2_2d(&tmQ, hq * D, row);
+              tma_prefetch_l2_2d(&tmQ, hq * D + 64, row);
             }
           }
         }
@@ -261,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
       const int t = warp - 1;
       int kv_base = 0, sp = 0, oi = 0;
       bool ok = true;
-      for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); ++it) {
+      for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I, head_pairs); ++it) {
         const int nb = t ? I.nblk_b : I.nblk_a;  // blocks this tile reads (0: no tile B)
         // Releases block j's K/V stage for a block this tile does not read. The arrival counts
         // toward that block's phase only once the block has been loaded (kv_full), so it can
@@ -360,7 +379,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
     int sp = 0;   // S/P blocks of this tile over all items
     int kvb = 0;  // K/V blocks over all items (ring stage of block j: (kvb + j) % KV_STAGES)
     bool ok = true;
-    for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I); kvb += I.nblk, ++it) {
+    for (int it = 0; ok && item_at(it, tiles, n_items, n_q, cu, ctx, I, head_pairs); kvb += I.nblk, ++it) {
       if (t == 1 && !I.has_b) continue;
       const int nb = t ? I.nblk_b : I.nblk_a;
       const int q0 = t ? I.q0b : I.q0a;
@@ -458,7 +477,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_tc2_kernel(
       if (ok) {
         tc_fence_after();
         const float inv = 1.f / l;
-        bf16* dst = out + (size_t)(I.seq0 + min(qrow, I.n - 1)) * ldo + I.h * D;
+        bf16* dst = out + (size_t)(I.seq0 + min(qrow, I.n - 1)) * ldo + (t ? I.hb : I.h) * D;
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           float v[32];
@@ -517,7 +536,7 @@ cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf
                                          const int* block_table, int max_pages, int num_pages, const int* cu,
                                          const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
                                          int d_head, bf16* out, int ldo, int num_sms, int* status,
-                                         cudaStream_t stream) {
+                                         cudaStream_t stream, bool head_pairs) {
   if (num_tiles <= 0) return cudaSuccess;
   if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8 || num_sms < 1 || (!k_scale != !v_scale) ||
       (reinterpret_cast<uintptr_t>(k_scale) & 15) || (reinterpret_cast<uintptr_t>(v_scale) & 15))
@@ -534,10 +553,10 @@ cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf
     if (e != cudaSuccess) return e;
   }
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)D);
-  const int n_items = num_tiles * n_q;
+  const int n_items = num_tiles * (head_pairs ? n_q / 2 : n_q);
   attn_tc2_kernel<<<n_items < num_sms ? n_items : num_sms, THREADS, SMEM_BYTES, stream>>>(
       mq, mk, mv, k_scale, v_scale, block_table, max_pages, num_pages, cu, ctx, tiles, n_items, n_q, n_kv, out, ldo,
-      scale_log2, status);
+      scale_log2, status, head_pairs);
   return cudaGetLastError();
 }
 

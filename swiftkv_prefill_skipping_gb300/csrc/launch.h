@@ -154,13 +154,15 @@ cudaError_t launch_attention_prefill(const bf16* q, int ldq, const bf16* k_pool,
                                      const int* cu, const int* ctx, const int* tiles, int num_tiles, int n_q,
                                      int n_kv, int d_head, bf16* out, int ldo, cudaStream_t stream);
 // Same on tcgen05 with two 128-row query tiles per CTA sharing every K/V block (d_head 128
-// only); tiles are 256-row tile pairs (seq << 16 | pair), heaviest first. Persistent: at most
-// num_sms CTAs, each walking its share of the (tile pair, head) items.
+// only), heaviest tiles first. head_pairs (n_q / n_kv even): tiles are 128-row tiles
+// (seq << 16 | tile) and an item is one tile for two query heads of one KV head; otherwise
+// tiles are 256-row tile pairs (seq << 16 | pair) and an item is one pair for one head.
+// Persistent: at most num_sms CTAs, each walking its share of the items.
 cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,
                                          const float* k_scale, const float* v_scale, const int* block_table, int max_pages, int num_pages, const int* cu,
                                          const int* ctx, const int* tiles, int num_tiles, int n_q, int n_kv,
                                          int d_head, bf16* out, int ldo, int num_sms, int* status,
-                                         cudaStream_t stream);
+                                         cudaStream_t stream, bool head_pairs);
 // Same on tcgen05 (d_head 128 only; cudaErrorNotSupported otherwise). tiles are 128-row tiles;
 // T = rows of q. status receives kStatusTimeout if a bounded wait expires.
 cudaError_t launch_attention_prefill_tc(const bf16* q, int ldq, int T, const bf16* k_pool, const bf16* v_pool,

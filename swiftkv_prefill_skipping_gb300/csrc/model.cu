@@ -494,7 +494,7 @@ int layer_rest(Ctx& x, int j, int M, float* xres, bf16* qb, bf16* ab, bf16* ub, 
   if (prefill && x.tc_attn && m->attn_impl == 0)
     e = launch_attention_prefill_tc2(qb, m->Nq, M, tkp, tvp, tks, tvs, x.kv->block_table, x.kv->max_pages_per_seq,
                                      x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
-                                     m->Nq, m->num_sms, m->status, x.s);
+                                     m->Nq, m->num_sms, m->status, x.s, (c.n_q / c.n_kv) % 2 == 0);
   else if (prefill && x.tc_attn)
     e = launch_attention_prefill_tc(qb, m->Nq, M, tkp, tvp, tks, tvs, x.kv->block_table, x.kv->max_pages_per_seq,
                                     x.kv->num_pages, x.w.cu, x.ctx, x.w.tiles, ntiles, c.n_q, c.n_kv, c.d_head, ab,
@@ -1071,7 +1071,10 @@ static int prefill_impl(swiftkv_model* m, const int32_t* tokens, const int32_t* 
   CK(cudaSetDevice(m->device));
 
   const bool tc_attn = m->attn_impl != 1 && m->cfg.d_head == 128;
-  const int tile_rows = tc_attn ? (m->attn_impl == 0 ? 256 : 128) : 64;
+  // the default tcgen05 attention pairs two query heads of one KV head on 128-row tiles when
+  // the group size is even, else two 128-row tiles of one head (256-row tile pairs)
+  const bool head_pairs = tc_attn && m->attn_impl == 0 && (m->cfg.n_q / m->cfg.n_kv) % 2 == 0;
+  const int tile_rows = tc_attn ? (m->attn_impl == 0 && !head_pairs ? 256 : 128) : 64;
   // Chunks of at most kShortChunk rows (decode tokens) are attended one row at a time by
   // the GQA-grouped single-row kernel: a 128-row query tile would be nearly empty and its CTA
   // per query head would read the sequence's keys once per head. The rest go in query
