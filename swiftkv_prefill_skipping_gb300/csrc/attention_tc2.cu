@@ -30,8 +30,8 @@
 //               tcgen05.st over the S columns it came from), then O / l from TMEM to global
 //               memory.
 // While one tile's softmax warps work, the tensor core runs the other tile's MMAs, and each
-// K/V block is loaded once for 256 query rows. Tile A needs up to 128 fewer keys than tile B;
-// its last blocks are skipped. An S buffer is refilled only after the P V that read the P
+// K/V block is loaded once for both tiles. Where tile A needs fewer keys than tile B (row
+// pairs), its last blocks are skipped. An S buffer is refilled only after the P V that read the P
 // stored over it has completed. Between items, Q is reloaded once the last S MMA of the item
 // has completed (q_empty), and a tile's first P V of the next item waits until its O has been
 // read out of TMEM (o_empty). FP8 cache: the K/V pools hold the e4m3 codes as (exact) bf16

@@ -289,7 +289,7 @@ struct Ctx {
   const swiftkv_kv_pages* kv;
   bf16* const* k_dev;  // device arrays of pool pointers
   bf16* const* v_dev;
-  bool tc_attn = false;  // prefill attention on tcgen05 (attn_impl 0: 256-row tile pairs, 2: 128-row tiles)
+  bool tc_attn = false;  // prefill attention on tcgen05 (attn_impl 0: two tiles per item, 2: one 128-row tile)
   const int* ctx = nullptr;  // device [P]: cached tokens before each chunk (nullptr: none)
   int nshort = 0;            // rows of short chunks, attended one row at a time (w.srow / w.sseq)
   SplitPlan sp_short{};      // key-split plan of those rows
