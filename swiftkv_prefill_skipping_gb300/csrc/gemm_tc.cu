@@ -306,11 +306,12 @@ __device__ __forceinline__ void unit_coords(int u, int m_units, int n_tiles, int
 // of 16 stayed best for QKV and gate/up, where larger and smaller groups both read more.
 //   K > 8192 (panels over 4 MB): groups of 8 weight tiles, activation panels swept per group;
 //   otherwise, at most 16 weight tiles: one group of all of them;
-//   otherwise: groups of 256-row units holding about 32 MB of activation panels (4 to 16).
+//   otherwise: groups of 256-row units holding 32 MiB of activation panels (16 at K = 4096,
+//   between 4 and 16).
 static int pair_order(int m_units, int n_tiles, int K) {
   if (K > 8192) return (std::min(8, n_tiles) << 1) | 1;
   if (n_tiles <= 16) return (n_tiles << 1) | 1;
-  const int g = std::min(16, std::max(4, (int)(32e6 / (512.0 * K))));
+  const int g = std::min(16, std::max(4, (32 << 20) / (512 * K)));
   return std::min(g, m_units) << 1;
 }
 
