@@ -268,6 +268,8 @@ int swiftkv_set_attention_impl(swiftkv_model* m, int impl);
  *   5 = skinny, one CTA per pair of 16-column strips over the whole K (M <= 64),
  *   6 = skinny, persistent, TMA-fed, 64-row weight tiles over the whole K (M <= 64 and
  *       N / 64 >= SMs / 2, else SWIFTKV_EUNSUPPORTED)
+ *   7 = impl 6's kernel and tiles with the residual epilogue of the decode rows' O and
+ *       down projections: C += A * B^T on the C passed in
  *   status  device int or NULL: receives SWIFTKV_STATUS_TIMEOUT if a bounded wait expired
  * Requires K % 64 == 0 and N % 128 == 0. */
 int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,

@@ -957,7 +957,7 @@ int swiftkv_set_attention_impl(swiftkv_model* m, int impl) {
 int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int K, int impl, int* status,
                       swiftkv_stream stream) {
   if (!A || !B || !C || M < 1 || N < 1 || K < 1) return fail(SWIFTKV_EINVAL, "bad gemm arguments");
-  if (impl < 0 || impl > 6 || impl == 3) return fail(SWIFTKV_EINVAL, "gemm impl %d", impl);
+  if (impl < 0 || impl > 7 || impl == 3) return fail(SWIFTKV_EINVAL, "gemm impl %d", impl);
   if (K % 64 || N % 128) return fail(SWIFTKV_EUNSUPPORTED, "gemm needs K %% 64 == 0 and N %% 128 == 0");
   cudaStream_t s = (cudaStream_t)stream;
   int dev = 0, sms = 0;
@@ -986,7 +986,8 @@ int swiftkv_gemm_bf16(const void* A, const void* B, float* C, int M, int N, int 
     e = launch_gemm_tiled(a, K, b, K, ep, s);
   } else if (impl == 5) {
     e = M > 64 ? cudaErrorNotSupported : launch_gemv(a, K, b, K, ep, s);
-  } else if (impl == 6) {
+  } else if (impl == 6 || impl == 7) {
+    if (impl == 7) ep.kind = EPI_RESID;  // C += A * B^T: the decode rows' O and down epilogue
     e = M > 64 ? cudaErrorNotSupported : launch_gemv_tma(a, K, b, K, ep, sms, st, s);
   } else if (impl == 2) {
     if (M > 64) e = cudaErrorNotSupported;

@@ -52,6 +52,34 @@ def test_skinny_gemm_matches_torch_fp32(M, N, K):
     assert err < 2e-5, (M, N, K, err)
 
 
+@pytest.mark.parametrize("M,N,K", [(24, 5120, 5120), (24, 5120, 13824), (16, 4096, 4096), (16, 8192, 1024),
+                                   (64, 5120, 512), (1, 5120, 256)])
+def test_residual_skinny_gemm_adds_the_impl6_product(M, N, K):
+    """impl 7 (C += A B^T, the decode rows' O and down epilogue) runs impl 6's kernel and
+    tiles with the residual epilogue: every column is accumulated over K in the same order,
+    so the result equals C0 plus impl 6's product bit for bit, and matches the fp32
+    reference. 64-row and 32-row weight tiles, M from 1 to 64."""
+    import torch
+    from swiftkv_prefill_skipping_gb300 import binding as B
+    g = torch.Generator(device="cuda").manual_seed(M * 7 + N + K)
+    A = (torch.randn(M, K, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    W = (torch.randn(N, K, device="cuda", generator=g) * 0.5).to(torch.bfloat16)
+    C0 = torch.randn(M, N, device="cuda", generator=g)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    prod = torch.full((M, N), float("nan"), device="cuda")
+    B.check(B.lib().swiftkv_gemm_bf16(A.data_ptr(), W.data_ptr(), prod.data_ptr(), M, N, K, 6, st.data_ptr(), stream))
+    acc = C0.clone()
+    B.check(B.lib().swiftkv_gemm_bf16(A.data_ptr(), W.data_ptr(), acc.data_ptr(), M, N, K, 7, st.data_ptr(), stream))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(acc, C0 + prod)
+    torch.backends.cuda.matmul.allow_tf32 = False
+    ref = A.float() @ W.float().T
+    err = ((acc - C0) - ref).abs().max().item() / ref.abs().max().item()
+    assert err < 2e-5, (M, N, K, err)
+
+
 def test_tcgen05_is_deterministic():
     import torch
     c1, _ = _run(0, 777, 1024, 1024, seed=3)
