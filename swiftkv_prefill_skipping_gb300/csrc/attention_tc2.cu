@@ -538,6 +538,8 @@ cudaError_t launch_attention_prefill_tc2(const bf16* q, int ldq, int T, const bf
                                          int d_head, bf16* out, int ldo, int num_sms, int* status,
                                          cudaStream_t stream, bool head_pairs) {
   if (num_tiles <= 0) return cudaSuccess;
+  // a head pair shares its KV head only when the group size is even
+  if (head_pairs && (n_kv < 1 || n_q % n_kv || (n_q / n_kv) % 2)) return cudaErrorNotSupported;
   if (d_head != D || (reinterpret_cast<uintptr_t>(q) & 15) || ldq % 8 || num_sms < 1 || (!k_scale != !v_scale) ||
       (reinterpret_cast<uintptr_t>(k_scale) & 15) || (reinterpret_cast<uintptr_t>(v_scale) & 15))
     return cudaErrorNotSupported;
